@@ -1,0 +1,186 @@
+/*
+ * moe_route.h -- C ABI of the routed-expert MoE layer for GB300 (sm_103a).
+ *
+ * One Mixture-of-Experts FFN layer that reads only the weights of the experts
+ * each token is routed to:
+ *
+ *   router   logits = x . Wr^T + bias, fp32 softmax, top-k (lowest index first
+ *            among equal probabilities), weights renormalised over the k
+ *            (lilting.ch "observing the Qwen MoE router", section "hooking the
+ *            router": gate -> softmax(precise) -> top-k indices)
+ *   experts  for every routed (token t, slot r) with e = idx[t][r]:
+ *              h = silu(Gate_e x_t) * (Up_e x_t),   o = Down_e h
+ *            y[t] = sum_r w[t][r] * o_{t,r}, summed over r in a fixed order
+ *            (Qiita "custom Metal gather_qmm": section 4, routing indices are an
+ *            input of the kernel and unrouted experts are never fetched;
+ *            section 7, gate/up share x, down takes each slot's own activation)
+ *   weights  symmetric int8 or int4 codes with one scale per block of 32
+ *            consecutive input elements ("sym8", same write-up, section 6),
+ *            stacked as [E][rows][cols] with cols contiguous (the MLX
+ *            (num_experts, output_dims, input_dims) layout of the lilting.ch
+ *            article, section "warm-up vs mmap cache")
+ *
+ * Conventions for every entry point:
+ *  - All array arguments are DEVICE pointers owned by the caller; descriptor
+ *    structs are host memory read during the call only. The library allocates
+ *    nothing and keeps no state between calls; it is reentrant as long as two
+ *    concurrent calls do not share a workspace.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued asynchronously; outputs are valid once the stream reaches
+ *    them. Launches use programmatic dependent launch between the library's
+ *    own kernels, so they can be captured into a CUDA graph.
+ *  - Synchronous argument checks return MOE_ERR_INVALID_ARG / MOE_ERR_WORKSPACE
+ *    / MOE_ERR_UNSUPPORTED before anything is launched. A failed launch returns
+ *    MOE_ERR_CUDA. Problems found on the device (an expert id outside [0, E))
+ *    are written to the workspace's status word -- the offending access is
+ *    skipped, never performed -- and are read back by moe_check_status().
+ *  - Workspace: `ws_bytes` >= moe_workspace_bytes(op, ...). It must be zeroed
+ *    once before its first use (cudaMemset); the library leaves its counters at
+ *    zero after every call.
+ *  - Alignment: every pointer 16-byte aligned; D and F multiples of 32, so
+ *    every int8 row (D or F bytes) and int4 row (D/2 or F/2 bytes) starts on a
+ *    16-byte boundary.
+ *  - No exception crosses this boundary.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,    /* valid but not implemented combination */
+    MOE_ERR_CUDA = 3,           /* a CUDA launch or copy failed */
+    MOE_ERR_BAD_INDEX = 4,      /* device: expert id outside [0, E) (access skipped) */
+    MOE_ERR_DEVICE_TIMEOUT = 5, /* device: a bounded wait ran out */
+    MOE_ERR_WORKSPACE = 6       /* workspace missing or too small */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_F16 = 2 } moe_dtype_t;
+
+typedef enum {
+    MOE_Q_INT8_SYM_B32 = 0, /* int8 codes in [-127, 127], one scale per 32 codes */
+    MOE_Q_INT4_SYM_B32 = 1  /* int4 codes in [-7, 7], two per byte: element 2j in the
+                               low nibble of byte j, 2j+1 in the high nibble */
+} moe_qfmt_t;
+
+/* Router of one layer. W is [E][D] in w_dtype (MOE_F32 or MOE_BF16), D contiguous.
+ * bias is [E] fp32 or NULL. norm_topk = 1 renormalises the k chosen
+ * probabilities to sum to 1, 0 returns them as they are. */
+typedef struct {
+    int E, D, k;
+    moe_dtype_t w_dtype;
+    const void* W;
+    const float* bias;
+    int norm_topk;
+} moe_router_t;
+
+/* Experts of one layer, all [E][rows][cols] with cols contiguous:
+ *   gate_q, up_q  [E][F][D]   (int4: [E][F][D/2] bytes)     gate_s, up_s [E][F][D/32]
+ *   down_q        [E][D][F]   (int4: [E][D][F/2] bytes)     down_s       [E][D][F/32]
+ * scales in s_dtype (MOE_F32 or MOE_F16). */
+typedef struct {
+    int E, D, F;
+    moe_qfmt_t q;
+    moe_dtype_t s_dtype;
+    const void *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
+} moe_experts_t;
+
+/* Operation ids for moe_workspace_bytes. */
+enum { MOE_OP_ROUTE = 0, MOE_OP_DECODE = 1, MOE_OP_LAYER = 2, MOE_OP_PREFILL = 3 };
+
+/*
+ * Bytes of workspace an operation needs for T tokens (T >= 1). Returns 0 for an
+ * invalid combination.
+ */
+size_t moe_workspace_bytes(int op, int T, int k, int E, int D, int F);
+
+/*
+ * Router: logits, fp32 softmax and top-k for T tokens.
+ *   x      [T][D] in x_dtype (MOE_F32 or MOE_BF16)
+ *   idx    [T][k] int32 out: expert ids, most probable first; equal fp32
+ *          probabilities are ordered by lower expert id
+ *   w      [T][k] fp32 out: routing weights (see norm_topk)
+ *   probs  [T][E] fp32 out, or NULL: the full softmax
+ * Source: lilting.ch "observing the Qwen MoE router", section "hooking the router".
+ */
+moe_status_t moe_route(const moe_router_t* router, const void* x, moe_dtype_t x_dtype, int T,
+                       int32_t* idx, float* w, float* probs, void* workspace, size_t ws_bytes,
+                       void* stream);
+
+/*
+ * Residency substitution (gist.science "Which expert misses are worth waiting
+ * for?", method section). Slots are visited in rank order; a routed expert that
+ * is not resident is kept (fetched) if it is the token's first choice or its
+ * weight is >= threshold, otherwise it is replaced by the resident expert of
+ * highest probability that is neither among the token's k routed experts nor
+ * already used as a replacement (ties: lower id); the replacement keeps the
+ * slot's weight.
+ *   probs     [T][E] fp32 (from moe_route)   idx_in, w_in [T][k]   resident [E] uint8
+ *   threshold 0.15 (the pages' rule); 0 = fetch every miss; +inf = first-choice rule
+ *   idx_out, w_out [T][k] out (may alias idx_in / w_in)
+ *   sub_flag  [T][k] uint8 out: 0 resident, 1 miss kept, 2 substituted,
+ *             3 miss kept because no resident candidate was left
+ *   sub_mass  [T] fp32 out: sum of the weights of substituted slots
+ */
+moe_status_t moe_substitute(int T, int E, int k, const float* probs, const int32_t* idx_in,
+                            const float* w_in, const uint8_t* resident, float threshold,
+                            int32_t* idx_out, float* w_out, uint8_t* sub_flag, float* sub_mass,
+                            void* stream);
+
+/*
+ * Routed experts for T tokens given the routing (Qiita "custom Metal
+ * gather_qmm", sections 4 and 7): only experts named in idx are read, each
+ * distinct expert once per call.
+ *   x       [T][D] in x_dtype (MOE_F32 or MOE_BF16)
+ *   idx, w  [T][k] routing (int32 ids in [0, E), fp32 weights)
+ *   y       [T][D] fp32 out
+ *   x_next  [T][D] in x_dtype out, or NULL: x + y rounded to x_dtype (residual)
+ */
+moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t x_dtype, int T,
+                        int k, const int32_t* idx, const float* w, float* y, void* x_next,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * One whole layer for T tokens: moe_route followed by moe_decode, with the
+ * router's outputs handed to the expert kernels on the device.
+ *   idx, w  [T][k] out    probs [T][E] out or NULL    y, x_next as moe_decode
+ */
+moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts, const void* x,
+                       moe_dtype_t x_dtype, int T, int32_t* idx, float* w, float* probs,
+                       float* y, void* x_next, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Prefill of T tokens: router, then the (token, slot) assignments grouped by
+ * expert (histogram, exclusive scan, stable permutation), a grouped matrix
+ * product per expert on the tensor cores, and the weighted un-permute.
+ *   y          [T][D] fp32 out
+ *   idx, w     [T][k] out, or NULL
+ *   counts     [E] int32 out, or NULL: assignments per expert
+ *   perm       [T*k] int32 out, or NULL: assignment id t*k+r at each grouped
+ *              position (experts ascending, (t, r) order inside an expert)
+ */
+moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* experts, const void* x,
+                         moe_dtype_t x_dtype, int T, float* y, int32_t* idx, float* w,
+                         int32_t* counts, int32_t* perm, void* workspace, size_t ws_bytes,
+                         void* stream);
+
+/*
+ * Waits for `stream`, reads the workspace's device status word, resets it to
+ * zero and returns it (MOE_OK if no device-side problem was recorded).
+ */
+moe_status_t moe_check_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_ROUTE_H */

@@ -1,0 +1,276 @@
+"""Thin Python binding of libmoe_route.so (argument marshalling only).
+
+Every function here converts torch tensors into device pointers, checks their
+dtype, shape, device and contiguity, calls the C entry point of the same name
+on the current torch stream, and raises ``MoeError`` on a non-OK status. No
+computation of the layer happens in Python, and there is no fallback: if the
+CUDA library is missing, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_route.so")
+
+# moe_status_t
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
+MOE_ERR_BAD_INDEX, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_WORKSPACE = 4, 5, 6
+# moe_dtype_t / moe_qfmt_t / op ids
+MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
+MOE_Q_INT8_SYM_B32, MOE_Q_INT4_SYM_B32 = 0, 1
+MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_LAYER, MOE_OP_PREFILL = 0, 1, 2, 3
+
+EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_substitute", "moe_decode", "moe_layer",
+            "moe_prefill", "moe_check_status", "moe_status_string")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+class _Router(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("D", ctypes.c_int), ("k", ctypes.c_int),
+                ("w_dtype", ctypes.c_int), ("W", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("norm_topk", ctypes.c_int)]
+
+
+class _Experts(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("D", ctypes.c_int), ("F", ctypes.c_int),
+                ("q", ctypes.c_int), ("s_dtype", ctypes.c_int),
+                ("gate_q", ctypes.c_void_p), ("gate_s", ctypes.c_void_p),
+                ("up_q", ctypes.c_void_p), ("up_s", ctypes.c_void_p),
+                ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p)]
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with moe_routed_expert_route_gb300/build.py "
+                          "(nvcc, sm_103a); there is no CPU fallback")
+    lib = ctypes.CDLL(path)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.moe_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.moe_workspace_bytes.restype = S
+    lib.moe_route.argtypes = [P, P, I, I, P, P, P, P, S, P]
+    lib.moe_substitute.argtypes = [I, I, I, P, P, P, P, ctypes.c_float, P, P, P, P, P]
+    lib.moe_decode.argtypes = [P, P, I, I, I, P, P, P, P, P, S, P]
+    lib.moe_layer.argtypes = [P, P, P, I, I, P, P, P, P, P, P, S, P]
+    lib.moe_prefill.argtypes = [P, P, P, I, I, P, P, P, P, P, P, S, P]
+    lib.moe_check_status.argtypes = [P, P]
+    lib.moe_status_string.argtypes = [I]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    for f in ("moe_route", "moe_substitute", "moe_decode", "moe_layer", "moe_prefill",
+              "moe_check_status"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
+
+
+_lib = load()
+
+
+def status_string(status: int) -> str:
+    return _lib.moe_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _act_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MOE_F32
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    raise ValueError(f"activations must be float32 or bfloat16, got {t.dtype}")
+
+
+@dataclass
+class Router:
+    """Router weights of one layer: W [E][D] (fp32/bf16), bias [E] fp32 or None."""
+    W: torch.Tensor
+    bias: Optional[torch.Tensor]
+    k: int
+    norm_topk: bool = True
+
+    def struct(self) -> _Router:
+        _dev(self.W, "W", (torch.float32, torch.bfloat16))
+        if self.bias is not None:
+            _dev(self.bias, "bias", torch.float32, (self.W.shape[0],))
+        E, D = self.W.shape
+        return _Router(E, D, self.k, MOE_F32 if self.W.dtype == torch.float32 else MOE_BF16,
+                       self.W.data_ptr(), None if self.bias is None else self.bias.data_ptr(),
+                       1 if self.norm_topk else 0)
+
+
+@dataclass
+class Experts:
+    """Quantised experts of one layer ([E][rows][cols], cols contiguous)."""
+    gate_q: torch.Tensor
+    gate_s: torch.Tensor
+    up_q: torch.Tensor
+    up_s: torch.Tensor
+    down_q: torch.Tensor
+    down_s: torch.Tensor
+    qbits: int = 8
+
+    @property
+    def E(self):
+        return self.gate_q.shape[0]
+
+    @property
+    def F(self):
+        return self.gate_q.shape[1]
+
+    @property
+    def D(self):
+        return self.down_q.shape[1]
+
+    @classmethod
+    def from_layer(cls, layer: dict, qbits: int) -> "Experts":
+        return cls(layer["gate_q"], layer["gate_s"], layer["up_q"], layer["up_s"],
+                   layer["down_q"], layer["down_s"], qbits)
+
+    def struct(self) -> _Experts:
+        E, F = self.gate_q.shape[:2]
+        D = self.down_q.shape[1]
+        cb = 1 if self.qbits == 8 else 2
+        qd = (torch.int8, torch.uint8)
+        sd = (torch.float32, torch.float16)
+        _dev(self.gate_q, "gate_q", qd, (E, F, D // cb))
+        _dev(self.up_q, "up_q", qd, (E, F, D // cb))
+        _dev(self.down_q, "down_q", qd, (E, D, F // cb))
+        _dev(self.gate_s, "gate_s", sd, (E, F, D // 32))
+        _dev(self.up_s, "up_s", self.gate_s.dtype, (E, F, D // 32))
+        _dev(self.down_s, "down_s", self.gate_s.dtype, (E, D, F // 32))
+        return _Experts(E, D, F, MOE_Q_INT8_SYM_B32 if self.qbits == 8 else MOE_Q_INT4_SYM_B32,
+                        MOE_F32 if self.gate_s.dtype == torch.float32 else MOE_F16,
+                        self.gate_q.data_ptr(), self.gate_s.data_ptr(), self.up_q.data_ptr(),
+                        self.up_s.data_ptr(), self.down_q.data_ptr(), self.down_s.data_ptr())
+
+
+def moe_workspace_bytes(op: int, T: int, k: int, E: int, D: int, F: int) -> int:
+    return int(_lib.moe_workspace_bytes(op, T, k, E, D, F))
+
+
+def workspace(op: int, T: int, k: int, E: int, D: int, F: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for `op` (torch allocations are 256-byte aligned)."""
+    n = moe_workspace_bytes(op, T, k, E, D, F)
+    if n == 0:
+        raise ValueError("invalid workspace request")
+    ws = torch.zeros(n, dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def moe_route(router: Router, x: torch.Tensor, idx: torch.Tensor, w: torch.Tensor,
+              probs: Optional[torch.Tensor], ws: torch.Tensor, stream=None):
+    r = router.struct()
+    T = x.shape[0]
+    _dev(x, "x", (torch.float32, torch.bfloat16), (T, r.D))
+    _dev(idx, "idx", torch.int32, (T, r.k))
+    _dev(w, "w", torch.float32, (T, r.k))
+    if probs is not None:
+        _dev(probs, "probs", torch.float32, (T, r.E))
+    _check("moe_route", _lib.moe_route(ctypes.byref(r), _ptr(x), _act_dtype(x), T, _ptr(idx),
+                                       _ptr(w), _ptr(probs), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_substitute(probs, idx_in, w_in, resident, threshold: float, idx_out, w_out, sub_flag,
+                   sub_mass, stream=None):
+    T, E = probs.shape
+    k = idx_in.shape[1]
+    _dev(probs, "probs", torch.float32)
+    _dev(idx_in, "idx_in", torch.int32, (T, k))
+    _dev(w_in, "w_in", torch.float32, (T, k))
+    _dev(resident, "resident", torch.uint8, (E,))
+    _dev(idx_out, "idx_out", torch.int32, (T, k))
+    _dev(w_out, "w_out", torch.float32, (T, k))
+    _dev(sub_flag, "sub_flag", torch.uint8, (T, k))
+    _dev(sub_mass, "sub_mass", torch.float32, (T,))
+    thr = float(threshold)
+    if math.isinf(thr):
+        thr = float("inf")
+    _check("moe_substitute", _lib.moe_substitute(T, E, k, _ptr(probs), _ptr(idx_in), _ptr(w_in),
+                                                 _ptr(resident), ctypes.c_float(thr), _ptr(idx_out),
+                                                 _ptr(w_out), _ptr(sub_flag), _ptr(sub_mass),
+                                                 _stream(stream)))
+
+
+def moe_decode(experts: Experts, x, idx, w, y, x_next, ws, stream=None):
+    e = experts.struct()
+    T, k = idx.shape
+    _dev(x, "x", (torch.float32, torch.bfloat16), (T, e.D))
+    _dev(idx, "idx", torch.int32)
+    _dev(w, "w", torch.float32, (T, k))
+    _dev(y, "y", torch.float32, (T, e.D))
+    if x_next is not None:
+        _dev(x_next, "x_next", x.dtype, (T, e.D))
+    _check("moe_decode", _lib.moe_decode(ctypes.byref(e), _ptr(x), _act_dtype(x), T, k, _ptr(idx),
+                                         _ptr(w), _ptr(y), _ptr(x_next), _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+
+
+def moe_layer(router: Router, experts: Experts, x, idx, w, probs, y, x_next, ws, stream=None):
+    r = router.struct()
+    e = experts.struct()
+    T = x.shape[0]
+    _dev(x, "x", (torch.float32, torch.bfloat16), (T, e.D))
+    _dev(idx, "idx", torch.int32, (T, r.k))
+    _dev(w, "w", torch.float32, (T, r.k))
+    if probs is not None:
+        _dev(probs, "probs", torch.float32, (T, r.E))
+    _dev(y, "y", torch.float32, (T, e.D))
+    if x_next is not None:
+        _dev(x_next, "x_next", x.dtype, (T, e.D))
+    _check("moe_layer", _lib.moe_layer(ctypes.byref(r), ctypes.byref(e), _ptr(x), _act_dtype(x), T,
+                                       _ptr(idx), _ptr(w), _ptr(probs), _ptr(y), _ptr(x_next),
+                                       _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_prefill(router: Router, experts: Experts, x, y, idx, w, counts, perm, ws, stream=None):
+    r = router.struct()
+    e = experts.struct()
+    T = x.shape[0]
+    _dev(x, "x", (torch.float32, torch.bfloat16), (T, e.D))
+    _dev(y, "y", torch.float32, (T, e.D))
+    for t, n, shp, dt in ((idx, "idx", (T, r.k), torch.int32), (w, "w", (T, r.k), torch.float32),
+                          (counts, "counts", (r.E,), torch.int32), (perm, "perm", (T * r.k,), torch.int32)):
+        if t is not None:
+            _dev(t, n, dt, shp)
+    _check("moe_prefill", _lib.moe_prefill(ctypes.byref(r), ctypes.byref(e), _ptr(x), _act_dtype(x), T,
+                                           _ptr(y), _ptr(idx), _ptr(w), _ptr(counts), _ptr(perm),
+                                           _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_check_status(ws: torch.Tensor, stream=None) -> int:
+    return int(_lib.moe_check_status(_ptr(ws), _stream(stream)))

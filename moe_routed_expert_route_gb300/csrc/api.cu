@@ -1,0 +1,270 @@
+// C ABI entry points: argument checks, workspace layout, kernel launches.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kMaxDecodeT = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Workspace sections, in bytes from the start. 0 = section not used.
+struct Layout {
+    size_t logits = 0, xq_hi = 0, xq_lo = 0, xq_s = 0, grp_expert = 0, grp_off = 0, assign = 0, h = 0;
+    size_t total = 0;
+};
+
+Layout layout(int op, int T, int k, int E, int D, int F) {
+    Layout L;
+    size_t off = sizeof(WsHeader);
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + std::max<size_t>(bytes, 1));
+        return o;
+    };
+    const bool route = op == MOE_OP_ROUTE || op == MOE_OP_LAYER;
+    const bool experts = op == MOE_OP_DECODE || op == MOE_OP_LAYER;
+    if (route) L.logits = take(sizeof(float) * (size_t)T * E);
+    if (experts) {
+        size_t ng = (size_t)std::min(T * k, E);
+        L.xq_hi = take((size_t)T * D);
+        L.xq_lo = take((size_t)T * D);
+        L.xq_s = take(sizeof(float) * (size_t)T * (D / kBlk));
+        L.grp_expert = take(sizeof(int32_t) * ng);
+        L.grp_off = take(sizeof(int32_t) * (ng + 1));
+        L.assign = take(sizeof(int32_t) * (size_t)T * k);
+        L.h = take(sizeof(float) * (size_t)T * k * F);
+    }
+    L.total = off;
+    return L;
+}
+
+bool al16(const void* p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
+}
+
+moe_status_t check_router(const moe_router_t* r, moe_dtype_t x_dtype) {
+    if (!r) return MOE_ERR_INVALID_ARG;
+    if (r->E < 1 || r->E > kMaxE || r->k < 1 || r->k > kMaxK || r->k > r->E) return MOE_ERR_INVALID_ARG;
+    if (r->D < kBlk || r->D % kBlk) return MOE_ERR_INVALID_ARG;
+    if (r->w_dtype != MOE_F32 && r->w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (!al16(r->W)) return MOE_ERR_INVALID_ARG;
+    if (r->bias && ((uintptr_t)r->bias & 3u)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status_t check_experts(const moe_experts_t* x, moe_dtype_t x_dtype, int k) {
+    if (!x) return MOE_ERR_INVALID_ARG;
+    if (x->E < 1 || x->E > kMaxE || k < 1 || k > kMaxK || k > x->E) return MOE_ERR_INVALID_ARG;
+    if (x->D < kBlk || x->D % kBlk || x->F < kBlk || x->F % kBlk) return MOE_ERR_INVALID_ARG;
+    if (x->q != MOE_Q_INT8_SYM_B32 && x->q != MOE_Q_INT4_SYM_B32) return MOE_ERR_UNSUPPORTED;
+    if (x->s_dtype != MOE_F32 && x->s_dtype != MOE_F16) return MOE_ERR_UNSUPPORTED;
+    if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    const void* ptrs[6] = {x->gate_q, x->gate_s, x->up_q, x->up_s, x->down_q, x->down_s};
+    for (const void* p : ptrs)
+        if (!al16(p)) return MOE_ERR_INVALID_ARG;
+    int qbits = x->q == MOE_Q_INT8_SYM_B32 ? 8 : 4;
+    if (!experts_supported(1, x->E, x->D, x->F, k, qbits)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+RouterParams router_params(const moe_router_t* r, const void* x, int T, int32_t* idx, float* w,
+                           float* probs, void* ws, const Layout& L) {
+    RouterParams p = {};
+    p.T = T;
+    p.E = r->E;
+    p.D = r->D;
+    p.k = r->k;
+    p.norm_topk = r->norm_topk ? 1 : 0;
+    p.W = r->W;
+    p.bias = r->bias;
+    p.x = x;
+    p.logits = at<float>(ws, L.logits);
+    p.idx = idx;
+    p.w = w;
+    p.probs = probs;
+    p.hdr = at<WsHeader>(ws, 0);
+    return p;
+}
+
+ExpertParams expert_params(const moe_experts_t* X, const void* x, moe_dtype_t x_dtype, int T, int k,
+                           const int32_t* idx, const float* w, float* y, void* x_next, void* ws,
+                           const Layout& L) {
+    ExpertParams p = {};
+    p.T = T;
+    p.E = X->E;
+    p.D = X->D;
+    p.F = X->F;
+    p.k = k;
+    p.qbits = X->q == MOE_Q_INT8_SYM_B32 ? 8 : 4;
+    p.s_f16 = X->s_dtype == MOE_F16;
+    p.gate_q = X->gate_q;
+    p.gate_s = X->gate_s;
+    p.up_q = X->up_q;
+    p.up_s = X->up_s;
+    p.down_q = X->down_q;
+    p.down_s = X->down_s;
+    p.idx = idx;
+    p.w = w;
+    p.x = x;
+    p.x_bf16 = x_dtype == MOE_BF16;
+    p.hdr = at<WsHeader>(ws, 0);
+    p.xq_hi = at<int8_t>(ws, L.xq_hi);
+    p.xq_lo = at<uint8_t>(ws, L.xq_lo);
+    p.xq_s = at<float>(ws, L.xq_s);
+    p.grp_expert = at<int32_t>(ws, L.grp_expert);
+    p.grp_off = at<int32_t>(ws, L.grp_off);
+    p.assign = at<int32_t>(ws, L.assign);
+    p.h = at<float>(ws, L.h);
+    p.y = y;
+    p.x_next = x_next;
+    p.max_groups = std::min(T * k, X->E);
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(int op, int T, int k, int E, int D, int F) {
+    if (T < 1 || k < 1 || E < 1 || D < kBlk || D % kBlk) return 0;
+    if ((op == MOE_OP_DECODE || op == MOE_OP_LAYER) && (F < kBlk || F % kBlk)) return 0;
+    if (op < MOE_OP_ROUTE || op > MOE_OP_LAYER) return 0;
+    return layout(op, T, k, E, D, F).total;
+}
+
+moe_status_t moe_route(const moe_router_t* router, const void* x, moe_dtype_t x_dtype, int T,
+                       int32_t* idx, float* w, float* probs, void* workspace, size_t ws_bytes,
+                       void* stream) {
+    moe_status_t st = check_router(router, x_dtype);
+    if (st != MOE_OK) return st;
+    if (T < 1 || !al16(x) || !idx || !w) return MOE_ERR_INVALID_ARG;
+    Layout L = layout(MOE_OP_ROUTE, T, router->k, router->E, router->D, kBlk);
+    if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    RouterParams p = router_params(router, x, T, idx, w, probs, workspace, L);
+    return from_cuda(launch_router(p, router->w_dtype == MOE_BF16, x_dtype == MOE_BF16,
+                                   static_cast<cudaStream_t>(stream), true));
+}
+
+moe_status_t moe_substitute(int T, int E, int k, const float* probs, const int32_t* idx_in,
+                            const float* w_in, const uint8_t* resident, float threshold,
+                            int32_t* idx_out, float* w_out, uint8_t* sub_flag, float* sub_mass,
+                            void* stream) {
+    if (T < 1 || E < 1 || E > kMaxE || k < 1 || k > kMaxK || k > E) return MOE_ERR_INVALID_ARG;
+    if (!probs || !idx_in || !w_in || !resident || !idx_out || !w_out || !sub_flag || !sub_mass)
+        return MOE_ERR_INVALID_ARG;
+    if (std::isnan(threshold) || threshold < 0.f) return MOE_ERR_INVALID_ARG;
+    SubstituteParams p = {T, E, k, probs, idx_in, w_in, resident, threshold, idx_out, w_out, sub_flag, sub_mass};
+    return from_cuda(launch_substitute(p, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t x_dtype, int T,
+                        int k, const int32_t* idx, const float* w, float* y, void* x_next,
+                        void* workspace, size_t ws_bytes, void* stream) {
+    moe_status_t st = check_experts(experts, x_dtype, k);
+    if (st != MOE_OK) return st;
+    if (T < 1 || T > kMaxDecodeT || !al16(x) || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
+    if (x_next && !al16(x_next)) return MOE_ERR_INVALID_ARG;
+    Layout L = layout(MOE_OP_DECODE, T, k, experts->E, experts->D, experts->F);
+    if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ExpertParams ep = expert_params(experts, x, x_dtype, T, k, idx, w, y, x_next, workspace, L);
+    PrepParams pp = {};
+    pp.T = T;
+    pp.E = experts->E;
+    pp.D = experts->D;
+    pp.k = k;
+    pp.qbits = ep.qbits;
+    pp.x = x;
+    pp.x_bf16 = ep.x_bf16;
+    pp.idx = idx;
+    pp.hdr = ep.hdr;
+    pp.xq_hi = at<int8_t>(workspace, L.xq_hi);
+    pp.xq_lo = at<uint8_t>(workspace, L.xq_lo);
+    pp.xq_s = at<float>(workspace, L.xq_s);
+    pp.grp_expert = at<int32_t>(workspace, L.grp_expert);
+    pp.grp_off = at<int32_t>(workspace, L.grp_off);
+    pp.assign = at<int32_t>(workspace, L.assign);
+    cudaError_t e = launch_prep(pp, s, true);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(launch_experts(ep, s));
+}
+
+moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts, const void* x,
+                       moe_dtype_t x_dtype, int T, int32_t* idx, float* w, float* probs, float* y,
+                       void* x_next, void* workspace, size_t ws_bytes, void* stream) {
+    moe_status_t st = check_router(router, x_dtype);
+    if (st != MOE_OK) return st;
+    st = check_experts(experts, x_dtype, router->k);
+    if (st != MOE_OK) return st;
+    if (router->E != experts->E || router->D != experts->D) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > kMaxDecodeT || !al16(x) || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
+    if (x_next && !al16(x_next)) return MOE_ERR_INVALID_ARG;
+    const int k = router->k;
+    Layout L = layout(MOE_OP_LAYER, T, k, experts->E, experts->D, experts->F);
+    if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    RouterParams rp = router_params(router, x, T, idx, w, probs, workspace, L);
+    ExpertParams ep = expert_params(experts, x, x_dtype, T, k, idx, w, y, x_next, workspace, L);
+    rp.xq_hi = const_cast<int8_t*>(ep.xq_hi);
+    rp.xq_lo = const_cast<uint8_t*>(ep.xq_lo);
+    rp.xq_s = const_cast<float*>(ep.xq_s);
+    rp.qbits = ep.qbits;
+    rp.grp_expert = const_cast<int32_t*>(ep.grp_expert);
+    rp.grp_off = const_cast<int32_t*>(ep.grp_off);
+    rp.assign = const_cast<int32_t*>(ep.assign);
+    cudaError_t e = launch_router(rp, router->w_dtype == MOE_BF16, x_dtype == MOE_BF16, s, true);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(launch_experts(ep, s));
+}
+
+moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* experts, const void* x,
+                         moe_dtype_t x_dtype, int T, float* y, int32_t* idx, float* w,
+                         int32_t* counts, int32_t* perm, void* workspace, size_t ws_bytes,
+                         void* stream) {
+    (void)router; (void)experts; (void)x; (void)x_dtype; (void)T; (void)y; (void)idx; (void)w;
+    (void)counts; (void)perm; (void)workspace; (void)ws_bytes; (void)stream;
+    return MOE_ERR_UNSUPPORTED;
+}
+
+moe_status_t moe_check_status(void* workspace, void* stream) {
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    return static_cast<moe_status_t>(st);
+}
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported combination";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_BAD_INDEX: return "expert id outside [0, E) (access skipped)";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// Kernel parameter blocks and launchers (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "common.cuh"
+
+namespace moe {
+
+// Launch with programmatic stream serialisation, so that a kernel may start its
+// prologue while the previous kernel in the stream drains; every kernel calls
+// griddepcontrol.wait before touching data the previous kernels produce.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+struct RouterParams {
+    int T, E, D, k, norm_topk;
+    const void* W;          // [E][D] bf16 or fp32
+    const float* bias;      // [E] or null
+    const void* x;          // [T][D] bf16 or fp32
+    float* logits;          // workspace [T][E]
+    int32_t* idx;           // [T][k]
+    float* w;               // [T][k]
+    float* probs;           // [T][E] or null
+    WsHeader* hdr;
+    // fixed-point copy of x for the expert kernels (null: not produced)
+    int8_t* xq_hi;
+    uint8_t* xq_lo;
+    float* xq_s;
+    int qbits;
+    // grouping of assignments by expert (null: not produced)
+    int32_t* grp_expert;
+    int32_t* grp_off;
+    int32_t* assign;
+};
+
+struct ExpertParams {
+    int T, E, D, F, k, qbits, s_f16;
+    const void *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
+    const int32_t* idx;     // [T][k]
+    const float* w;         // [T][k]
+    const void* x;          // [T][D] (residual source)
+    int x_bf16;
+    WsHeader* hdr;
+    const int8_t* xq_hi;    // [T][D] fixed-point planes of x
+    const uint8_t* xq_lo;
+    const float* xq_s;      // [T][D/32]
+    const int32_t* grp_expert;
+    const int32_t* grp_off;
+    const int32_t* assign;
+    float* h;               // workspace [T*k][F]
+    float* y;               // [T][D]
+    void* x_next;           // [T][D] or null
+    int max_groups;         // upper bound of distinct experts, sizes the grid
+};
+
+struct PrepParams {
+    int T, E, D, k, qbits;
+    const void* x;
+    int x_bf16;
+    const int32_t* idx;
+    WsHeader* hdr;
+    int8_t* xq_hi;
+    uint8_t* xq_lo;
+    float* xq_s;
+    int32_t* grp_expert;
+    int32_t* grp_off;
+    int32_t* assign;
+};
+
+struct SubstituteParams {
+    int T, E, k;
+    const float* probs;
+    const int32_t* idx_in;
+    const float* w_in;
+    const uint8_t* resident;
+    float threshold;
+    int32_t* idx_out;
+    float* w_out;
+    uint8_t* flag;
+    float* mass;
+};
+
+cudaError_t launch_router(const RouterParams& p, bool w_bf16, bool x_bf16, cudaStream_t s, bool pdl);
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_experts(const ExpertParams& p, cudaStream_t s);
+cudaError_t launch_substitute(const SubstituteParams& p, cudaStream_t s);
+bool experts_supported(int T, int E, int D, int F, int k, int qbits);
+
+}  // namespace moe

@@ -1,0 +1,117 @@
+"""C ABI checks that need no GPU: the library loads, exports every function the
+header declares, sizes workspaces, and rejects bad arguments before launching."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_routed_expert_route_gb300 as M
+from moe_routed_expert_route_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z_]+)\s*\(",
+                                src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert "moe_route" in names and "moe_decode" in names and "moe_prefill" in names
+    lib = ctypes.CDLL(M.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(names) == set(L.EXPORTED)
+
+
+def test_status_strings():
+    for s in range(7):
+        assert M.status_string(s) and M.status_string(s) != "unknown status"
+    assert M.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes():
+    a = M.moe_workspace_bytes(M.MOE_OP_LAYER, 1, 8, 256, 2048, 768)
+    b = M.moe_workspace_bytes(M.MOE_OP_LAYER, 64, 8, 256, 2048, 768)
+    assert 0 < a < b
+    # h alone needs T*k*F floats
+    assert b >= 64 * 8 * 768 * 4
+    assert M.moe_workspace_bytes(M.MOE_OP_DECODE, 1, 8, 256, 2048, 768) > 0
+    assert M.moe_workspace_bytes(M.MOE_OP_ROUTE, 4, 2, 8, 64, 0) > 0
+    assert M.moe_workspace_bytes(M.MOE_OP_LAYER, 0, 8, 256, 2048, 768) == 0
+    assert M.moe_workspace_bytes(M.MOE_OP_LAYER, 1, 8, 256, 2047, 768) == 0
+    assert M.moe_workspace_bytes(M.MOE_OP_DECODE, 1, 8, 256, 2048, 100) == 0
+
+
+def _router(E=8, D=64, k=2, W=16):
+    return L._Router(E, D, k, L.MOE_BF16, W, None, 1)
+
+
+def test_invalid_arguments_rejected_before_launch():
+    lib = L._lib
+    r = _router()
+    null = None
+    # null x / outputs
+    assert lib.moe_route(ctypes.byref(r), null, L.MOE_BF16, 1, 16, 16, null, 256, 10 ** 6, null) == \
+        M.MOE_ERR_INVALID_ARG
+    # k > E
+    bad = _router(E=4, k=5)
+    assert lib.moe_route(ctypes.byref(bad), 16, L.MOE_BF16, 1, 16, 16, null, 256, 10 ** 6, null) == \
+        M.MOE_ERR_INVALID_ARG
+    # D not a multiple of 32
+    bad = _router(D=48)
+    assert lib.moe_route(ctypes.byref(bad), 16, L.MOE_BF16, 1, 16, 16, null, 256, 10 ** 6, null) == \
+        M.MOE_ERR_INVALID_ARG
+    # misaligned router weights
+    bad = _router(W=18)
+    assert lib.moe_route(ctypes.byref(bad), 16, L.MOE_BF16, 1, 16, 16, null, 256, 10 ** 6, null) == \
+        M.MOE_ERR_INVALID_ARG
+    # unsupported activation dtype
+    assert lib.moe_route(ctypes.byref(r), 16, L.MOE_F16, 1, 16, 16, null, 256, 10 ** 6, null) == \
+        M.MOE_ERR_UNSUPPORTED
+    # workspace too small / misaligned / missing
+    assert lib.moe_route(ctypes.byref(r), 16, L.MOE_BF16, 1, 16, 16, null, 256, 8, null) == \
+        M.MOE_ERR_WORKSPACE
+    assert lib.moe_route(ctypes.byref(r), 16, L.MOE_BF16, 1, 16, 16, null, 272, 10 ** 6, null) == \
+        M.MOE_ERR_WORKSPACE
+    assert lib.moe_route(ctypes.byref(r), 16, L.MOE_BF16, 1, 16, 16, null, null, 10 ** 6, null) == \
+        M.MOE_ERR_WORKSPACE
+    # experts: F not a multiple of 32, null scale, k > E
+    ex = L._Experts(8, 64, 48, L.MOE_Q_INT8_SYM_B32, L.MOE_F16, 16, 16, 16, 16, 16, 16)
+    assert lib.moe_decode(ctypes.byref(ex), 16, L.MOE_BF16, 1, 2, 16, 16, 16, null, 256, 10 ** 6,
+                          null) == M.MOE_ERR_INVALID_ARG
+    ex = L._Experts(8, 64, 64, L.MOE_Q_INT8_SYM_B32, L.MOE_F16, 16, null, 16, 16, 16, 16)
+    assert lib.moe_decode(ctypes.byref(ex), 16, L.MOE_BF16, 1, 2, 16, 16, 16, null, 256, 10 ** 6,
+                          null) == M.MOE_ERR_INVALID_ARG
+    ex = L._Experts(8, 64, 64, L.MOE_Q_INT8_SYM_B32, L.MOE_F16, 16, 16, 16, 16, 16, 16)
+    assert lib.moe_decode(ctypes.byref(ex), 16, L.MOE_BF16, 1, 9, 16, 16, 16, null, 256, 10 ** 6,
+                          null) == M.MOE_ERR_INVALID_ARG
+    # T = 0
+    assert lib.moe_decode(ctypes.byref(ex), 16, L.MOE_BF16, 0, 2, 16, 16, 16, null, 256, 10 ** 6,
+                          null) == M.MOE_ERR_INVALID_ARG
+    # substitution: negative / NaN threshold, k > E
+    assert lib.moe_substitute(1, 8, 2, 16, 16, 16, 16, ctypes.c_float(-1.0), 16, 16, 16, 16, null) == \
+        M.MOE_ERR_INVALID_ARG
+    assert lib.moe_substitute(1, 8, 2, 16, 16, 16, 16, ctypes.c_float(float("nan")), 16, 16, 16, 16,
+                              null) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_substitute(1, 8, 9, 16, 16, 16, 16, ctypes.c_float(0.15), 16, 16, 16, 16, null) == \
+        M.MOE_ERR_INVALID_ARG
+    # check_status without workspace
+    assert lib.moe_check_status(null, null) == M.MOE_ERR_WORKSPACE
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+    W = torch.zeros(8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        M.Router(W, None, 2).struct()

@@ -1,0 +1,293 @@
+"""GPU path vs the CPU oracle, element by element, through the C ABI.
+
+Criteria (kept identical everywhere):
+  * routing ids: bit-exact, except tokens whose sorted oracle probabilities have
+    two neighbours among the first k+1 within 1e-6 (a near tie: another
+    summation order may rank them differently); the number skipped is asserted
+    to be small and printed;
+  * routing weights and probabilities: |gpu - oracle| <= 1e-5 / 1e-6;
+  * layer output y (fp32): max |y_gpu - y_oracle| <= 2e-3 * max |y_oracle| per
+    tensor, where the oracle is evaluated on the routing the GPU chose (the
+    routing itself is checked separately above), so near-tie tokens are checked
+    too.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+M = None
+if torch.cuda.is_available():
+    import moe_routed_expert_route_gb300 as M  # noqa: F811
+
+DEV = "cuda"
+REL_TOL = 2e-3
+NTH = os.cpu_count() or 1
+
+
+def small_cfg(E, k, D, F, qbits=8, scale=torch.float16, x_dtype=torch.bfloat16,
+              router_dtype=torch.bfloat16, zipf=1.1, sigma=0.035, cfg_id=50):
+    return W.LayerConfig(f"E{E}k{k}D{D}F{F}q{qbits}", E=E, k=k, D=D, F=F, T=1, qbits=qbits,
+                         scale_dtype=scale, x_dtype=x_dtype, router_dtype=router_dtype,
+                         router_sigma=sigma, zipf=zipf, layers=1, cfg_id=cfg_id)
+
+
+def gpu_layer(cfg, layer, x, probs=True, x_next=False):
+    T = x.shape[0]
+    router = M.Router(layer["Wr"], layer["bias"], cfg.k)
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    out = dict(idx=torch.empty(T, cfg.k, dtype=torch.int32, device=DEV),
+               w=torch.empty(T, cfg.k, dtype=torch.float32, device=DEV),
+               probs=torch.empty(T, cfg.E, dtype=torch.float32, device=DEV) if probs else None,
+               y=torch.empty(T, cfg.D, dtype=torch.float32, device=DEV),
+               x_next=torch.empty_like(x) if x_next else None)
+    ws = M.workspace(M.MOE_OP_LAYER, T, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_layer(router, experts, x, out["idx"], out["w"], out["probs"], out["y"], out["x_next"], ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    return {k_: (v.cpu() if v is not None else None) for k_, v in out.items()}
+
+
+def check_routing(ref, got, k, max_skip_frac=0.1):
+    T = ref["idx"].shape[0]
+    skip = set(oracle.near_tie_tokens(ref["probs32"], k).tolist())
+    keep = np.array([t for t in range(T) if t not in skip], dtype=np.int64)
+    assert len(skip) <= max(1, int(max_skip_frac * T)), f"{len(skip)} near-tie tokens of {T}"
+    gi = got["idx"].numpy()
+    assert np.array_equal(gi[keep], ref["idx"][keep]), "routing ids differ from the oracle"
+    np.testing.assert_allclose(got["w"].numpy()[keep], ref["w"][keep], rtol=0, atol=1e-5)
+    if got.get("probs") is not None:
+        np.testing.assert_allclose(got["probs"].numpy(), ref["probs"], rtol=0, atol=1e-6)
+    return len(skip)
+
+
+def check_y(layer, x, got, qbits, T=None):
+    y_ref = oracle.moe(layer, x, got["idx"], got["w"].double(), qbits, nthreads=NTH)
+    y = got["y"].double().numpy()
+    err = np.abs(y - y_ref).max()
+    bound = REL_TOL * np.abs(y_ref).max()
+    assert err <= bound, f"max|y - oracle| = {err:.3e} > {bound:.3e}"
+    return err / np.abs(y_ref).max()
+
+
+# ------------------------------------------------------------------ tiny
+
+def test_tiny_layer_matches_oracle():
+    cfg = W.CONFIGS[0]
+    layer = W.make_layer(cfg, 0, DEV)
+    x = W.make_tokens(cfg, cfg.T, 0, DEV)
+    got = gpu_layer(cfg, layer, x)
+    ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
+    check_routing(ref, got, cfg.k)
+    check_y(layer, x, got, cfg.qbits)
+    # and against the oracle's own routing, token by token where routing agrees
+    np.testing.assert_allclose(got["y"].double().numpy(), ref["y"], rtol=0,
+                               atol=REL_TOL * np.abs(ref["y"]).max())
+
+
+def test_route_then_decode_equals_layer():
+    cfg = W.CONFIGS[0]
+    layer = W.make_layer(cfg, 0, DEV)
+    x = W.make_tokens(cfg, 9, 1, DEV)
+    T = x.shape[0]
+    router = M.Router(layer["Wr"], layer["bias"], cfg.k)
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    idx = torch.empty(T, cfg.k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, cfg.k, dtype=torch.float32, device=DEV)
+    ws_r = M.workspace(M.MOE_OP_ROUTE, T, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_route(router, x, idx, w, None, ws_r)
+    y = torch.empty(T, cfg.D, dtype=torch.float32, device=DEV)
+    xn = torch.empty_like(x)
+    ws = M.workspace(M.MOE_OP_DECODE, T, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_decode(experts, x, idx, w, y, xn, ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    got = gpu_layer(cfg, layer, x)
+    assert torch.equal(got["idx"], idx.cpu()) and torch.equal(got["w"], w.cpu())
+    assert torch.equal(got["y"], y.cpu())
+    assert torch.equal(xn.cpu(), (x.float() + y).to(x.dtype).cpu())
+
+
+@pytest.mark.parametrize("qbits,scale,x_dtype,rdt", [
+    (8, torch.float32, torch.float32, torch.float32),
+    (8, torch.float16, torch.bfloat16, torch.bfloat16),
+    (4, torch.float16, torch.bfloat16, torch.bfloat16),
+    (4, torch.float32, torch.float32, torch.bfloat16),
+])
+@pytest.mark.parametrize("shape", [(13, 3, 96, 160, 7), (5, 5, 32, 32, 3), (40, 6, 512, 352, 11),
+                                   (1, 1, 64, 64, 2)])
+def test_ragged_shapes(qbits, scale, x_dtype, rdt, shape):
+    E, k, D, F, T = shape
+    cfg = small_cfg(E, k, D, F, qbits, scale, x_dtype, rdt, zipf=None, sigma=0.2, cfg_id=60 + qbits)
+    layer = W.make_layer(cfg, 0, DEV)
+    x = W.make_tokens(cfg, T, 3, DEV)
+    got = gpu_layer(cfg, layer, x)
+    ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
+    check_routing(ref, got, cfg.k, max_skip_frac=0.5)
+    check_y(layer, x, got, cfg.qbits)
+
+
+def test_k_equals_e_and_one_hot():
+    cfg = small_cfg(8, 8, 64, 96, zipf=None, sigma=0.2, cfg_id=70)
+    layer = W.make_layer(cfg, 0, DEV)
+    x = W.make_tokens(cfg, 6, 0, DEV)
+    got = gpu_layer(cfg, layer, x)
+    ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
+    check_routing(ref, got, cfg.k)
+    check_y(layer, x, got, cfg.qbits)
+    np.testing.assert_allclose(got["w"].numpy().sum(1), 1.0, atol=1e-6)
+    # one-hot router: bias +30 on expert 5, k = 1 -> y = that expert's MLP
+    cfg1 = small_cfg(8, 1, 64, 96, zipf=None, sigma=0.01, cfg_id=71)
+    layer1 = W.make_layer(cfg1, 0, DEV)
+    layer1["bias"] = torch.zeros(8, device=DEV)
+    layer1["bias"][5] = 30.0
+    got1 = gpu_layer(cfg1, layer1, x)
+    assert (got1["idx"] == 5).all() and torch.allclose(got1["w"], torch.ones_like(got1["w"]))
+    y_ref = oracle.moe(layer1, x, np.full((6, 1), 5, np.int32), np.ones((6, 1)), 8)
+    assert np.abs(got1["y"].double().numpy() - y_ref).max() <= REL_TOL * np.abs(y_ref).max()
+
+
+# -------------------------------------------------- decode (256 experts)
+
+@pytest.fixture(scope="module")
+def cfg1_layers():
+    cfg = W.CONFIGS[1]
+    return cfg, [W.make_layer(cfg, l, DEV, chunk=64) for l in range(3)]
+
+
+def test_decode_e256_chain_matches_oracle(cfg1_layers):
+    """Three chained layers at T=1: each GPU layer is fed the oracle's input so
+    a near tie in one layer cannot carry into the next."""
+    cfg, layers = cfg1_layers
+    x = W.make_tokens(cfg, 1, 0, DEV)
+    skipped = 0
+    for l, layer in enumerate(layers):
+        got = gpu_layer(cfg, layer, x, x_next=True)
+        ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
+        skipped += check_routing(ref, got, cfg.k, max_skip_frac=1.0)
+        check_y(layer, x, got, cfg.qbits)
+        # x_{l+1} = bf16(x_l + y_l), built from the oracle's y
+        x = (x.cpu().double() + torch.from_numpy(ref["y"])).to(torch.bfloat16).to(DEV)
+    assert skipped <= 1
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16, 32, 64])
+def test_batched_decode_sweep(cfg1_layers, T):
+    cfg, layers = cfg1_layers
+    layer = layers[0]
+    x = W.make_tokens(cfg, T, 7, DEV)
+    got = gpu_layer(cfg, layer, x)
+    ref = oracle.router(x, layer["Wr"], layer["bias"], cfg.k)
+    check_routing(ref, got, cfg.k)
+    check_y(layer, x, got, cfg.qbits)
+
+
+def test_deterministic_reruns(cfg1_layers):
+    cfg, layers = cfg1_layers
+    x = W.make_tokens(cfg, 4, 9, DEV)
+    a = gpu_layer(cfg, layers[1], x)
+    for _ in range(5):
+        b = gpu_layer(cfg, layers[1], x)
+        assert torch.equal(a["y"], b["y"]) and torch.equal(a["idx"], b["idx"])
+
+
+def test_cuda_graph_replay_matches_eager(cfg1_layers):
+    cfg, layers = cfg1_layers
+    T = 2
+    x = W.make_tokens(cfg, T, 11, DEV)
+    router = M.Router(layers[2]["Wr"], layers[2]["bias"], cfg.k)
+    experts = M.Experts.from_layer(layers[2], cfg.qbits)
+    idx = torch.empty(T, cfg.k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, cfg.k, dtype=torch.float32, device=DEV)
+    y = torch.empty(T, cfg.D, dtype=torch.float32, device=DEV)
+    ws = M.workspace(M.MOE_OP_LAYER, T, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        M.moe_layer(router, experts, x, idx, w, None, y, None, ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        M.moe_layer(router, experts, x, idx, w, None, y, None, ws)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    eager = gpu_layer(cfg, layers[2], x)
+    assert torch.equal(y.cpu(), eager["y"])
+
+
+# ------------------------------------------------------ substitution (int4)
+
+@pytest.fixture(scope="module")
+def cfg3_layer():
+    cfg = W.CONFIGS[3]
+    return cfg, W.make_layer(cfg, 0, DEV, chunk=64), W.make_resident_mask(cfg, 0, DEV)
+
+
+@pytest.mark.parametrize("T", [1, 16])
+@pytest.mark.parametrize("threshold", [0.15, 0.0, float("inf")])
+def test_substitution_and_int4_decode(cfg3_layer, T, threshold):
+    cfg, layer, mask = cfg3_layer
+    x = W.make_tokens(cfg, T, 2, DEV)
+    router = M.Router(layer["Wr"], layer["bias"], cfg.k)
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    k = cfg.k
+    idx = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    probs = torch.empty(T, cfg.E, dtype=torch.float32, device=DEV)
+    ws_r = M.workspace(M.MOE_OP_ROUTE, T, k, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_route(router, x, idx, w, probs, ws_r)
+    idx2 = torch.empty_like(idx)
+    w2 = torch.empty_like(w)
+    flag = torch.empty(T, k, dtype=torch.uint8, device=DEV)
+    mass = torch.empty(T, dtype=torch.float32, device=DEV)
+    M.moe_substitute(probs, idx, w, mask, threshold, idx2, w2, flag, mass)
+    y = torch.empty(T, cfg.D, dtype=torch.float32, device=DEV)
+    ws = M.workspace(M.MOE_OP_DECODE, T, k, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_decode(experts, x, idx2, w2, y, None, ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    got = dict(idx=idx.cpu(), w=w.cpu(), probs=probs.cpu())
+    ref = oracle.router(x, layer["Wr"], layer["bias"], k)
+    check_routing(ref, got, k, max_skip_frac=0.2)
+    # substitution on the GPU's own routing and probabilities (decisions in fp32)
+    sref = oracle.substitute(probs.cpu().numpy(), idx.cpu(), w.cpu().double(), mask.cpu(), threshold)
+    assert np.array_equal(flag.cpu().numpy(), sref["flag"])
+    assert np.array_equal(idx2.cpu().numpy(), sref["idx"])
+    np.testing.assert_allclose(mass.cpu().numpy(), sref["mass"], rtol=0, atol=1e-6)
+    assert torch.equal(w2.cpu(), w.cpu())
+    check_y(layer, x, dict(idx=idx2.cpu(), w=w2.cpu(), y=y.cpu()), cfg.qbits)
+    n_sub = int((flag == 2).sum())
+    print(f"T={T} thr={threshold}: substituted {n_sub}/{T * k}, mass mean {mass.mean().item():.4f}")
+
+
+# ------------------------------------------------------------- edge cases
+
+def test_bad_expert_id_is_reported_and_skipped():
+    cfg = W.CONFIGS[0]
+    layer = W.make_layer(cfg, 0, DEV)
+    x = W.make_tokens(cfg, 3, 4, DEV)
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    idx = torch.tensor([[1, 2], [cfg.E + 5, 0], [3, -1]], dtype=torch.int32, device=DEV)
+    w = torch.full((3, 2), 0.5, device=DEV)
+    y = torch.empty(3, cfg.D, device=DEV)
+    ws = M.workspace(M.MOE_OP_DECODE, 3, 2, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_decode(experts, x, idx, w, y, None, ws)
+    assert M.moe_check_status(ws) == M.MOE_ERR_BAD_INDEX
+    assert M.moe_check_status(ws) == M.MOE_OK  # reset by the read
+    # the valid slots are still computed: token 0 fully, tokens 1/2 their valid slot
+    ic = idx.cpu().numpy().copy()
+    wc = w.cpu().double().numpy().copy()
+    bad = (ic < 0) | (ic >= cfg.E)
+    wc[bad] = 0.0
+    ic[bad] = 0
+    y_ref = oracle.moe(layer, x, ic, wc, cfg.qbits)
+    assert np.abs(y.cpu().double().numpy() - y_ref).max() <= REL_TOL * np.abs(y_ref).max()
+    # the library keeps working after a reported error
+    idx.fill_(1)
+    M.moe_decode(experts, x, idx, w, y, None, ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
