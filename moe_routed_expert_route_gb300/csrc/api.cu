@@ -138,6 +138,31 @@ ExpertParams expert_params(const moe_experts_t* X, const void* x, moe_dtype_t x_
     return p;
 }
 
+FusedParams fused_params(const moe_experts_t* X, const void* x, int k, float* y, void* x_next,
+                         void* ws, const Layout& L) {
+    FusedParams f = {};
+    f.E = X->E;
+    f.D = X->D;
+    f.F = X->F;
+    f.k = k;
+    f.x = x;
+    f.gate_q = X->gate_q;
+    f.gate_s = X->gate_s;
+    f.up_q = X->up_q;
+    f.up_s = X->up_s;
+    f.down_q = X->down_q;
+    f.down_s = X->down_s;
+    f.y = y;
+    f.x_next = x_next;
+    f.hdr = at<WsHeader>(ws, 0);
+    f.logits = L.logits ? at<float>(ws, L.logits) : nullptr;
+    f.h = at<float>(ws, L.h);
+    return f;
+}
+
+int qbits_of(const moe_experts_t* X) { return X->q == MOE_Q_INT8_SYM_B32 ? 8 : 4; }
+int scale_bytes(const moe_experts_t* X) { return X->s_dtype == MOE_F16 ? 2 : 4; }
+
 }  // namespace
 
 extern "C" {
@@ -184,6 +209,19 @@ moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t
     Layout L = layout(MOE_OP_DECODE, T, k, experts->E, experts->D, experts->F);
     if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 1) {
+        FusedParams fp = fused_params(experts, x, k, y, x_next, workspace, L);
+        size_t smem = 0;
+        int grid = 0;
+        if (fused_plan(experts->E, experts->D, experts->F, k, qbits_of(experts), scale_bytes(experts),
+                       x_dtype == MOE_BF16 ? 2 : 4, false, &fp, &smem, &grid)) {
+            fp.has_router = 0;
+            fp.idx_in = idx;
+            fp.w_in = w;
+            return from_cuda(launch_fused(fp, qbits_of(experts), experts->s_dtype == MOE_F16,
+                                          x_dtype == MOE_BF16, grid, smem, s));
+        }
+    }
     ExpertParams ep = expert_params(experts, x, x_dtype, T, k, idx, w, y, x_next, workspace, L);
     PrepParams pp = {};
     pp.T = T;
@@ -220,6 +258,23 @@ moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts,
     Layout L = layout(MOE_OP_LAYER, T, k, experts->E, experts->D, experts->F);
     if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 1 && (router->w_dtype == MOE_BF16) == (x_dtype == MOE_BF16)) {
+        FusedParams fp = fused_params(experts, x, k, y, x_next, workspace, L);
+        size_t smem = 0;
+        int grid = 0;
+        if (fused_plan(experts->E, experts->D, experts->F, k, qbits_of(experts), scale_bytes(experts),
+                       x_dtype == MOE_BF16 ? 2 : 4, true, &fp, &smem, &grid)) {
+            fp.has_router = 1;
+            fp.norm_topk = router->norm_topk ? 1 : 0;
+            fp.W = router->W;
+            fp.bias = router->bias;
+            fp.idx = idx;
+            fp.w = w;
+            fp.probs = probs;
+            return from_cuda(launch_fused(fp, qbits_of(experts), experts->s_dtype == MOE_F16,
+                                          x_dtype == MOE_BF16, grid, smem, s));
+        }
+    }
     RouterParams rp = router_params(router, x, T, idx, w, probs, workspace, L);
     ExpertParams ep = expert_params(experts, x, x_dtype, T, k, idx, w, y, x_next, workspace, L);
     rp.xq_hi = const_cast<int8_t*>(ep.xq_hi);
@@ -249,7 +304,10 @@ moe_status_t moe_check_status(void* workspace, void* stream) {
     int st = 0;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // after a device-side problem the launch may have left its counters
+    // mid-way: clear the whole header, not only the status word
+    size_t clear = st != 0 ? sizeof(WsHeader) : sizeof(int);
+    if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     return static_cast<moe_status_t>(st);
 }

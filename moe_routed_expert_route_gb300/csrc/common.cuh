@@ -16,12 +16,14 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // ------------------------------------------------------------ workspace header
 // The first 256 bytes of every workspace: device status word, the router's
-// "CTAs finished" counter, and the number of distinct routed experts.
+// "CTAs finished" counter, the number of distinct routed experts and the grid
+// barrier counter. Counters are back at zero when a launch ends.
 struct WsHeader {
     int status;
     unsigned int done;
     int n_groups;
-    int pad[61];
+    unsigned int bar;  // grid-barrier counter of the persistent layer kernel
+    int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

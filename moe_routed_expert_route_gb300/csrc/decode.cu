@@ -21,48 +21,11 @@
 // int4 widened to 16*q by masking its nibbles into the top of each byte) times
 // the 16-bit fixed-point activation block via dp4a, exact in int32, then one
 // fp32 multiply by (weight scale * activation scale) per 16-byte chunk.
+#include "dots.cuh"
 #include "group.cuh"
 #include "kernels.h"
 
 namespace moe {
-
-// ------------------------------------------------------------- integer dots
-// 16 int8 codes (one 16-byte chunk) against the matching 16 plane bytes.
-__device__ __forceinline__ int dot_i8_chunk(const uint4 q, const uint4 hi, const uint4 lo) {
-    int h = dp4a_ss(q.x, hi.x, 0);
-    h = dp4a_ss(q.y, hi.y, h);
-    h = dp4a_ss(q.z, hi.z, h);
-    h = dp4a_ss(q.w, hi.w, h);
-    int l = dp4a_su(q.x, lo.x, 0);
-    l = dp4a_su(q.y, lo.y, l);
-    l = dp4a_su(q.z, lo.z, l);
-    l = dp4a_su(q.w, lo.w, l);
-    return h * 256 + l;
-}
-
-// 32 int4 codes (one 16-byte chunk = one quantisation block) against the 32
-// plane bytes of that block, returning 16 * sum(q * X): each word's low
-// nibbles (even elements) and high nibbles (odd elements) are moved to the top
-// of their bytes, where a two's complement nibble reads as 16 * its value.
-__device__ __forceinline__ int dot_i4_word(uint32_t w, uint32_t he, uint32_t ho, uint32_t le,
-                                           uint32_t lo, int& h, int& l) {
-    uint32_t ev = (w << 4) & 0xF0F0F0F0u;
-    uint32_t od = w & 0xF0F0F0F0u;
-    h = dp4a_ss(ev, he, h);
-    h = dp4a_ss(od, ho, h);
-    l = dp4a_su(ev, le, l);
-    l = dp4a_su(od, lo, l);
-    return 0;
-}
-__device__ __forceinline__ int dot_i4_chunk(const uint4 q, const uint4 h0, const uint4 h1,
-                                            const uint4 l0, const uint4 l1) {
-    int h = 0, l = 0;
-    dot_i4_word(q.x, h0.x, h0.y, l0.x, l0.y, h, l);
-    dot_i4_word(q.y, h0.z, h0.w, l0.z, l0.w, h, l);
-    dot_i4_word(q.z, h1.x, h1.y, l1.x, l1.y, h, l);
-    dot_i4_word(q.w, h1.z, h1.w, l1.z, l1.w, h, l);
-    return h * 256 + l;
-}
 
 template <int QB>
 struct Chunk {
@@ -136,13 +99,17 @@ __global__ void __launch_bounds__(256) gateup_kernel(ExpertParams p) {
 
     pdl_wait();
     pdl_trigger();
-    const int ng = ld_cg_i32(&p.hdr->n_groups);
-    const int ntask = ng * p.F;
-    for (int task = gwarp; task < ntask; task += nwarps) {
+    for (int task = gwarp; task < p.max_groups * p.F; task += nwarps) {
         const int g = task / p.F;
         const int n = task - g * p.F;
+        // the group count and the group's entries are fetched together; g is
+        // below the workspace's group capacity, so the speculative reads stay
+        // inside it
+        const int ng = ld_cg_i32(&p.hdr->n_groups);
         const int e = ld_cg_i32(p.grp_expert + g);
         const int a0 = ld_cg_i32(p.grp_off + g), a1 = ld_cg_i32(p.grp_off + g + 1);
+        const int asg0 = ld_cg_i32(p.assign + min(max(a0, 0), p.T * p.k - 1));
+        if (g >= ng) break;
         const size_t row = (size_t)e * p.F + n;
         uint4 gv[NCH], uv[NCH];
         float gsc[NCH], usc[NCH];
@@ -160,7 +127,7 @@ __global__ void __launch_bounds__(256) gateup_kernel(ExpertParams p) {
             }
         }
         for (int a = a0; a < a1; a++) {
-            const int asg = ld_cg_i32(p.assign + a);
+            const int asg = a == a0 ? asg0 : ld_cg_i32(p.assign + a);
             const int t = asg / p.k;
             const int8_t* xh = p.xq_hi + (size_t)t * p.D;
             const uint8_t* xl = p.xq_lo + (size_t)t * p.D;
@@ -194,6 +161,8 @@ __global__ void __launch_bounds__(256) gateup_kernel(ExpertParams p) {
 }
 
 // ------------------------------------------------------------------- down
+constexpr int kConvBatch = 24;  // h blocks converted per warp per round trip
+
 template <int QB, typename ST, int NLD>
 __global__ void __launch_bounds__(256) down_kernel(ExpertParams p) {
     extern __shared__ __align__(16) unsigned char s_raw[];
@@ -236,17 +205,31 @@ __global__ void __launch_bounds__(256) down_kernel(ExpertParams p) {
     pdl_trigger();
 
     // this token's gated activations, k slots x F, into fixed point (scale
-    // folded with the slot's routing weight)
-    for (int blk = warp; blk < p.k * nbF; blk += 8) {
-        int r = blk / nbF, b = blk - r * nbF;
-        float hv = ld_cg_f32(p.h + ((size_t)t * p.k + r) * p.F + b * kBlk + lane);
-        float m = warp_max(fabsf(hv));
-        Fx f = fx_of_blockmax(m);
-        int X = fx_code(hv, f.mul);
-        int pos = r * p.F + b * kBlk + fx_pos(lane, QB);
-        s_hi[pos] = (int8_t)(X >> 8);
-        s_lo[pos] = (uint8_t)(X & 0xff);
-        if (lane == 0) s_sc[blk] = f.scale * ld_cg_f32(p.w + (size_t)t * p.k + r);
+    // folded with the slot's routing weight); the loads of a batch are all
+    // issued before the first is used
+    const int nblk = p.k * nbF;
+    const float* ht = p.h + (size_t)t * p.k * p.F;
+    for (int base = warp; base < nblk; base += 8 * kConvBatch) {
+        float hv[kConvBatch], wr[kConvBatch];
+#pragma unroll
+        for (int i = 0; i < kConvBatch; i++) {
+            int blk = base + 8 * i;
+            hv[i] = blk < nblk ? ld_cg_f32(ht + (size_t)blk * kBlk + lane) : 0.f;
+            wr[i] = blk < nblk ? ld_cg_f32(p.w + (size_t)t * p.k + blk / nbF) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kConvBatch; i++) {
+            int blk = base + 8 * i;
+            if (blk < nblk) {
+                float m = warp_max(fabsf(hv[i]));
+                Fx f = fx_of_blockmax(m);
+                int X = fx_code(hv[i], f.mul);
+                int pos = blk * kBlk + fx_pos(lane, QB);
+                s_hi[pos] = (int8_t)(X >> 8);
+                s_lo[pos] = (uint8_t)(X & 0xff);
+                if (lane == 0) s_sc[blk] = f.scale * wr[i];
+            }
+        }
     }
     __syncthreads();
     if (d >= p.D) return;

@@ -1,0 +1,415 @@
+// One whole MoE layer for one token in ONE persistent launch (decode, T = 1).
+//
+// lilting.ch "observing the Qwen MoE router" (section "hooking the router"):
+// router logits -> fp32 softmax -> top-k. Qiita "custom Metal gather_qmm"
+// (sections 4 and 7): only the k routed experts' rows are read, gate and up
+// share x, down takes each slot's own activation, and the slots are combined
+// with the routing weights.
+//
+// Grid = one CTA of 16 warps per SM, all resident. Phases:
+//   0  before waiting on the previous launch: each CTA loads its slice of the
+//      router weights (1-4 experts' rows) into registers
+//   1  x -> shared memory (fp32) and its 16-bit fixed-point planes; the CTA's
+//      router logits -> workspace                       [grid barrier 1]
+//   2  every CTA reads all E logits and runs the softmax + top-k itself (no
+//      second exchange is needed to learn the routing)
+//   3  one thread starts bulk (TMA) copies of this CTA's rows of the k down
+//      matrices into shared memory; meanwhile the 16 warps stream this CTA's
+//      share of the k*F gate/up row pairs from HBM (two row pairs in flight per
+//      warp) and write h = silu(g)*u to the workspace  [grid barrier 2]
+//   4  the k*F activations -> shared memory; each warp owns one slot and some
+//      of the CTA's rows, dots them against the staged down rows; the CTA then
+//      combines the k slots in slot order: y[d] = sum_r w[r]*o_r[d]; x_next.
+// Without a router (moe_decode) phases 0-2 are replaced by reading idx/w.
+#include "dots.cuh"
+#include "group.cuh"
+#include "kernels.h"
+#include "sync.cuh"
+
+namespace moe {
+
+constexpr int kFThreads = 512;
+constexpr int kFWarps = 16;
+constexpr int kNRC = 2;  // router 16-byte chunks per lane
+constexpr int kNCH = 4;  // gate/up 16-byte chunks per lane
+constexpr int kNP = 4;   // down 8-byte pieces per lane
+
+struct FusedLayout {
+    size_t x, xhi, xlo, xs, dq, ds, h, part, total;
+};
+
+__host__ __device__ inline size_t fl_align(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline FusedLayout fused_layout(int D, int F, int k, int qbits, int s_bytes, int rows) {
+    FusedLayout L;
+    size_t o = 0;
+    const size_t rowF = qbits == 8 ? F : F / 2;
+    L.x = o;    o = fl_align(o + sizeof(float) * D, 16);
+    L.xhi = o;  o = fl_align(o + D, 16);
+    L.xlo = o;  o = fl_align(o + D, 16);
+    L.xs = o;   o = fl_align(o + sizeof(float) * (D / kBlk), 16);
+    L.dq = o;   o = fl_align(o + (size_t)k * rows * rowF, 16);
+    L.ds = o;   o = fl_align(o + (size_t)k * rows * (F / kBlk) * s_bytes, 16);
+    L.h = o;    o = fl_align(o + sizeof(float) * (size_t)k * F, 16);
+    L.part = o; o = fl_align(o + sizeof(float) * (size_t)k * rows, 16);
+    L.total = o;
+    return L;
+}
+
+template <int QB, typename ST>
+struct RowPair {
+    uint4 g[kNCH], u[kNCH];
+    float gs[kNCH], us[kNCH];
+};
+
+template <int QB, typename ST, typename XT, int NJ>
+__global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    __shared__ float s_rpart[kFWarps];
+    __shared__ int s_idx[32];
+    __shared__ float s_w[32];
+    __shared__ int s_abort;
+    __shared__ __align__(8) uint64_t s_bar;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int D = p.D, F = p.F, k = p.k;
+    const int nb = D / kBlk, nbF = F / kBlk;
+    const int rowD = QB == 8 ? D : D / 2;    // bytes of a gate/up row
+    const int rowF = QB == 8 ? F : F / 2;    // bytes of a down row
+    const FusedLayout L = fused_layout(D, F, k, QB, sizeof(ST), p.rows);
+    float* s_x = reinterpret_cast<float*>(sm + L.x);
+    int8_t* s_xhi = reinterpret_cast<int8_t*>(sm + L.xhi);
+    uint8_t* s_xlo = sm + L.xlo;
+    float* s_xs = reinterpret_cast<float*>(sm + L.xs);
+    uint8_t* s_dq = sm + L.dq;
+    ST* s_ds = reinterpret_cast<ST*>(sm + L.ds);
+    float* s_h = reinterpret_cast<float*>(sm + L.h);
+    float* s_part = reinterpret_cast<float*>(sm + L.part);
+    int* status = &p.hdr->status;
+    unsigned* bar = &p.hdr->bar;
+
+    // ---------------------------------------------------------- phase 0
+    if (tid == 0) {
+        s_abort = 0;
+        mbar_init(&s_bar, 1);
+        fence_barrier_init();
+    }
+    const XT* Wr = reinterpret_cast<const XT*>(p.W);
+    constexpr int EPC = 16 / sizeof(XT);
+    const int e_begin = (int)((long)c * p.E / G), e_end = (int)((long)(c + 1) * p.E / G);
+    const int nseg = p.router_nseg;
+    const int rj = warp / nseg, rs = warp - rj * nseg;
+    const int re = e_begin + rj;
+    const int seg = D / nseg;
+    const bool rvalid = p.has_router && re < e_end;
+    uint4 wr[kNRC];
+#pragma unroll
+    for (int i = 0; i < kNRC; i++) {
+        int ci = i * 32 + lane;
+        wr[i] = make_uint4(0, 0, 0, 0);
+        if (rvalid && ci * EPC < seg) wr[i] = ld_stream16(Wr + (size_t)re * D + rs * seg + ci * EPC);
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+
+    // ---------------------------------------------------------- phase 1
+    const XT* X = reinterpret_cast<const XT*>(p.x);
+    for (int i = tid; i < D; i += kFThreads) s_x[i] = ldcg_f32(X + i);
+    __syncthreads();
+    for (int b = warp; b < nb; b += kFWarps)
+        fx_store_block(s_x[b * kBlk + lane], lane, QB, s_xhi + b * kBlk, s_xlo + b * kBlk, s_xs + b);
+    int nbar = 0;
+    if (p.has_router) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < kNRC; i++) {
+            int ci = i * 32 + lane;
+            if (rvalid && ci * EPC < seg) {
+                const float* xs = s_x + rs * seg + ci * EPC;
+                const uint32_t* wq = reinterpret_cast<const uint32_t*>(&wr[i]);
+#pragma unroll
+                for (int q = 0; q < EPC; q++) {
+                    float wf;
+                    if constexpr (sizeof(XT) == 2) wf = (q & 1) ? bf16hi(wq[q >> 1]) : bf16lo(wq[q >> 1]);
+                    else wf = __uint_as_float(wq[q]);
+                    acc = fmaf(wf, xs[q], acc);
+                }
+            }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) s_rpart[warp] = acc;
+        __syncthreads();
+        if (tid < e_end - e_begin) {
+            float l = 0.f;
+            for (int s = 0; s < nseg; s++) l += s_rpart[tid * nseg + s];
+            if (p.bias) l += p.bias[e_begin + tid];
+            p.logits[e_begin + tid] = l;
+        }
+        grid_barrier(bar, (unsigned)G * (++nbar), status, &s_abort);
+
+        // ------------------------------------------------------ phase 2
+        if (warp == 0) {
+            int sel_e;
+            float sel_p;
+            softmax_topk_warp<NJ>(p.logits, p.E, k, (c == 0) ? p.probs : nullptr, lane, sel_e, sel_p);
+            float norm = warp_sum(lane < k ? sel_p : 0.f);
+            float wv = p.norm_topk ? sel_p / norm : sel_p;
+            if (lane < k) {
+                s_idx[lane] = sel_e;
+                s_w[lane] = wv;
+                if (c == 0) {
+                    p.idx[lane] = sel_e;
+                    p.w[lane] = wv;
+                }
+            }
+        }
+    } else if (tid < k) {
+        int e = ld_cg_i32(p.idx_in + tid);
+        if (e < 0 || e >= p.E) {
+            if (c == 0) record_error(status, MOE_ERR_BAD_INDEX);
+            e = -1;
+        }
+        s_idx[tid] = e;
+        s_w[tid] = ld_cg_f32(p.w_in + tid);
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------- phase 3
+    const int d_begin = (int)((long)c * D / G), d_end = (int)((long)(c + 1) * D / G);
+    const int nrows = d_end - d_begin;
+    if (tid == 0) {
+        unsigned bytes = 0;
+        for (int r = 0; r < k; r++)
+            if (s_idx[r] >= 0) bytes += nrows * (rowF + nbF * (int)sizeof(ST));
+        mbar_arrive_expect_tx(&s_bar, bytes);
+        const uint8_t* DQ = reinterpret_cast<const uint8_t*>(p.down_q);
+        const ST* DS = reinterpret_cast<const ST*>(p.down_s);
+        if (nrows > 0) {
+            for (int r = 0; r < k; r++) {
+                int e = s_idx[r];
+                if (e < 0) continue;
+                size_t row0 = (size_t)e * D + d_begin;
+                bulk_g2s(s_dq + (size_t)r * p.rows * rowF, DQ + row0 * rowF, nrows * rowF, &s_bar);
+                bulk_g2s(s_ds + (size_t)r * p.rows * nbF, DS + row0 * nbF, nrows * nbF * (int)sizeof(ST), &s_bar);
+            }
+        }
+    }
+
+    const uint8_t* GQ = reinterpret_cast<const uint8_t*>(p.gate_q);
+    const uint8_t* UQ = reinterpret_cast<const uint8_t*>(p.up_q);
+    const ST* GS = reinterpret_cast<const ST*>(p.gate_s);
+    const ST* US = reinterpret_cast<const ST*>(p.up_s);
+    const int nchunk = rowD / 16;
+    const long total = (long)k * F;
+    const int g_begin = (int)((long)c * total / G), g_end = (int)((long)(c + 1) * total / G);
+
+    auto load_pair = [&](int g, RowPair<QB, ST>& rp) {
+        int r = g / F, n = g - r * F;
+        int e = s_idx[r];
+        bool ok = g < g_end && e >= 0;
+        size_t row = (size_t)(ok ? e : 0) * F + n;
+#pragma unroll
+        for (int j = 0; j < kNCH; j++) {
+            int ci = j * 32 + lane;
+            if (ok && ci < nchunk) {
+                rp.g[j] = ld_stream16(GQ + row * rowD + 16 * ci);
+                rp.u[j] = ld_stream16(UQ + row * rowD + 16 * ci);
+                int blk = QB == 8 ? (ci >> 1) : ci;
+                rp.gs[j] = to_f32(GS[row * nb + blk]);
+                rp.us[j] = to_f32(US[row * nb + blk]);
+            } else {
+                rp.g[j] = rp.u[j] = make_uint4(0, 0, 0, 0);
+                rp.gs[j] = rp.us[j] = 0.f;
+            }
+        }
+    };
+    auto finish_pair = [&](int g, const RowPair<QB, ST>& rp) {
+        float ga = 0.f, ua = 0.f;
+#pragma unroll
+        for (int j = 0; j < kNCH; j++) {
+            int ci = j * 32 + lane;
+            if (ci < nchunk) {
+                int ig, iu;
+                float xs;
+                if constexpr (QB == 8) {
+                    uint4 hi = *reinterpret_cast<const uint4*>(s_xhi + 16 * ci);
+                    uint4 lo = *reinterpret_cast<const uint4*>(s_xlo + 16 * ci);
+                    ig = dot_i8_chunk(rp.g[j], hi, lo);
+                    iu = dot_i8_chunk(rp.u[j], hi, lo);
+                    xs = s_xs[ci >> 1];
+                } else {
+                    const uint4* H = reinterpret_cast<const uint4*>(s_xhi + 32 * ci);
+                    const uint4* Lo = reinterpret_cast<const uint4*>(s_xlo + 32 * ci);
+                    uint4 h0 = H[0], h1 = H[1], l0 = Lo[0], l1 = Lo[1];
+                    ig = dot_i4_chunk(rp.g[j], h0, h1, l0, l1);
+                    iu = dot_i4_chunk(rp.u[j], h0, h1, l0, l1);
+                    xs = s_xs[ci] * (1.0f / 16.0f);
+                }
+                ga = fmaf((float)ig, rp.gs[j] * xs, ga);
+                ua = fmaf((float)iu, rp.us[j] * xs, ua);
+            }
+        }
+        ga = warp_sum(ga);
+        ua = warp_sum(ua);
+        if (lane == 0) p.h[g] = silu_mul(ga, ua);
+    };
+
+    {
+        RowPair<QB, ST> A, B;
+        int g = g_begin + warp;
+        load_pair(g, A);
+        while (g < g_end) {
+            int g2 = g + kFWarps;
+            load_pair(g2, B);
+            finish_pair(g, A);
+            if (g2 >= g_end) break;
+            int g3 = g2 + kFWarps;
+            load_pair(g3, A);
+            finish_pair(g2, B);
+            g = g3;
+        }
+    }
+    grid_barrier(bar, (unsigned)G * (++nbar), status, &s_abort);
+
+    // ---------------------------------------------------------- phase 4
+    for (int i = tid * 4; i < k * F; i += kFThreads * 4) {
+        uint4 v = ld_cg16(p.h + i);
+        *reinterpret_cast<uint4*>(s_h + i) = v;
+    }
+    mbar_wait(&s_bar, 0, status);
+    __syncthreads();
+
+    const int wps = kFWarps / k;  // warps per slot (k <= 16)
+    const int slot = warp / wps, sub = warp - slot * wps;
+    if (slot < k && s_idx[slot] >= 0) {
+        constexpr int EPP = QB == 8 ? 8 : 16;  // elements per 8-byte piece
+        const int npieces = rowF / 8;
+        float hreg[kNP][EPP];
+#pragma unroll
+        for (int i = 0; i < kNP; i++) {
+            int pc = i * 32 + lane;
+#pragma unroll
+            for (int q = 0; q < EPP; q++)
+                hreg[i][q] = pc < npieces ? s_h[slot * F + pc * EPP + q] : 0.f;
+        }
+        const uint8_t* dq0 = s_dq + (size_t)slot * p.rows * rowF;
+        const ST* ds0 = s_ds + (size_t)slot * p.rows * nbF;
+        for (int row = sub; row < nrows; row += wps) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < kNP; i++) {
+                int pc = i * 32 + lane;
+                if (pc < npieces) {
+                    uint2 wv = *reinterpret_cast<const uint2*>(dq0 + (size_t)row * rowF + 8 * pc);
+                    float s = to_f32(ds0[row * nbF + (pc * EPP) / kBlk]);
+                    float dot = 0.f;
+                    if constexpr (QB == 8) {
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            uint32_t wd = q < 4 ? wv.x : wv.y;
+                            int code = (int)(int8_t)((wd >> (8 * (q & 3))) & 0xff);
+                            dot = fmaf((float)code, hreg[i][q], dot);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; q++) {
+                            uint32_t wd = q < 8 ? wv.x : wv.y;
+                            int code = ((int)(wd << (28 - 4 * (q & 7)))) >> 28;
+                            dot = fmaf((float)code, hreg[i][q], dot);
+                        }
+                    }
+                    acc = fmaf(s, dot, acc);
+                }
+            }
+            acc = warp_sum(acc);
+            if (lane == 0) s_part[row * k + slot] = acc;
+        }
+    }
+    __syncthreads();
+    if (tid < nrows) {
+        float y = 0.f;
+        for (int r = 0; r < k; r++)
+            if (s_idx[r] >= 0) y = fmaf(s_w[r], s_part[tid * k + r], y);
+        const int d = d_begin + tid;
+        p.y[d] = y;
+        if (p.x_next) {
+            if constexpr (sizeof(XT) == 2)
+                reinterpret_cast<__nv_bfloat16*>(p.x_next)[d] = __float2bfloat16_rn(s_x[d] + y);
+            else
+                reinterpret_cast<float*>(p.x_next)[d] = s_x[d] + y;
+        }
+    }
+    grid_exit(bar, (unsigned)G * (nbar + 1));
+}
+
+// ------------------------------------------------------------- host side
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+}
+
+static int pow2ceil(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Grid and per-CTA shape for one layer; false if the fused kernel cannot run it.
+bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes, bool has_router,
+                FusedParams* fp, size_t* smem, int* grid) {
+    int G = std::min(sm_count(), D);
+    if (G < 1 || k > 16 || k < 1) return false;
+    const int rows = (D + G - 1) / G;
+    const int rowD = qbits == 8 ? D : D / 2, rowF = qbits == 8 ? F : F / 2;
+    if (rowD / 16 > 32 * kNCH) return false;
+    if (rowF / 8 > 32 * kNP) return false;
+    if (F % 4) return false;
+    if (((F / kBlk) * s_bytes) % 16) return false;  // bulk copies of whole scale rows
+    if (has_router) {
+        int nexp = (E + G - 1) / G;
+        int nseg = kFWarps / pow2ceil(nexp);
+        if (nseg < 1 || D % nseg) return false;
+        int seg = D / nseg;
+        int epc = 16 / x_bytes;
+        if (seg % epc || seg / epc > 32 * kNRC) return false;
+        fp->router_nseg = nseg;
+        if (E > 1024) return false;
+    } else {
+        fp->router_nseg = 1;
+    }
+    FusedLayout L = fused_layout(D, F, k, qbits, s_bytes, rows);
+    if (L.total > 200 * 1024) return false;
+    fp->rows = rows;
+    *smem = L.total;
+    *grid = G;
+    return true;
+}
+
+template <int QB, typename ST, typename XT>
+static cudaError_t launch_fused_t(const FusedParams& p, int grid, size_t smem, cudaStream_t s) {
+    if (p.E <= 32) return launch(fused_layer_kernel<QB, ST, XT, 1>, dim3(grid), dim3(kFThreads), smem, s, true, p);
+    if (p.E <= 256) return launch(fused_layer_kernel<QB, ST, XT, 8>, dim3(grid), dim3(kFThreads), smem, s, true, p);
+    if (p.E <= 512) return launch(fused_layer_kernel<QB, ST, XT, 16>, dim3(grid), dim3(kFThreads), smem, s, true, p);
+    return launch(fused_layer_kernel<QB, ST, XT, 32>, dim3(grid), dim3(kFThreads), smem, s, true, p);
+}
+
+cudaError_t launch_fused(const FusedParams& p, int qbits, bool s_f16, bool x_bf16, int grid, size_t smem,
+                         cudaStream_t s) {
+    if (qbits == 8) {
+        if (s_f16) return x_bf16 ? launch_fused_t<8, __half, __nv_bfloat16>(p, grid, smem, s)
+                                  : launch_fused_t<8, __half, float>(p, grid, smem, s);
+        return x_bf16 ? launch_fused_t<8, float, __nv_bfloat16>(p, grid, smem, s)
+                      : launch_fused_t<8, float, float>(p, grid, smem, s);
+    }
+    if (s_f16) return x_bf16 ? launch_fused_t<4, __half, __nv_bfloat16>(p, grid, smem, s)
+                              : launch_fused_t<4, __half, float>(p, grid, smem, s);
+    return x_bf16 ? launch_fused_t<4, float, __nv_bfloat16>(p, grid, smem, s)
+                  : launch_fused_t<4, float, float>(p, grid, smem, s);
+}
+
+}  // namespace moe

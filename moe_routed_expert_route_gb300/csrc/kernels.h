@@ -101,6 +101,28 @@ struct SubstituteParams {
     float* mass;
 };
 
+struct FusedParams {
+    int E, D, F, k, norm_topk, has_router, router_nseg, rows;
+    const void* W;            // router [E][D], same dtype as x
+    const float* bias;
+    const void* x;            // [1][D]
+    const void *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
+    const int32_t* idx_in;    // [k] when has_router == 0
+    const float* w_in;
+    int32_t* idx;             // [k] out when has_router
+    float* w;
+    float* probs;             // [E] or null
+    float* y;                 // [D]
+    void* x_next;             // [D] or null
+    WsHeader* hdr;
+    float* logits;            // workspace [E]
+    float* h;                 // workspace [k][F]
+};
+
+bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes, bool has_router,
+                FusedParams* fp, size_t* smem, int* grid);
+cudaError_t launch_fused(const FusedParams& p, int qbits, bool s_f16, bool x_bf16, int grid, size_t smem,
+                         cudaStream_t s);
 cudaError_t launch_router(const RouterParams& p, bool w_bf16, bool x_bf16, cudaStream_t s, bool pdl);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_experts(const ExpertParams& p, cudaStream_t s);

@@ -133,6 +133,59 @@ def test_ragged_shapes(qbits, scale, x_dtype, rdt, shape):
     check_y(layer, x, got, cfg.qbits)
 
 
+@pytest.mark.parametrize("qbits,scale,x_dtype,rdt", [
+    (8, torch.float32, torch.float32, torch.float32),
+    (8, torch.float16, torch.bfloat16, torch.bfloat16),
+    (4, torch.float16, torch.bfloat16, torch.bfloat16),
+    (4, torch.float32, torch.float32, torch.float32),
+])
+@pytest.mark.parametrize("shape", [(8, 2, 64, 128), (13, 3, 96, 256), (300, 7, 1024, 512),
+                                   (16, 16, 2048, 256), (1, 1, 32, 128), (256, 8, 2048, 768)])
+def test_single_token_layer(qbits, scale, x_dtype, rdt, shape):
+    """T = 1 runs the persistent one-launch layer kernel (grid barriers, bulk
+    copies of the down rows) wherever its shape rules allow."""
+    E, k, D, F = shape
+    cfg = small_cfg(E, k, D, F, qbits, scale, x_dtype, rdt, zipf=1.1, sigma=0.1, cfg_id=80 + qbits)
+    layer = W.make_layer(cfg, 0, DEV)
+    for stream in range(3):
+        x = W.make_tokens(cfg, 1, stream, DEV)
+        got = gpu_layer(cfg, layer, x, x_next=True)
+        ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
+        check_routing(ref, got, cfg.k, max_skip_frac=1.0)
+        check_y(layer, x, got, cfg.qbits)
+        assert torch.equal(got["x_next"], (x.cpu().float() + got["y"]).to(x.dtype))
+        # the same routing through moe_decode (no router phase)
+        experts = M.Experts.from_layer(layer, cfg.qbits)
+        y2 = torch.empty(1, D, dtype=torch.float32, device=DEV)
+        ws = M.workspace(M.MOE_OP_DECODE, 1, k, E, D, F, DEV)
+        M.moe_decode(experts, x, got["idx"].to(DEV), got["w"].to(DEV), y2, None, ws)
+        assert M.moe_check_status(ws) == M.MOE_OK
+        check_y(layer, x, dict(idx=got["idx"], w=got["w"], y=y2.cpu()), cfg.qbits)
+
+
+def test_single_token_repeated_launches_reuse_workspace():
+    """Back-to-back persistent launches on one workspace: the grid-barrier
+    counter must be back at zero after every launch."""
+    cfg = small_cfg(64, 4, 512, 256, cfg_id=90)
+    layer = W.make_layer(cfg, 0, DEV)
+    router = M.Router(layer["Wr"], layer["bias"], cfg.k)
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    ws = M.workspace(M.MOE_OP_LAYER, 1, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
+    xs = [W.make_tokens(cfg, 1, s, DEV) for s in range(20)]
+    outs = []
+    for x in xs:
+        idx = torch.empty(1, cfg.k, dtype=torch.int32, device=DEV)
+        w = torch.empty(1, cfg.k, device=DEV)
+        y = torch.empty(1, cfg.D, device=DEV)
+        M.moe_layer(router, experts, x, idx, w, None, y, None, ws)
+        outs.append((x, idx, w, y))
+    assert M.moe_check_status(ws) == M.MOE_OK
+    hdr = ws[:16].view(torch.int32).cpu().tolist()
+    assert hdr[1] == 0 and hdr[3] == 0, f"counters not reset: {hdr}"
+    for x, idx, w, y in outs[::5]:
+        check_y(layer, x, dict(idx=idx.cpu(), w=w.cpu(), y=y.cpu()), cfg.qbits)
+
+
 def test_k_equals_e_and_one_hot():
     cfg = small_cfg(8, 8, 64, 96, zipf=None, sigma=0.2, cfg_id=70)
     layer = W.make_layer(cfg, 0, DEV)
