@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe_route.h"
+#include "moe_route.h"
 
 namespace moe {
 

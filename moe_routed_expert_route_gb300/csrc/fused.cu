@@ -33,14 +33,16 @@ constexpr int kFWarps = 16;
 constexpr int kNRC = 2;  // router 16-byte chunks per lane
 constexpr int kNCH = 4;  // gate/up 16-byte chunks per lane
 constexpr int kNP = 4;   // down 8-byte pieces per lane
+constexpr int kHB = 12;  // activation blocks converted per warp per batch of loads
 
 struct FusedLayout {
-    size_t x, xhi, xlo, xs, dq, ds, h, part, total;
+    size_t x, xhi, xlo, xs, dq, ds, hhi, hlo, hs, part, p, total;
 };
 
 __host__ __device__ inline size_t fl_align(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline FusedLayout fused_layout(int D, int F, int k, int qbits, int s_bytes, int rows) {
+__host__ __device__ inline FusedLayout fused_layout(int E, int D, int F, int k, int qbits, int s_bytes,
+                                                   int rows) {
     FusedLayout L;
     size_t o = 0;
     const size_t rowF = qbits == 8 ? F : F / 2;
@@ -50,8 +52,11 @@ __host__ __device__ inline FusedLayout fused_layout(int D, int F, int k, int qbi
     L.xs = o;   o = fl_align(o + sizeof(float) * (D / kBlk), 16);
     L.dq = o;   o = fl_align(o + (size_t)k * rows * rowF, 16);
     L.ds = o;   o = fl_align(o + (size_t)k * rows * (F / kBlk) * s_bytes, 16);
-    L.h = o;    o = fl_align(o + sizeof(float) * (size_t)k * F, 16);
+    L.hhi = o;  o = fl_align(o + (size_t)k * F, 16);
+    L.hlo = o;  o = fl_align(o + (size_t)k * F, 16);
+    L.hs = o;   o = fl_align(o + sizeof(float) * (size_t)k * (F / kBlk), 16);
     L.part = o; o = fl_align(o + sizeof(float) * (size_t)k * rows, 16);
+    L.p = o;    o = fl_align(o + sizeof(float) * (E + 4), 16);
     L.total = o;
     return L;
 }
@@ -66,6 +71,7 @@ template <int QB, typename ST, typename XT, int NJ>
 __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p) {
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ float s_rpart[kFWarps];
+    __shared__ float s_red[33];
     __shared__ int s_idx[32];
     __shared__ float s_w[32];
     __shared__ int s_abort;
@@ -77,15 +83,18 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     const int nb = D / kBlk, nbF = F / kBlk;
     const int rowD = QB == 8 ? D : D / 2;    // bytes of a gate/up row
     const int rowF = QB == 8 ? F : F / 2;    // bytes of a down row
-    const FusedLayout L = fused_layout(D, F, k, QB, sizeof(ST), p.rows);
+    const FusedLayout L = fused_layout(p.E, D, F, k, QB, sizeof(ST), p.rows);
     float* s_x = reinterpret_cast<float*>(sm + L.x);
     int8_t* s_xhi = reinterpret_cast<int8_t*>(sm + L.xhi);
     uint8_t* s_xlo = sm + L.xlo;
     float* s_xs = reinterpret_cast<float*>(sm + L.xs);
     uint8_t* s_dq = sm + L.dq;
     ST* s_ds = reinterpret_cast<ST*>(sm + L.ds);
-    float* s_h = reinterpret_cast<float*>(sm + L.h);
+    int8_t* s_hhi = reinterpret_cast<int8_t*>(sm + L.hhi);
+    uint8_t* s_hlo = sm + L.hlo;
+    float* s_hs = reinterpret_cast<float*>(sm + L.hs);
     float* s_part = reinterpret_cast<float*>(sm + L.part);
+    float* s_p = reinterpret_cast<float*>(sm + L.p);
     int* status = &p.hdr->status;
     unsigned* bar = &p.hdr->bar;
 
@@ -150,20 +159,11 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
         grid_barrier(bar, (unsigned)G * (++nbar), status, &s_abort);
 
         // ------------------------------------------------------ phase 2
-        if (warp == 0) {
-            int sel_e;
-            float sel_p;
-            softmax_topk_warp<NJ>(p.logits, p.E, k, (c == 0) ? p.probs : nullptr, lane, sel_e, sel_p);
-            float norm = warp_sum(lane < k ? sel_p : 0.f);
-            float wv = p.norm_topk ? sel_p / norm : sel_p;
-            if (lane < k) {
-                s_idx[lane] = sel_e;
-                s_w[lane] = wv;
-                if (c == 0) {
-                    p.idx[lane] = sel_e;
-                    p.w[lane] = wv;
-                }
-            }
+        softmax_topk_block<kFThreads>(p.logits, p.E, k, p.norm_topk, (c == 0) ? p.probs : nullptr, s_p,
+                                      s_red, s_idx, s_w);
+        if (c == 0 && tid < k) {
+            p.idx[tid] = s_idx[tid];
+            p.w[tid] = s_w[tid];
         }
     } else if (tid < k) {
         int e = ld_cg_i32(p.idx_in + tid);
@@ -179,7 +179,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     // ---------------------------------------------------------- phase 3
     const int d_begin = (int)((long)c * D / G), d_end = (int)((long)(c + 1) * D / G);
     const int nrows = d_end - d_begin;
-    if (tid == 0) {
+    // bulk copies of this CTA's down rows; started once the first gate/up rows
+    // are on their way, so the gate/up bytes (needed first) are requested first
+    auto issue_down = [&]() {
         unsigned bytes = 0;
         for (int r = 0; r < k; r++)
             if (s_idx[r] >= 0) bytes += nrows * (rowF + nbF * (int)sizeof(ST));
@@ -195,7 +197,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                 bulk_g2s(s_ds + (size_t)r * p.rows * nbF, DS + row0 * nbF, nrows * nbF * (int)sizeof(ST), &s_bar);
             }
         }
-    }
+    };
+    bool down_issued = false;
 
     const uint8_t* GQ = reinterpret_cast<const uint8_t*>(p.gate_q);
     const uint8_t* UQ = reinterpret_cast<const uint8_t*>(p.up_q);
@@ -260,6 +263,10 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
         RowPair<QB, ST> A, B;
         int g = g_begin + warp;
         load_pair(g, A);
+        if (tid == 0) {
+            issue_down();
+            down_issued = true;
+        }
         while (g < g_end) {
             int g2 = g + kFWarps;
             load_pair(g2, B);
@@ -274,9 +281,25 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     grid_barrier(bar, (unsigned)G * (++nbar), status, &s_abort);
 
     // ---------------------------------------------------------- phase 4
-    for (int i = tid * 4; i < k * F; i += kFThreads * 4) {
-        uint4 v = ld_cg16(p.h + i);
-        *reinterpret_cast<uint4*>(s_h + i) = v;
+    // the k*F activations -> 16-bit fixed point (blocks of 32 along F); the
+    // loads of a batch are all issued before the first is used
+    (void)down_issued;
+    {
+        const int nblk = k * nbF;
+        for (int base = warp; base < nblk; base += kFWarps * kHB) {
+            float hv[kHB];
+#pragma unroll
+            for (int i = 0; i < kHB; i++) {
+                int blk = base + kFWarps * i;
+                hv[i] = blk < nblk ? ld_cg_f32(p.h + (size_t)blk * kBlk + lane) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < kHB; i++) {
+                int blk = base + kFWarps * i;
+                if (blk < nblk)
+                    fx_store_block(hv[i], lane, QB, s_hhi + blk * kBlk, s_hlo + blk * kBlk, s_hs + blk);
+            }
+        }
     }
     mbar_wait(&s_bar, 0, status);
     __syncthreads();
@@ -284,15 +307,21 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     const int wps = kFWarps / k;  // warps per slot (k <= 16)
     const int slot = warp / wps, sub = warp - slot * wps;
     if (slot < k && s_idx[slot] >= 0) {
-        constexpr int EPP = QB == 8 ? 8 : 16;  // elements per 8-byte piece
+        constexpr int PB = QB == 8 ? 8 : 16;  // elements (= plane bytes) per 8-byte piece of codes
+        constexpr int PW = PB / 4;            // plane words per piece
         const int npieces = rowF / 8;
-        float hreg[kNP][EPP];
+        uint32_t hh[kNP][PW], hl[kNP][PW];
+        float hsc[kNP];
 #pragma unroll
         for (int i = 0; i < kNP; i++) {
             int pc = i * 32 + lane;
+            const bool ok = pc < npieces;
 #pragma unroll
-            for (int q = 0; q < EPP; q++)
-                hreg[i][q] = pc < npieces ? s_h[slot * F + pc * EPP + q] : 0.f;
+            for (int q = 0; q < PW; q++) {
+                hh[i][q] = ok ? reinterpret_cast<const uint32_t*>(s_hhi + slot * F + PB * pc)[q] : 0u;
+                hl[i][q] = ok ? reinterpret_cast<const uint32_t*>(s_hlo + slot * F + PB * pc)[q] : 0u;
+            }
+            hsc[i] = ok ? s_hs[slot * nbF + (PB * pc) / kBlk] * (QB == 8 ? 1.0f : 1.0f / 16.0f) : 0.f;
         }
         const uint8_t* dq0 = s_dq + (size_t)slot * p.rows * rowF;
         const ST* ds0 = s_ds + (size_t)slot * p.rows * nbF;
@@ -303,24 +332,16 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                 int pc = i * 32 + lane;
                 if (pc < npieces) {
                     uint2 wv = *reinterpret_cast<const uint2*>(dq0 + (size_t)row * rowF + 8 * pc);
-                    float s = to_f32(ds0[row * nbF + (pc * EPP) / kBlk]);
-                    float dot = 0.f;
+                    float s = to_f32(ds0[row * nbF + (PB * pc) / kBlk]);
+                    int h = 0, l = 0;
                     if constexpr (QB == 8) {
-#pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            uint32_t wd = q < 4 ? wv.x : wv.y;
-                            int code = (int)(int8_t)((wd >> (8 * (q & 3))) & 0xff);
-                            dot = fmaf((float)code, hreg[i][q], dot);
-                        }
+                        h = dp4a_ss(wv.x, hh[i][0], dp4a_ss(wv.y, hh[i][1], 0));
+                        l = dp4a_su(wv.x, hl[i][0], dp4a_su(wv.y, hl[i][1], 0));
                     } else {
-#pragma unroll
-                        for (int q = 0; q < 16; q++) {
-                            uint32_t wd = q < 8 ? wv.x : wv.y;
-                            int code = ((int)(wd << (28 - 4 * (q & 7)))) >> 28;
-                            dot = fmaf((float)code, hreg[i][q], dot);
-                        }
+                        dot_i4_word(wv.x, hh[i][0], hh[i][1], hl[i][0], hl[i][1], h, l);
+                        dot_i4_word(wv.y, hh[i][2], hh[i][3], hl[i][2], hl[i][3], h, l);
                     }
-                    acc = fmaf(s, dot, acc);
+                    acc = fmaf((float)(h * 256 + l), s * hsc[i], acc);
                 }
             }
             acc = warp_sum(acc);
@@ -382,7 +403,7 @@ bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes,
     } else {
         fp->router_nseg = 1;
     }
-    FusedLayout L = fused_layout(D, F, k, qbits, s_bytes, rows);
+    FusedLayout L = fused_layout(E, D, F, k, qbits, s_bytes, rows);
     if (L.total > 200 * 1024) return false;
     fp->rows = rows;
     *smem = L.total;
