@@ -3,6 +3,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cmath>
 
 #include "kernels.h"
@@ -34,7 +35,8 @@ Layout layout(int op, int T, int k, int E, int D, int F) {
     };
     const bool route = op == MOE_OP_ROUTE || op == MOE_OP_LAYER;
     const bool experts = op == MOE_OP_DECODE || op == MOE_OP_LAYER;
-    if (route) L.logits = take(sizeof(float) * (size_t)T * E);
+    // logits and h are sized for 64-bit tagged values (single-token layer kernel)
+    if (route) L.logits = take(sizeof(uint64_t) * (size_t)T * E);
     if (experts) {
         size_t ng = (size_t)std::min(T * k, E);
         L.xq_hi = take((size_t)T * D);
@@ -43,7 +45,7 @@ Layout layout(int op, int T, int k, int E, int D, int F) {
         L.grp_expert = take(sizeof(int32_t) * ng);
         L.grp_off = take(sizeof(int32_t) * (ng + 1));
         L.assign = take(sizeof(int32_t) * (size_t)T * k);
-        L.h = take(sizeof(float) * (size_t)T * k * F);
+        L.h = take(sizeof(uint64_t) * (size_t)T * k * F);
     }
     L.total = off;
     return L;
@@ -155,8 +157,8 @@ FusedParams fused_params(const moe_experts_t* X, const void* x, int k, float* y,
     f.y = y;
     f.x_next = x_next;
     f.hdr = at<WsHeader>(ws, 0);
-    f.logits = L.logits ? at<float>(ws, L.logits) : nullptr;
-    f.h = at<float>(ws, L.h);
+    f.logits = L.logits ? at<uint64_t>(ws, L.logits) : nullptr;
+    f.h = at<uint64_t>(ws, L.h);
     return f;
 }
 
@@ -304,9 +306,10 @@ moe_status_t moe_check_status(void* workspace, void* stream) {
     int st = 0;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-    // after a device-side problem the launch may have left its counters
-    // mid-way: clear the whole header, not only the status word
-    size_t clear = st != 0 ? sizeof(WsHeader) : sizeof(int);
+    // after a device-side problem a launch may have left its counters mid-way:
+    // clear status, router counter, group count and barrier counter (the
+    // launch sequence number keeps counting up)
+    size_t clear = st != 0 ? offsetof(WsHeader, seq) : sizeof(int);
     if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     return static_cast<moe_status_t>(st);

@@ -16,14 +16,16 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // ------------------------------------------------------------ workspace header
 // The first 256 bytes of every workspace: device status word, the router's
-// "CTAs finished" counter, the number of distinct routed experts and the grid
-// barrier counter. Counters are back at zero when a launch ends.
+// "CTAs finished" counter, the number of distinct routed experts, a grid
+// barrier counter (back at zero when a launch ends) and the launch sequence
+// number that tags values exchanged between CTAs of the persistent kernel.
 struct WsHeader {
     int status;
     unsigned int done;
     int n_groups;
-    unsigned int bar;  // grid-barrier counter of the persistent layer kernel
-    int pad[60];
+    unsigned int bar;  // grid-barrier counter (kept at zero between launches)
+    unsigned int seq;  // launch sequence number of the persistent layer kernel
+    int pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -6,20 +6,23 @@
 // share x, down takes each slot's own activation, and the slots are combined
 // with the routing weights.
 //
-// Grid = one CTA of 16 warps per SM, all resident. Phases:
+// Grid = one CTA of 16 warps per SM, all resident. The CTAs exchange two small
+// vectors through L2, each value tagged with the launch's sequence number so
+// that readers poll the data itself instead of meeting at a grid barrier:
 //   0  before waiting on the previous launch: each CTA loads its slice of the
 //      router weights (1-4 experts' rows) into registers
-//   1  x -> shared memory (fp32) and its 16-bit fixed-point planes; the CTA's
-//      router logits -> workspace                       [grid barrier 1]
-//   2  every CTA reads all E logits and runs the softmax + top-k itself (no
-//      second exchange is needed to learn the routing)
+//   1  x -> shared memory; the CTA's logits -> workspace (tagged)
+//   2  warp 0 of every CTA polls all E logits and runs the softmax + top-k
+//      (no second exchange is needed to learn the routing); the other warps
+//      turn x into 16-bit fixed-point planes meanwhile
 //   3  one thread starts bulk (TMA) copies of this CTA's rows of the k down
-//      matrices into shared memory; meanwhile the 16 warps stream this CTA's
-//      share of the k*F gate/up row pairs from HBM (two row pairs in flight per
-//      warp) and write h = silu(g)*u to the workspace  [grid barrier 2]
-//   4  the k*F activations -> shared memory; each warp owns one slot and some
-//      of the CTA's rows, dots them against the staged down rows; the CTA then
-//      combines the k slots in slot order: y[d] = sum_r w[r]*o_r[d]; x_next.
+//      matrices into shared memory; the 16 warps stream this CTA's share of
+//      the k*F gate/up row pairs from HBM (two row pairs in flight per warp)
+//      and write h = silu(g)*u to the workspace (tagged)
+//   4  every CTA polls all k*F activations into fixed-point planes; each warp
+//      owns one slot and some of the CTA's rows, dots them against the staged
+//      down rows; the CTA combines the k slots in slot order,
+//      y[d] = sum_r w[r] * o_r[d], and writes x_next = x + y.
 // Without a router (moe_decode) phases 0-2 are replaced by reading idx/w.
 #include "dots.cuh"
 #include "group.cuh"
@@ -34,15 +37,15 @@ constexpr int kNRC = 2;  // router 16-byte chunks per lane
 constexpr int kNCH = 4;  // gate/up 16-byte chunks per lane
 constexpr int kNP = 4;   // down 8-byte pieces per lane
 constexpr int kHB = 12;  // activation blocks converted per warp per batch of loads
+constexpr int kRU = 4;   // down rows reduced together
 
 struct FusedLayout {
-    size_t x, xhi, xlo, xs, dq, ds, hhi, hlo, hs, part, p, total;
+    size_t x, xhi, xlo, xs, dq, ds, hhi, hlo, hs, part, total;
 };
 
 __host__ __device__ inline size_t fl_align(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline FusedLayout fused_layout(int E, int D, int F, int k, int qbits, int s_bytes,
-                                                   int rows) {
+__host__ __device__ inline FusedLayout fused_layout(int D, int F, int k, int qbits, int s_bytes, int rows) {
     FusedLayout L;
     size_t o = 0;
     const size_t rowF = qbits == 8 ? F : F / 2;
@@ -56,7 +59,6 @@ __host__ __device__ inline FusedLayout fused_layout(int E, int D, int F, int k, 
     L.hlo = o;  o = fl_align(o + (size_t)k * F, 16);
     L.hs = o;   o = fl_align(o + sizeof(float) * (size_t)k * (F / kBlk), 16);
     L.part = o; o = fl_align(o + sizeof(float) * (size_t)k * rows, 16);
-    L.p = o;    o = fl_align(o + sizeof(float) * (E + 4), 16);
     L.total = o;
     return L;
 }
@@ -67,14 +69,39 @@ struct RowPair {
     float gs[kNCH], us[kNCH];
 };
 
+// Fixed-point conversion of NB blocks of 32 values held one per lane, the
+// NB max-reductions interleaved so their shuffles overlap.
+template <int NB>
+__device__ __forceinline__ void fx_store_blocks(const float (&v)[NB], const int (&blk)[NB], int nblk, int lane,
+                                                int qbits, int8_t* hi, uint8_t* lo, float* scale) {
+    float m[NB];
+#pragma unroll
+    for (int i = 0; i < NB; i++) m[i] = fabsf(v[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < NB; i++) m[i] = fmaxf(m[i], __shfl_xor_sync(kFull, m[i], o));
+#pragma unroll
+    for (int i = 0; i < NB; i++) {
+        if (blk[i] < nblk) {
+            Fx f = fx_of_blockmax(m[i]);
+            int X = fx_code(v[i], f.mul);
+            int pos = blk[i] * kBlk + fx_pos(lane, qbits);
+            hi[pos] = (int8_t)(X >> 8);
+            lo[pos] = (uint8_t)(X & 0xff);
+            if (lane == 0) scale[blk[i]] = f.scale;
+        }
+    }
+}
+
 template <int QB, typename ST, typename XT, int NJ>
 __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p) {
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ float s_rpart[kFWarps];
-    __shared__ float s_red[33];
     __shared__ int s_idx[32];
     __shared__ float s_w[32];
     __shared__ int s_abort;
+    __shared__ unsigned s_seq;
     __shared__ __align__(8) uint64_t s_bar;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -83,7 +110,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     const int nb = D / kBlk, nbF = F / kBlk;
     const int rowD = QB == 8 ? D : D / 2;    // bytes of a gate/up row
     const int rowF = QB == 8 ? F : F / 2;    // bytes of a down row
-    const FusedLayout L = fused_layout(p.E, D, F, k, QB, sizeof(ST), p.rows);
+    const FusedLayout L = fused_layout(D, F, k, QB, sizeof(ST), p.rows);
     float* s_x = reinterpret_cast<float*>(sm + L.x);
     int8_t* s_xhi = reinterpret_cast<int8_t*>(sm + L.xhi);
     uint8_t* s_xlo = sm + L.xlo;
@@ -94,9 +121,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     uint8_t* s_hlo = sm + L.hlo;
     float* s_hs = reinterpret_cast<float*>(sm + L.hs);
     float* s_part = reinterpret_cast<float*>(sm + L.part);
-    float* s_p = reinterpret_cast<float*>(sm + L.p);
     int* status = &p.hdr->status;
-    unsigned* bar = &p.hdr->bar;
 
     // ---------------------------------------------------------- phase 0
     if (tid == 0) {
@@ -122,14 +147,32 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     __syncthreads();
     pdl_wait();
     pdl_trigger();
+    // the previous launch on this workspace has completed: its sequence
+    // number increment is visible
+    if (tid == 0) s_seq = *reinterpret_cast<volatile unsigned*>(&p.hdr->seq);
 
     // ---------------------------------------------------------- phase 1
     const XT* X = reinterpret_cast<const XT*>(p.x);
     for (int i = tid; i < D; i += kFThreads) s_x[i] = ldcg_f32(X + i);
     __syncthreads();
-    for (int b = warp; b < nb; b += kFWarps)
-        fx_store_block(s_x[b * kBlk + lane], lane, QB, s_xhi + b * kBlk, s_xlo + b * kBlk, s_xs + b);
-    int nbar = 0;
+    const unsigned tag = seq_tag(s_seq);
+
+    // x -> fixed-point planes, by warps first..15 (warp 0 is busy with the
+    // routing when there is a router)
+    auto convert_x = [&](int first) {
+        const int nw = kFWarps - first;
+        for (int b0 = warp - first; b0 < nb; b0 += nw * 4) {
+            float v[4];
+            int blk[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                blk[i] = b0 + nw * i;
+                v[i] = blk[i] < nb ? s_x[blk[i] * kBlk + lane] : 0.f;
+            }
+            fx_store_blocks<4>(v, blk, nb, lane, QB, s_xhi, s_xlo, s_xs);
+        }
+    };
+
     if (p.has_router) {
         float acc = 0.f;
 #pragma unroll
@@ -154,25 +197,40 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
             float l = 0.f;
             for (int s = 0; s < nseg; s++) l += s_rpart[tid * nseg + s];
             if (p.bias) l += p.bias[e_begin + tid];
-            p.logits[e_begin + tid] = l;
+            st_tagged(p.logits + e_begin + tid, l, tag);
         }
-        grid_barrier(bar, (unsigned)G * (++nbar), status, &s_abort);
-
         // ------------------------------------------------------ phase 2
-        softmax_topk_block<kFThreads>(p.logits, p.E, k, p.norm_topk, (c == 0) ? p.probs : nullptr, s_p,
-                                      s_red, s_idx, s_w);
-        if (c == 0 && tid < k) {
-            p.idx[tid] = s_idx[tid];
-            p.w[tid] = s_w[tid];
+        if (warp == 0) {
+            float lg[NJ];
+            ld_tagged_all<NJ>(p.logits, lane, 32, p.E, tag, lg, status, &s_abort);
+            int sel_e;
+            float sel_p;
+            softmax_topk_regs<NJ>(lg, p.E, k, (c == 0) ? p.probs : nullptr, lane, sel_e, sel_p);
+            if (sel_e < 0 || sel_e >= p.E) sel_e = -1;  // only after a timed-out poll; never dereferenced
+            float norm = warp_sum(lane < k ? sel_p : 0.f);
+            float wv = p.norm_topk ? sel_p / norm : sel_p;
+            if (lane < k) {
+                s_idx[lane] = sel_e;
+                s_w[lane] = wv;
+                if (c == 0) {
+                    p.idx[lane] = sel_e;
+                    p.w[lane] = wv;
+                }
+            }
+        } else {
+            convert_x(1);
         }
-    } else if (tid < k) {
-        int e = ld_cg_i32(p.idx_in + tid);
-        if (e < 0 || e >= p.E) {
-            if (c == 0) record_error(status, MOE_ERR_BAD_INDEX);
-            e = -1;
+    } else {
+        if (tid < k) {
+            int e = ld_cg_i32(p.idx_in + tid);
+            if (e < 0 || e >= p.E) {
+                if (c == 0) record_error(status, MOE_ERR_BAD_INDEX);
+                e = -1;
+            }
+            s_idx[tid] = e;
+            s_w[tid] = ld_cg_f32(p.w_in + tid);
         }
-        s_idx[tid] = e;
-        s_w[tid] = ld_cg_f32(p.w_in + tid);
+        convert_x(0);
     }
     __syncthreads();
 
@@ -198,7 +256,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
             }
         }
     };
-    bool down_issued = false;
 
     const uint8_t* GQ = reinterpret_cast<const uint8_t*>(p.gate_q);
     const uint8_t* UQ = reinterpret_cast<const uint8_t*>(p.up_q);
@@ -210,8 +267,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
 
     auto load_pair = [&](int g, RowPair<QB, ST>& rp) {
         int r = g / F, n = g - r * F;
-        int e = s_idx[r];
-        bool ok = g < g_end && e >= 0;
+        int e = g < g_end ? s_idx[r] : -1;
+        bool ok = e >= 0;
         size_t row = (size_t)(ok ? e : 0) * F + n;
 #pragma unroll
         for (int j = 0; j < kNCH; j++) {
@@ -254,19 +311,19 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                 ua = fmaf((float)iu, rp.us[j] * xs, ua);
             }
         }
-        ga = warp_sum(ga);
-        ua = warp_sum(ua);
-        if (lane == 0) p.h[g] = silu_mul(ga, ua);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {  // both reductions interleaved
+            ga += __shfl_xor_sync(kFull, ga, o);
+            ua += __shfl_xor_sync(kFull, ua, o);
+        }
+        if (lane == 0 && g < g_end) st_tagged(p.h + g, silu_mul(ga, ua), tag);
     };
 
     {
         RowPair<QB, ST> A, B;
         int g = g_begin + warp;
         load_pair(g, A);
-        if (tid == 0) {
-            issue_down();
-            down_issued = true;
-        }
+        if (tid == 0) issue_down();
         while (g < g_end) {
             int g2 = g + kFWarps;
             load_pair(g2, B);
@@ -278,27 +335,20 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
             g = g3;
         }
     }
-    grid_barrier(bar, (unsigned)G * (++nbar), status, &s_abort);
 
     // ---------------------------------------------------------- phase 4
-    // the k*F activations -> 16-bit fixed point (blocks of 32 along F); the
-    // loads of a batch are all issued before the first is used
-    (void)down_issued;
+    // the k*F activations of this launch (tagged) -> 16-bit fixed point per
+    // block of 32 along F; a warp takes kHB blocks per round, all loads in
+    // flight together and their max-reductions interleaved
     {
         const int nblk = k * nbF;
         for (int base = warp; base < nblk; base += kFWarps * kHB) {
             float hv[kHB];
+            int blk[kHB];
 #pragma unroll
-            for (int i = 0; i < kHB; i++) {
-                int blk = base + kFWarps * i;
-                hv[i] = blk < nblk ? ld_cg_f32(p.h + (size_t)blk * kBlk + lane) : 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < kHB; i++) {
-                int blk = base + kFWarps * i;
-                if (blk < nblk)
-                    fx_store_block(hv[i], lane, QB, s_hhi + blk * kBlk, s_hlo + blk * kBlk, s_hs + blk);
-            }
+            for (int i = 0; i < kHB; i++) blk[i] = base + kFWarps * i;
+            ld_tagged_all<kHB>(p.h, base * kBlk + lane, kFWarps * kBlk, nblk * kBlk, tag, hv, status, &s_abort);
+            fx_store_blocks<kHB>(hv, blk, nblk, lane, QB, s_hhi, s_hlo, s_hs);
         }
     }
     mbar_wait(&s_bar, 0, status);
@@ -325,27 +375,43 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
         }
         const uint8_t* dq0 = s_dq + (size_t)slot * p.rows * rowF;
         const ST* ds0 = s_ds + (size_t)slot * p.rows * nbF;
-        for (int row = sub; row < nrows; row += wps) {
-            float acc = 0.f;
+        for (int row0 = sub; row0 < nrows; row0 += wps * kRU) {
+            float acc[kRU];
 #pragma unroll
-            for (int i = 0; i < kNP; i++) {
-                int pc = i * 32 + lane;
-                if (pc < npieces) {
-                    uint2 wv = *reinterpret_cast<const uint2*>(dq0 + (size_t)row * rowF + 8 * pc);
-                    float s = to_f32(ds0[row * nbF + (PB * pc) / kBlk]);
-                    int h = 0, l = 0;
-                    if constexpr (QB == 8) {
-                        h = dp4a_ss(wv.x, hh[i][0], dp4a_ss(wv.y, hh[i][1], 0));
-                        l = dp4a_su(wv.x, hl[i][0], dp4a_su(wv.y, hl[i][1], 0));
-                    } else {
-                        dot_i4_word(wv.x, hh[i][0], hh[i][1], hl[i][0], hl[i][1], h, l);
-                        dot_i4_word(wv.y, hh[i][2], hh[i][3], hl[i][2], hl[i][3], h, l);
+            for (int u = 0; u < kRU; u++) {
+                const int row = row0 + u * wps;
+                acc[u] = 0.f;
+                if (row < nrows) {
+#pragma unroll
+                    for (int i = 0; i < kNP; i++) {
+                        int pc = i * 32 + lane;
+                        if (pc < npieces) {
+                            uint2 wv = *reinterpret_cast<const uint2*>(dq0 + (size_t)row * rowF + 8 * pc);
+                            float sc = to_f32(ds0[row * nbF + (PB * pc) / kBlk]);
+                            int h = 0, l = 0;
+                            if constexpr (QB == 8) {
+                                h = dp4a_ss(wv.x, hh[i][0], dp4a_ss(wv.y, hh[i][1], 0));
+                                l = dp4a_su(wv.x, hl[i][0], dp4a_su(wv.y, hl[i][1], 0));
+                            } else {
+                                dot_i4_word(wv.x, hh[i][0], hh[i][1], hl[i][0], hl[i][1], h, l);
+                                dot_i4_word(wv.y, hh[i][2], hh[i][3], hl[i][2], hl[i][3], h, l);
+                            }
+                            acc[u] = fmaf((float)(h * 256 + l), sc * hsc[i], acc[u]);
+                        }
                     }
-                    acc = fmaf((float)(h * 256 + l), s * hsc[i], acc);
                 }
             }
-            acc = warp_sum(acc);
-            if (lane == 0) s_part[row * k + slot] = acc;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int u = 0; u < kRU; u++) acc[u] += __shfl_xor_sync(kFull, acc[u], o);
+            if (lane == 0) {
+#pragma unroll
+                for (int u = 0; u < kRU; u++) {
+                    const int row = row0 + u * wps;
+                    if (row < nrows) s_part[row * k + slot] = acc[u];
+                }
+            }
         }
     }
     __syncthreads();
@@ -362,7 +428,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                 reinterpret_cast<float*>(p.x_next)[d] = s_x[d] + y;
         }
     }
-    grid_exit(bar, (unsigned)G * (nbar + 1));
+    // every CTA read the sequence number before producing anything CTA 0
+    // waited for, so CTA 0 may advance it for the next launch
+    if (c == 0 && tid == 0) atomicAdd(&p.hdr->seq, 1u);
 }
 
 // ------------------------------------------------------------- host side
@@ -403,7 +471,7 @@ bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes,
     } else {
         fp->router_nseg = 1;
     }
-    FusedLayout L = fused_layout(E, D, F, k, qbits, s_bytes, rows);
+    FusedLayout L = fused_layout(D, F, k, qbits, s_bytes, rows);
     if (L.total > 200 * 1024) return false;
     fp->rows = rows;
     *smem = L.total;

@@ -79,22 +79,18 @@ __device__ inline void group_assignments(const int32_t* __restrict__ idx, int n,
     __syncthreads();
 }
 
-// Softmax and top-k of one token, by one warp. Lane l holds logits of experts
-// l, l+32, ... (NJ per lane, NJ*32 >= E). Probabilities are
+// Softmax and top-k of one token, by one warp, from logits already in
+// registers: lane l holds the logits of experts l, l+32, ... (NJ per lane,
+// NJ*32 >= E; entries e >= E are ignored). Probabilities are
 // p_e = exp(l_e - max) / sum; the k largest are chosen largest first, equal
 // fp32 values by lower expert id. Lanes r < k return (sel_e, sel_p) of rank r.
 template <int NJ>
-__device__ __forceinline__ void softmax_topk_warp(const float* __restrict__ logits_t, int E, int k,
-                                                  float* __restrict__ probs_t, int lane,
-                                                  int& sel_e, float& sel_p) {
-    float p[NJ];
+__device__ __forceinline__ void softmax_topk_regs(float (&p)[NJ], int E, int k, float* __restrict__ probs_t,
+                                                  int lane, int& sel_e, float& sel_p) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < NJ; j++) {
-        int e = j * 32 + lane;
-        p[j] = (e < E) ? ld_cg_f32(logits_t + e) : -INFINITY;
-        mx = fmaxf(mx, p[j]);
-    }
+    for (int j = 0; j < NJ; j++)
+        if (j * 32 + lane < E) mx = fmaxf(mx, p[j]);
     mx = warp_max(mx);
     float s = 0.f;
 #pragma unroll
@@ -130,89 +126,18 @@ __device__ __forceinline__ void softmax_topk_warp(const float* __restrict__ logi
     }
 }
 
-// Softmax and top-k of one token by a whole CTA (NT threads, NT >= 64, a
-// multiple of 32). Probabilities p_e = exp(l_e - max) / sum are computed once;
-// then every expert's rank among them is counted directly,
-//   rank(e) = #{j : p_j > p_e} + #{j < e : p_j == p_e},
-// so rank is the position in the order "largest first, lower id on ties",
-// and the experts of rank < k are the top k in that order. Two threads share
-// the count of one expert (each scans half of the experts). Writes s_idx[r],
-// s_w[r] for r < k (weights renormalised when norm_topk) and probs_out if
-// given. Scratch: s_p[E + 4] floats (16-byte aligned), s_red[33] floats.
-template <int NT>
-__device__ inline void softmax_topk_block(const float* __restrict__ logits, int E, int k, int norm_topk,
-                                          float* __restrict__ probs_out, float* s_p, float* s_red,
-                                          int* s_idx, float* s_w) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int NW = NT / 32;
-    float m = -INFINITY;
-    for (int e = tid; e < E; e += NT) {
-        float l = ld_cg_f32(logits + e);
-        s_p[e] = l;
-        m = fmaxf(m, l);
+// The same, reading the logits (written by an earlier kernel) through L2.
+template <int NJ>
+__device__ __forceinline__ void softmax_topk_warp(const float* __restrict__ logits_t, int E, int k,
+                                                  float* __restrict__ probs_t, int lane,
+                                                  int& sel_e, float& sel_p) {
+    float p[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; j++) {
+        int e = j * 32 + lane;
+        p[j] = (e < E) ? ld_cg_f32(logits_t + e) : -INFINITY;
     }
-    m = warp_max(m);
-    if (lane == 0) s_red[warp] = m;
-    __syncthreads();
-    if (tid == 0) {
-        float v = s_red[0];
-        for (int i = 1; i < NW; i++) v = fmaxf(v, s_red[i]);
-        s_red[32] = v;
-    }
-    __syncthreads();
-    m = s_red[32];
-    float sum = 0.f;
-    for (int e = tid; e < E; e += NT) {
-        float v = expf(s_p[e] - m);
-        s_p[e] = v;
-        sum += v;
-    }
-    sum = warp_sum(sum);
-    __syncthreads();
-    if (lane == 0) s_red[warp] = sum;
-    __syncthreads();
-    if (tid == 0) {
-        float v = 0.f;
-        for (int i = 0; i < NW; i++) v += s_red[i];
-        s_red[32] = v;
-    }
-    __syncthreads();
-    sum = s_red[32];
-    for (int e = tid; e < E; e += NT) {
-        float v = s_p[e] / sum;
-        s_p[e] = v;
-        if (probs_out) probs_out[e] = v;
-    }
-    if (tid < 4) s_p[E + tid] = -1.f;  // padding for the 4-wide scan, below every probability
-    __syncthreads();
-    const int half = (E + 7) / 8 * 4;  // multiple of 4
-    for (int base = 0; base < 2 * E; base += NT) {  // uniform trip count: the shuffle sees full warps
-        const int t = base + tid;
-        const bool valid = t < 2 * E;
-        const int e = valid ? (t >> 1) : 0, part = t & 1;
-        const float pe = s_p[e];
-        const int j0 = part * half, j1 = valid ? min(E, j0 + half) : j0;
-        int cnt = 0;
-        for (int j = j0; j < j1; j += 4) {
-            float4 q = *reinterpret_cast<const float4*>(s_p + j);
-            cnt += (q.x > pe) + (q.y > pe) + (q.z > pe) + (q.w > pe);
-            cnt += (q.x == pe && j < e) + (q.y == pe && j + 1 < e) + (q.z == pe && j + 2 < e) +
-                   (q.w == pe && j + 3 < e);
-        }
-        cnt += __shfl_xor_sync(kFull, cnt, 1);  // the other half of the same expert
-        if (valid && part == 0 && cnt < k) {
-            s_idx[cnt] = e;
-            s_w[cnt] = pe;
-        }
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float n = 0.f;
-        for (int r = 0; r < k; r++) n += s_w[r];
-        if (norm_topk)
-            for (int r = 0; r < k; r++) s_w[r] = s_w[r] / n;
-    }
-    __syncthreads();
+    softmax_topk_regs<NJ>(p, E, k, probs_t, lane, sel_e, sel_p);
 }
 
 }  // namespace moe

@@ -116,8 +116,8 @@ struct FusedParams {
     float* y;                 // [D]
     void* x_next;             // [D] or null
     WsHeader* hdr;
-    float* logits;            // workspace [E]
-    float* h;                 // workspace [k][F]
+    uint64_t* logits;         // workspace [E], tagged values
+    uint64_t* h;              // workspace [k][F], tagged values
 };
 
 bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes, bool has_router,

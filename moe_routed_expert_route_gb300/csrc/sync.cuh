@@ -1,4 +1,4 @@
-// mbarrier, bulk-copy (TMA) and grid-barrier helpers (sm_90+ PTX), all waits bounded.
+// mbarrier, bulk-copy (TMA) and inter-CTA exchange helpers (sm_90+ PTX), all waits bounded.
 #pragma once
 
 #include "common.cuh"
@@ -60,48 +60,63 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned phase, int* st
     return true;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+// Values exchanged between the CTAs of one launch carry a tag derived from the
+// launch's sequence number in the upper 32 bits of one 64-bit word, so a reader
+// can tell a value of this launch from a stale one without a separate barrier:
+// it polls the data itself. 64-bit aligned accesses are single-copy atomic.
+// The tag is a negative quiet-NaN bit pattern holding 22 bits of the sequence
+// number: zeroed memory and ordinary float data never look like a current tag.
+__device__ __forceinline__ unsigned seq_tag(unsigned seq) { return 0xFFC00000u | (seq & 0x3FFFFFu); }
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, unsigned tag) {
+    uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
 }
+__device__ __forceinline__ bool tag_ok(uint64_t w, unsigned tag) { return (unsigned)(w >> 32) == tag; }
+__device__ __forceinline__ float tag_val(uint64_t w) { return __uint_as_float((unsigned)w); }
 
-// Grid-wide barrier over a counter that only grows within a launch: barrier
-// number b (1, 2, ...) completes when the counter reaches b * nblocks. All CTAs
-// of the grid must be resident (one CTA per SM, grid <= SM count). The wait is
-// bounded: on timeout the status word records MOE_ERR_DEVICE_TIMEOUT, `*abort`
-// is set and the CTA goes on (its results are then not valid), so a broken
-// launch ends instead of hanging the GPU.
-__device__ __forceinline__ void grid_barrier(unsigned* counter, unsigned target, int* status, int* abort) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        red_release_add(counter, 1u);
-        if (!*abort) {
-            long long t0 = clock64();
-            while (ld_acquire_u32(counter) < target) {
-                if (clock64() - t0 > kSpinLimitCycles) {
-                    record_error(status, MOE_ERR_DEVICE_TIMEOUT);
-                    *abort = 1;
-                    break;
+// Reads n tagged values [i0, i0 + n*stride) of this launch into out[] (n is a
+// compile-time bound, entries with i >= limit read as 0), polling until every
+// value carries `tag`. Bounded: on timeout records MOE_ERR_DEVICE_TIMEOUT,
+// sets *abort and returns what it has.
+template <int N>
+__device__ __forceinline__ void ld_tagged_all(const uint64_t* base, int i0, int stride, int limit,
+                                              unsigned tag, float* out, int* status, int* abort) {
+    bool ready[N];
+#pragma unroll
+    for (int q = 0; q < N; q++) {
+        int i = i0 + q * stride;
+        ready[q] = i >= limit;
+        out[q] = 0.f;
+    }
+    long long t0 = clock64();
+    while (true) {
+        uint64_t w[N];
+#pragma unroll
+        for (int q = 0; q < N; q++)  // all loads in flight before the first is examined
+            if (!ready[q]) w[q] = ld_tagged(base + i0 + q * stride);
+        bool all = true;
+#pragma unroll
+        for (int q = 0; q < N; q++) {
+            if (!ready[q]) {
+                if (tag_ok(w[q], tag)) {
+                    ready[q] = true;
+                    out[q] = tag_val(w[q]);
+                } else {
+                    all = false;
                 }
             }
         }
-    }
-    __syncthreads();
-}
-
-// Last arrival of a launch: the CTA that brings the counter to `total` resets
-// it to zero for the next launch (every CTA has passed every barrier by then).
-__device__ __forceinline__ void grid_exit(unsigned* counter, unsigned total) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        unsigned prev = atomicAdd(counter, 1u);
-        if (prev == total - 1) atomicExch(counter, 0u);
+        if (all || *abort) break;
+        if (clock64() - t0 > kSpinLimitCycles) {
+            record_error(status, MOE_ERR_DEVICE_TIMEOUT);
+            *abort = 1;
+            break;
+        }
     }
 }
 
