@@ -3,7 +3,6 @@
 #include <stdint.h>
 
 #include <algorithm>
-#include <cstddef>
 #include <cmath>
 
 #include "kernels.h"
@@ -158,7 +157,7 @@ FusedParams fused_params(const moe_experts_t* X, const void* x, int k, float* y,
     f.x_next = x_next;
     f.hdr = at<WsHeader>(ws, 0);
     f.logits = L.logits ? at<uint64_t>(ws, L.logits) : nullptr;
-    f.h = at<uint64_t>(ws, L.h);
+    f.h = at<float>(ws, L.h);
     return f;
 }
 
@@ -307,9 +306,8 @@ moe_status_t moe_check_status(void* workspace, void* stream) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
     // after a device-side problem a launch may have left its counters mid-way:
-    // clear status, router counter, group count and barrier counter (the
-    // launch sequence number keeps counting up)
-    size_t clear = st != 0 ? offsetof(WsHeader, seq) : sizeof(int);
+    // clear the whole header (status, counters, launch sequence number)
+    size_t clear = st != 0 ? sizeof(WsHeader) : sizeof(int);
     if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     return static_cast<moe_status_t>(st);

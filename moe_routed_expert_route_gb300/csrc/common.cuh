@@ -23,9 +23,10 @@ struct WsHeader {
     int status;
     unsigned int done;
     int n_groups;
-    unsigned int bar;  // grid-barrier counter (kept at zero between launches)
+    unsigned int bar;  // unused, zero
     unsigned int seq;  // launch sequence number of the persistent layer kernel
-    int pad[59];
+    unsigned int hcount[2];  // CTAs done with their activations, by launch parity
+    int pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

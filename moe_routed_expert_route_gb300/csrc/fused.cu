@@ -7,8 +7,8 @@
 // with the routing weights.
 //
 // Grid = one CTA of 16 warps per SM, all resident. The CTAs exchange two small
-// vectors through L2, each value tagged with the launch's sequence number so
-// that readers poll the data itself instead of meeting at a grid barrier:
+// vectors through L2: the logits are tagged with the launch's sequence number
+// so that readers poll the data itself instead of meeting at a grid barrier:
 //   0  before waiting on the previous launch: each CTA loads its slice of the
 //      router weights (1-4 experts' rows) into registers
 //   1  x -> shared memory; the CTA's logits -> workspace (tagged)
@@ -18,8 +18,10 @@
 //   3  one thread starts bulk (TMA) copies of this CTA's rows of the k down
 //      matrices into shared memory; the 16 warps stream this CTA's share of
 //      the k*F gate/up row pairs from HBM (two row pairs in flight per warp)
-//      and write h = silu(g)*u to the workspace (tagged)
-//   4  every CTA polls all k*F activations into fixed-point planes; each warp
+//      and write h = silu(g)*u to the workspace; the CTA then arrives on a
+//      completion counter (polling ~150 KB of tagged activations from every
+//      CTA would flood L2 while other CTAs still stream)
+//   4  every CTA reads all k*F activations into fixed-point planes; each warp
 //      owns one slot and some of the CTA's rows, dots them against the staged
 //      down rows; the CTA combines the k slots in slot order,
 //      y[d] = sum_r w[r] * o_r[d], and writes x_next = x + y.
@@ -149,7 +151,10 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     pdl_trigger();
     // the previous launch on this workspace has completed: its sequence
     // number increment is visible
-    if (tid == 0) s_seq = *reinterpret_cast<volatile unsigned*>(&p.hdr->seq);
+    if (tid == 0) {
+        s_seq = *reinterpret_cast<volatile unsigned*>(&p.hdr->seq);
+        if (c == 0) p.hdr->hcount[(s_seq + 1) & 1] = 0u;  // the next launch's counter
+    }
 
     // ---------------------------------------------------------- phase 1
     const XT* X = reinterpret_cast<const XT*>(p.x);
@@ -316,7 +321,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
             ga += __shfl_xor_sync(kFull, ga, o);
             ua += __shfl_xor_sync(kFull, ua, o);
         }
-        if (lane == 0 && g < g_end) st_tagged(p.h + g, silu_mul(ga, ua), tag);
+        if (lane == 0 && g < g_end) p.h[g] = silu_mul(ga, ua);
     };
 
     {
@@ -337,17 +342,21 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     }
 
     // ---------------------------------------------------------- phase 4
-    // the k*F activations of this launch (tagged) -> 16-bit fixed point per
-    // block of 32 along F; a warp takes kHB blocks per round, all loads in
-    // flight together and their max-reductions interleaved
+    // wait for every CTA's activations (one counter per launch parity; the
+    // other one is cleared for the next launch), then all k*F of them ->
+    // 16-bit fixed point per block of 32 along F; a warp takes kHB blocks per
+    // round, all loads in flight together and their max-reductions interleaved
+    arrive_and_wait(&p.hdr->hcount[s_seq & 1], (unsigned)G, status, &s_abort);
     {
         const int nblk = k * nbF;
         for (int base = warp; base < nblk; base += kFWarps * kHB) {
             float hv[kHB];
             int blk[kHB];
 #pragma unroll
-            for (int i = 0; i < kHB; i++) blk[i] = base + kFWarps * i;
-            ld_tagged_all<kHB>(p.h, base * kBlk + lane, kFWarps * kBlk, nblk * kBlk, tag, hv, status, &s_abort);
+            for (int i = 0; i < kHB; i++) {
+                blk[i] = base + kFWarps * i;
+                hv[i] = blk[i] < nblk ? ld_cg_f32(p.h + (size_t)blk[i] * kBlk + lane) : 0.f;
+            }
             fx_store_blocks<kHB>(hv, blk, nblk, lane, QB, s_hhi, s_hlo, s_hs);
         }
     }

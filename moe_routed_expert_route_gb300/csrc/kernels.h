@@ -117,7 +117,7 @@ struct FusedParams {
     void* x_next;             // [D] or null
     WsHeader* hdr;
     uint64_t* logits;         // workspace [E], tagged values
-    uint64_t* h;              // workspace [k][F], tagged values
+    float* h;                 // workspace [k][F]
 };
 
 bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes, bool has_router,

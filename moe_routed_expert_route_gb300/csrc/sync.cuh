@@ -60,6 +60,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned phase, int* st
     return true;
 }
 
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Arrive on a completion counter and wait until `target` CTAs have arrived:
+// one thread per CTA polls one word. Bounded: on timeout records
+// MOE_ERR_DEVICE_TIMEOUT, sets *abort and returns (results are then invalid),
+// so a broken launch ends instead of hanging the GPU.
+__device__ __forceinline__ void arrive_and_wait(unsigned* counter, unsigned target, int* status, int* abort) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        red_release_add(counter, 1u);
+        if (!*abort) {
+            long long t0 = clock64();
+            while (ld_acquire_u32(counter) < target) {
+                if (clock64() - t0 > kSpinLimitCycles) {
+                    record_error(status, MOE_ERR_DEVICE_TIMEOUT);
+                    *abort = 1;
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
 // Values exchanged between the CTAs of one launch carry a tag derived from the
 // launch's sequence number in the upper 32 bits of one 64-bit word, so a reader
 // can tell a value of this launch from a stale one without a separate barrier:
