@@ -15,10 +15,10 @@
 //   2  warp 0 of every CTA polls all E logits and runs the softmax + top-k
 //      (no second exchange is needed to learn the routing); the other warps
 //      turn x into 16-bit fixed-point planes meanwhile
-//   3  one thread starts bulk (TMA) copies of this CTA's rows of the k down
-//      matrices into shared memory; the 16 warps stream this CTA's share of
-//      the k*F gate/up row pairs from HBM (two row pairs in flight per warp)
-//      and write h = silu(g)*u to the workspace; the CTA then arrives on a
+//   3  the 16 warps stream this CTA's share of the k*F gate/up row pairs from
+//      HBM (two row pairs in flight per warp) and write h = silu(g)*u to the
+//      workspace; one thread then starts bulk (TMA) copies of this CTA's rows
+//      of the k down matrices into shared memory, and the CTA arrives on a
 //      completion counter (polling ~150 KB of tagged activations from every
 //      CTA would flood L2 while other CTAs still stream)
 //   4  every CTA reads all k*F activations into fixed-point planes; each warp
@@ -242,8 +242,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     // ---------------------------------------------------------- phase 3
     const int d_begin = (int)((long)c * D / G), d_end = (int)((long)(c + 1) * D / G);
     const int nrows = d_end - d_begin;
-    // bulk copies of this CTA's down rows; started once the first gate/up rows
-    // are on their way, so the gate/up bytes (needed first) are requested first
+    // bulk copies of this CTA's down rows, started after this CTA's gate/up
+    // rows: those bytes are needed first, the down rows only after the
+    // activation exchange, which they overlap
     auto issue_down = [&]() {
         unsigned bytes = 0;
         for (int r = 0; r < k; r++)
@@ -328,7 +329,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
         RowPair<QB, ST> A, B;
         int g = g_begin + warp;
         load_pair(g, A);
-        if (tid == 0) issue_down();
         while (g < g_end) {
             int g2 = g + kFWarps;
             load_pair(g2, B);
@@ -340,6 +340,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
             g = g3;
         }
     }
+
+    // the down rows stream while the CTAs exchange activations
+    if (tid == 0) issue_down();
 
     // ---------------------------------------------------------- phase 4
     // wait for every CTA's activations (one counter per launch parity; the
@@ -490,10 +493,15 @@ bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes,
 
 template <int QB, typename ST, typename XT>
 static cudaError_t launch_fused_t(const FusedParams& p, int grid, size_t smem, cudaStream_t s) {
-    if (p.E <= 32) return launch(fused_layer_kernel<QB, ST, XT, 1>, dim3(grid), dim3(kFThreads), smem, s, true, p);
-    if (p.E <= 256) return launch(fused_layer_kernel<QB, ST, XT, 8>, dim3(grid), dim3(kFThreads), smem, s, true, p);
-    if (p.E <= 512) return launch(fused_layer_kernel<QB, ST, XT, 16>, dim3(grid), dim3(kFThreads), smem, s, true, p);
-    return launch(fused_layer_kernel<QB, ST, XT, 32>, dim3(grid), dim3(kFThreads), smem, s, true, p);
+    const dim3 g(grid), b(kFThreads);
+    switch (topk_nj(p.E, p.k)) {
+        case 1: return launch(fused_layer_kernel<QB, ST, XT, 1>, g, b, smem, s, true, p);
+        case 2: return launch(fused_layer_kernel<QB, ST, XT, 2>, g, b, smem, s, true, p);
+        case 4: return launch(fused_layer_kernel<QB, ST, XT, 4>, g, b, smem, s, true, p);
+        case 8: return launch(fused_layer_kernel<QB, ST, XT, 8>, g, b, smem, s, true, p);
+        case 16: return launch(fused_layer_kernel<QB, ST, XT, 16>, g, b, smem, s, true, p);
+        default: return launch(fused_layer_kernel<QB, ST, XT, 32>, g, b, smem, s, true, p);
+    }
 }
 
 cudaError_t launch_fused(const FusedParams& p, int qbits, bool s_f16, bool x_bf16, int grid, size_t smem,

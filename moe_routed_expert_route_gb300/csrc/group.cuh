@@ -5,6 +5,14 @@
 
 namespace moe {
 
+// Values per lane for the one-warp top-k: a power of two with NJ*32 >= E and NJ >= k.
+inline int topk_nj(int E, int k) {
+    int need = (E + 31) / 32 > k ? (E + 31) / 32 : k;
+    int nj = 1;
+    while (nj < need) nj <<= 1;
+    return nj;
+}
+
 // Groups the n routing assignments idx[0..n) (assignment i = token i/k, slot
 // i%k) by expert, inside ONE CTA:
 //   cnt[e]          number of assignments routed to e
@@ -79,11 +87,43 @@ __device__ inline void group_assignments(const int32_t* __restrict__ idx, int n,
     __syncthreads();
 }
 
+// In-register bitonic networks on N (a power of two) unsigned 64-bit values,
+// largest first. All indices are compile-time constants.
+__device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
+    uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+    a = hi;
+    b = lo;
+}
+template <int N>
+__device__ __forceinline__ void bitonic_merge_desc(uint64_t (&v)[N]) {
+#pragma unroll
+    for (int stride = N / 2; stride > 0; stride >>= 1)
+#pragma unroll
+        for (int i = 0; i < N; i++)
+            if ((i & stride) == 0) cas_desc(v[i], v[i + stride]);
+}
+template <int N>
+__device__ __forceinline__ void bitonic_sort_desc(uint64_t (&v)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+        for (int stride = size / 2; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < N; i++) {
+                const int j = i + stride;
+                if ((i & stride) == 0) {
+                    if ((i & size) == 0) cas_desc(v[i], v[j]);   // descending run
+                    else cas_desc(v[j], v[i]);                   // ascending run
+                }
+            }
+}
+
 // Softmax and top-k of one token, by one warp, from logits already in
-// registers: lane l holds the logits of experts l, l+32, ... (NJ per lane,
-// NJ*32 >= E; entries e >= E are ignored). Probabilities are
-// p_e = exp(l_e - max) / sum; the k largest are chosen largest first, equal
-// fp32 values by lower expert id. Lanes r < k return (sel_e, sel_p) of rank r.
+// registers: lane l holds the logits of experts l, l+32, ... (NJ per lane, a
+// power of two, NJ*32 >= E, NJ >= k; entries e >= E are ignored).
+// Probabilities are p_e = exp(l_e - max) / sum; the k largest are chosen
+// largest first, equal fp32 values by lower expert id. Lanes r < k return
+// (sel_e, sel_p) of rank r.
 template <int NJ>
 __device__ __forceinline__ void softmax_topk_regs(float (&p)[NJ], int E, int k, float* __restrict__ probs_t,
                                                   int lane, int& sel_e, float& sel_p) {
@@ -100,29 +140,45 @@ __device__ __forceinline__ void softmax_topk_regs(float (&p)[NJ], int E, int k, 
         s += p[j];
     }
     s = warp_sum(s);
-    unsigned key[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; j++) {
         int e = j * 32 + lane;
         p[j] = p[j] / s;
         if (e < E && probs_t) probs_t[e] = p[j];
-        key[j] = (e < E) ? __float_as_uint(p[j]) + 1u : 0u;  // p >= 0: bits are ordered
+    }
+    // selection: order key (fp32 bits + 1 of p >= 0, 0 for padding) in the
+    // high word, ~id in the low word, so that one unsigned 64-bit comparison
+    // ranks "larger p first, lower id on equal p"
+    uint64_t v[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; j++) {
+        int e = j * 32 + lane;
+        unsigned key = (e < E) ? __float_as_uint(p[j]) + 1u : 0u;
+        v[j] = ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (unsigned)e);
+    }
+    bitonic_sort_desc<NJ>(v);  // this lane's values, best first
+    constexpr int KP = NJ;  // list length kept while merging (>= k)
+    // butterfly over the lanes: two sorted lists -> the KP best of their union
+    // (max of A[i] and B[KP-1-i] is bitonic, then a bitonic merge sorts it);
+    // both partners get the same list, so after 5 rounds every lane holds the
+    // warp's KP best, sorted
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint64_t b[KP];
+#pragma unroll
+        for (int i = 0; i < KP; i++) b[i] = __shfl_xor_sync(kFull, v[i], o);
+#pragma unroll
+        for (int i = 0; i < KP; i++) v[i] = v[i] > b[KP - 1 - i] ? v[i] : b[KP - 1 - i];
+        bitonic_merge_desc<KP>(v);
     }
     sel_e = -1;
     sel_p = 0.f;
-    for (int r = 0; r < k; r++) {
-        unsigned bk = 0;
-        int be = 0x7fffffff;
 #pragma unroll
-        for (int j = 0; j < NJ; j++)
-            if (key[j] > bk) { bk = key[j]; be = j * 32 + lane; }
-        unsigned mk = __reduce_max_sync(kFull, bk);
-        unsigned cand = (bk == mk && mk != 0u) ? (unsigned)be : 0x7fffffffu;
-        unsigned we = __reduce_min_sync(kFull, cand);
-        if (lane == r) { sel_e = (int)we; sel_p = __uint_as_float(mk - 1u); }
-#pragma unroll
-        for (int j = 0; j < NJ; j++)
-            if (j * 32 + lane == (int)we) key[j] = 0u;
+    for (int i = 0; i < KP; i++) {
+        if (i == lane && i < k && (unsigned)(v[i] >> 32) != 0u) {
+            sel_e = (int)(0xffffffffu - (unsigned)v[i]);
+            sel_p = __uint_as_float((unsigned)(v[i] >> 32) - 1u);
+        }
     }
 }
 

@@ -101,10 +101,14 @@ template <typename WT, typename XT, int NCH>
 static cudaError_t launch_router_nj(const RouterParams& p, cudaStream_t s, bool pdl) {
     dim3 grid((p.E + 7) / 8), block(256);
     size_t smem = p.grp_expert ? sizeof(int) * (2 * p.E + 1) : 0;
-    if (p.E <= 32) return launch(router_kernel<WT, XT, NCH, 1>, grid, block, smem, s, pdl, p);
-    if (p.E <= 256) return launch(router_kernel<WT, XT, NCH, 8>, grid, block, smem, s, pdl, p);
-    if (p.E <= 512) return launch(router_kernel<WT, XT, NCH, 16>, grid, block, smem, s, pdl, p);
-    return launch(router_kernel<WT, XT, NCH, 32>, grid, block, smem, s, pdl, p);
+    switch (topk_nj(p.E, p.k)) {
+        case 1: return launch(router_kernel<WT, XT, NCH, 1>, grid, block, smem, s, pdl, p);
+        case 2: return launch(router_kernel<WT, XT, NCH, 2>, grid, block, smem, s, pdl, p);
+        case 4: return launch(router_kernel<WT, XT, NCH, 4>, grid, block, smem, s, pdl, p);
+        case 8: return launch(router_kernel<WT, XT, NCH, 8>, grid, block, smem, s, pdl, p);
+        case 16: return launch(router_kernel<WT, XT, NCH, 16>, grid, block, smem, s, pdl, p);
+        default: return launch(router_kernel<WT, XT, NCH, 32>, grid, block, smem, s, pdl, p);
+    }
 }
 
 template <typename WT, typename XT>
