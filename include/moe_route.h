@@ -172,6 +172,29 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
                          void* stream);
 
 /*
+ * moe_layer for ONE token (T = 1) without a workspace: no counterpart in the
+ * pages; it exists for callers that cannot allocate device memory where they
+ * run a layer (a frozen or captured memory pool, a host runtime whose
+ * allocator is out of reach, an embedding that hands over only its input and
+ * output buffers). Its scratch is a static device array inside the library of
+ * 139,520 bytes (header + E tagged logits + k*F activations), held by every GPU
+ * that loads the library until the process exits. Limits: E <= 1024,
+ * k*F <= 32768, k <= 16, router weights in the dtype of x; larger sizes return
+ * MOE_ERR_WORKSPACE, shapes the single-token kernel cannot run return
+ * MOE_ERR_UNSUPPORTED. Nothing is allocated: the first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) and caches it, so make
+ * that first call before any stream capture. Every call on a device shares the
+ * array, which keeps the previous call's contents (the status word is cleared
+ * at the start of each call); calls whose execution overlaps on the GPU, e.g.
+ * on two streams, race and must be avoided. Device-side conditions (an expert
+ * id out of range, a timed-out wait) are not reported by this entry point.
+ * Arguments as moe_layer with T = 1.
+ */
+moe_status_t moe_layer_noalloc(const moe_router_t* router, const moe_experts_t* experts, const void* x,
+                               moe_dtype_t x_dtype, int32_t* idx, float* w, float* probs, float* y,
+                               void* x_next, void* stream);
+
+/*
  * Waits for `stream`, reads the workspace's device status word, resets it to
  * zero and returns it (MOE_OK if no device-side problem was recorded).
  */

@@ -28,7 +28,7 @@ MOE_Q_INT8_SYM_B32, MOE_Q_INT4_SYM_B32 = 0, 1
 MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_LAYER, MOE_OP_PREFILL = 0, 1, 2, 3
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_substitute", "moe_decode", "moe_layer",
-            "moe_prefill", "moe_check_status", "moe_status_string")
+            "moe_prefill", "moe_layer_noalloc", "moe_check_status", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -64,11 +64,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_decode.argtypes = [P, P, I, I, I, P, P, P, P, P, S, P]
     lib.moe_layer.argtypes = [P, P, P, I, I, P, P, P, P, P, P, S, P]
     lib.moe_prefill.argtypes = [P, P, P, I, I, P, P, P, P, P, P, S, P]
+    lib.moe_layer_noalloc.argtypes = [P, P, P, I, P, P, P, P, P, P]
     lib.moe_check_status.argtypes = [P, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for f in ("moe_route", "moe_substitute", "moe_decode", "moe_layer", "moe_prefill",
-              "moe_check_status"):
+              "moe_layer_noalloc", "moe_check_status"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -270,6 +271,23 @@ def moe_prefill(router: Router, experts: Experts, x, y, idx, w, counts, perm, ws
     _check("moe_prefill", _lib.moe_prefill(ctypes.byref(r), ctypes.byref(e), _ptr(x), _act_dtype(x), T,
                                            _ptr(y), _ptr(idx), _ptr(w), _ptr(counts), _ptr(perm),
                                            _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_layer_noalloc(router: Router, experts: Experts, x, idx, w, probs, y, x_next, stream=None):
+    """One token through the layer with the library's static scratch (no workspace)."""
+    r = router.struct()
+    e = experts.struct()
+    _dev(x, "x", (torch.float32, torch.bfloat16), (1, e.D))
+    _dev(idx, "idx", torch.int32, (1, r.k))
+    _dev(w, "w", torch.float32, (1, r.k))
+    if probs is not None:
+        _dev(probs, "probs", torch.float32, (1, r.E))
+    _dev(y, "y", torch.float32, (1, e.D))
+    if x_next is not None:
+        _dev(x_next, "x_next", x.dtype, (1, e.D))
+    _check("moe_layer_noalloc", _lib.moe_layer_noalloc(ctypes.byref(r), ctypes.byref(e), _ptr(x),
+                                                       _act_dtype(x), _ptr(idx), _ptr(w), _ptr(probs),
+                                                       _ptr(y), _ptr(x_next), _stream(stream)))
 
 
 def moe_check_status(ws: torch.Tensor, stream=None) -> int:
