@@ -50,6 +50,48 @@ Layout layout(int op, int T, int k, int E, int D, int F) {
     return L;
 }
 
+// Prefill workspace sections.
+struct PLayout {
+    size_t logits, idx, w, xh, chunk_cnt, chunk_base, cnt, off, gend, tgroup, tm0, nmt, perm_tok, inv, hp, yp;
+    size_t total;
+    int nchunk, max_mtiles;
+};
+
+PLayout prefill_layout(int T, int k, int E, int D, int F) {
+    PLayout L = {};
+    size_t o = sizeof(WsHeader);
+    auto take = [&](size_t bytes) {
+        size_t r = o;
+        o = align_up(o + std::max<size_t>(bytes, 1));
+        return r;
+    };
+    const size_t n = (size_t)T * k;
+    L.nchunk = (int)((n + kPermChunk - 1) / kPermChunk);
+    L.max_mtiles = (int)((n + 127) / 128) + E;
+    L.logits = take(sizeof(float) * (size_t)T * E);
+    L.idx = take(sizeof(int32_t) * n);
+    L.w = take(sizeof(float) * n);
+    L.xh = take(2 * (size_t)T * D);
+    L.chunk_cnt = take(sizeof(int32_t) * (size_t)L.nchunk * E);
+    L.chunk_base = take(sizeof(int32_t) * (size_t)L.nchunk * E);
+    L.cnt = take(sizeof(int32_t) * E);
+    L.off = take(sizeof(int32_t) * (E + 1));
+    L.gend = take(sizeof(int32_t) * E);
+    L.tgroup = take(sizeof(int32_t) * L.max_mtiles);
+    L.tm0 = take(sizeof(int32_t) * L.max_mtiles);
+    L.nmt = take(sizeof(int));
+    L.perm_tok = take(sizeof(int32_t) * n);
+    L.inv = take(sizeof(int32_t) * n);
+    L.hp = take(2 * n * F);
+    L.yp = take(sizeof(float) * n * D);
+    L.total = o;
+    return L;
+}
+
+bool prefill_shape_ok(int E, int D, int F) {
+    return D % 128 == 0 && F % 64 == 0 && D >= 128 && F >= 64 && E <= 1024;
+}
+
 bool al16(const void* p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
 
 template <typename T>
@@ -170,7 +212,8 @@ extern "C" {
 
 size_t moe_workspace_bytes(int op, int T, int k, int E, int D, int F) {
     if (T < 1 || k < 1 || E < 1 || D < kBlk || D % kBlk) return 0;
-    if ((op == MOE_OP_DECODE || op == MOE_OP_LAYER) && (F < kBlk || F % kBlk)) return 0;
+    if ((op == MOE_OP_DECODE || op == MOE_OP_LAYER || op == MOE_OP_PREFILL) && (F < kBlk || F % kBlk)) return 0;
+    if (op == MOE_OP_PREFILL) return prefill_shape_ok(E, D, F) ? prefill_layout(T, k, E, D, F).total : 0;
     if (op < MOE_OP_ROUTE || op > MOE_OP_LAYER) return 0;
     return layout(op, T, k, E, D, F).total;
 }
@@ -294,9 +337,137 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
                          moe_dtype_t x_dtype, int T, float* y, int32_t* idx, float* w,
                          int32_t* counts, int32_t* perm, void* workspace, size_t ws_bytes,
                          void* stream) {
-    (void)router; (void)experts; (void)x; (void)x_dtype; (void)T; (void)y; (void)idx; (void)w;
-    (void)counts; (void)perm; (void)workspace; (void)ws_bytes; (void)stream;
-    return MOE_ERR_UNSUPPORTED;
+    moe_status_t st = check_router(router, x_dtype);
+    if (st != MOE_OK) return st;
+    const int k = router->k;
+    st = check_experts(experts, x_dtype, k);
+    if (st != MOE_OK) return st;
+    if (router->E != experts->E || router->D != experts->D) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || !al16(x) || !y) return MOE_ERR_INVALID_ARG;
+    const int E = experts->E, D = experts->D, F = experts->F;
+    if (!prefill_shape_ok(E, D, F)) return MOE_ERR_UNSUPPORTED;
+    PLayout P = prefill_layout(T, k, E, D, F);
+    if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < P.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader* hdr = at<WsHeader>(workspace, 0);
+    int32_t* idx_buf = idx ? idx : at<int32_t>(workspace, P.idx);
+    float* w_buf = w ? w : at<float>(workspace, P.w);
+    float* logits = at<float>(workspace, P.logits);
+    cudaError_t e;
+
+    // routing: tensor-core logits + one warp per token when the shapes allow,
+    // else the CUDA-core router kernel
+    if (x_dtype == MOE_BF16 && router->w_dtype == MOE_BF16 && E % 128 == 0 && D % 64 == 0) {
+        GemmParams g = {};
+        g.A = x;
+        g.K = D;
+        g.B0 = router->W;
+        g.B1 = router->W;
+        g.b_row_bytes = 2 * D;
+        g.rows_per_ntile = 128;
+        g.half_off = 64;
+        g.n_mtiles = (T + 127) / 128;
+        g.m_total = T;
+        g.n_ntiles = E / 128;
+        g.C = logits;
+        g.ldc = E;
+        g.hdr = hdr;
+        e = launch_gemm(g, 16, false, false, g.n_mtiles, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        TopkParams tp = {T, E, k, router->norm_topk ? 1 : 0, logits, router->bias, idx_buf, w_buf, nullptr};
+        e = launch_topk(tp, s);
+    } else {
+        RouterParams rp = {};
+        rp.T = T;
+        rp.E = E;
+        rp.D = D;
+        rp.k = k;
+        rp.norm_topk = router->norm_topk ? 1 : 0;
+        rp.W = router->W;
+        rp.bias = router->bias;
+        rp.x = x;
+        rp.logits = logits;
+        rp.idx = idx_buf;
+        rp.w = w_buf;
+        rp.hdr = hdr;
+        e = launch_router(rp, router->w_dtype == MOE_BF16, x_dtype == MOE_BF16, s, true);
+    }
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    void* xh = at<void>(workspace, P.xh);
+    e = launch_to_f16(x, x_dtype == MOE_BF16, xh, (long)T * D, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    PermParams pp = {};
+    pp.n = T * k;
+    pp.k = k;
+    pp.E = E;
+    pp.nchunk = P.nchunk;
+    pp.idx = idx_buf;
+    pp.hdr = hdr;
+    pp.chunk_cnt = at<int32_t>(workspace, P.chunk_cnt);
+    pp.chunk_base = at<int32_t>(workspace, P.chunk_base);
+    pp.cnt = at<int32_t>(workspace, P.cnt);
+    pp.off = at<int32_t>(workspace, P.off);
+    pp.group_end = at<int32_t>(workspace, P.gend);
+    pp.counts_out = counts;
+    pp.tile_group = at<int32_t>(workspace, P.tgroup);
+    pp.tile_m0 = at<int32_t>(workspace, P.tm0);
+    pp.n_mtiles = at<int>(workspace, P.nmt);
+    pp.perm_tok = at<int32_t>(workspace, P.perm_tok);
+    pp.perm_out = perm;
+    pp.inv = at<int32_t>(workspace, P.inv);
+    e = launch_perm(pp, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    const int qbits = qbits_of(experts);
+    const int cb = qbits == 8 ? 1 : 2;  // divisor: bytes per element of a code row
+    const bool sf16 = experts->s_dtype == MOE_F16;
+    GemmParams g1 = {};
+    g1.A = xh;
+    g1.a_rows = pp.perm_tok;
+    g1.K = D;
+    g1.B0 = experts->gate_q;
+    g1.B1 = experts->up_q;
+    g1.S0 = experts->gate_s;
+    g1.S1 = experts->up_s;
+    g1.b_row_bytes = D / cb;
+    g1.b_estride = (size_t)F * (D / cb);
+    g1.s_estride = (size_t)F * (D / kBlk);
+    g1.rows_per_ntile = 64;
+    g1.half_off = 0;
+    g1.tile_group = pp.tile_group;
+    g1.tile_m0 = pp.tile_m0;
+    g1.group_end = pp.group_end;
+    g1.n_mtiles_dev = pp.n_mtiles;
+    g1.n_ntiles = F / 64;
+    g1.C = at<void>(workspace, P.hp);
+    g1.ldc = F;
+    g1.hdr = hdr;
+    e = launch_gemm(g1, qbits, sf16, true, P.max_mtiles, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    GemmParams g2 = g1;
+    g2.A = at<void>(workspace, P.hp);
+    g2.a_rows = nullptr;
+    g2.K = F;
+    g2.B0 = experts->down_q;
+    g2.B1 = experts->down_q;
+    g2.S0 = experts->down_s;
+    g2.S1 = experts->down_s;
+    g2.b_row_bytes = F / cb;
+    g2.b_estride = (size_t)D * (F / cb);
+    g2.s_estride = (size_t)D * (F / kBlk);
+    g2.rows_per_ntile = 128;
+    g2.half_off = 64;
+    g2.n_ntiles = D / 128;
+    g2.C = at<void>(workspace, P.yp);
+    g2.ldc = D;
+    e = launch_gemm(g2, qbits, sf16, false, P.max_mtiles, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    CombineParams cp = {T, D, k, pp.inv, w_buf, at<float>(workspace, P.yp), y};
+    return from_cuda(launch_combine(cp, s));
 }
 
 moe_status_t moe_check_status(void* workspace, void* stream) {

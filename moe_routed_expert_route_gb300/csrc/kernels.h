@@ -120,6 +120,72 @@ struct FusedParams {
     float* h;                 // workspace [k][F]
 };
 
+// Grouped tensor-core matrix product (prefill). Tile (mt, nt): 128 rows of A
+// (positions m0.. of tile mt, gathered through a_rows) times 128 rows of B.
+struct GemmParams {
+    const void* A;              // row-major 16-bit [rows][K]
+    const int32_t* a_rows;      // position -> A row, or null (identity)
+    int K;
+    const void *B0, *B1;        // B rows [0,64) of a tile from B0, [64,128) from B1
+    const void *S0, *S1;        // their scales (quantised B), or null
+    size_t b_estride;           // bytes between experts' code matrices
+    size_t s_estride;           // scale elements between experts
+    int b_row_bytes;
+    int rows_per_ntile;         // B row of tile nt, row j: nt*rows_per_ntile + (j&63) + (j>=64)*half_off
+    int half_off;
+    const int32_t* tile_group;  // [mt] expert, or null (group 0)
+    const int32_t* tile_m0;     // [mt] first position, or null (mt*128)
+    const int32_t* group_end;   // [g] end position, or null (m_total)
+    const int* n_mtiles_dev;    // number of m-tiles on the device, or null (n_mtiles)
+    int n_mtiles, m_total, n_ntiles;
+    void* C;                    // fp32 [pos][ldc] (plain) or fp16 [pos][ldc] (SwiGLU)
+    int ldc;
+    WsHeader* hdr;
+};
+
+struct TopkParams {
+    int T, E, k, norm_topk;
+    const float* logits;        // [T][E]
+    const float* bias;          // [E] or null
+    int32_t* idx;
+    float* w;
+    float* probs;               // [T][E] or null
+};
+
+constexpr int kPermChunk = 1024;  // assignments per histogram/placement CTA
+
+struct PermParams {
+    int n, k, E, nchunk;
+    const int32_t* idx;         // [n] expert of assignment i = t*k + r
+    WsHeader* hdr;
+    int32_t* chunk_cnt;         // [nchunk][E]
+    int32_t* chunk_base;        // [nchunk][E]
+    int32_t* cnt;               // [E]
+    int32_t* off;               // [E+1]
+    int32_t* group_end;         // [E]
+    int32_t* counts_out;        // [E] or null
+    int32_t* tile_group;        // [n/128 + E]
+    int32_t* tile_m0;
+    int* n_mtiles;
+    int32_t* perm_tok;          // [n] position -> token
+    int32_t* perm_out;          // [n] position -> assignment id, or null
+    int32_t* inv;               // [n] assignment -> position
+};
+
+struct CombineParams {
+    int T, D, k;
+    const int32_t* inv;
+    const float* w;
+    const float* Y;             // [n][D]
+    float* y;                   // [T][D]
+};
+
+cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu, int max_mtiles, cudaStream_t s);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
+cudaError_t launch_to_f16(const void* x, bool x_bf16, void* out, long n, cudaStream_t s);
+cudaError_t launch_perm(const PermParams& p, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
 bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes, bool has_router,
                 FusedParams* fp, size_t* smem, int* grid);
 cudaError_t launch_fused(const FusedParams& p, int qbits, bool s_f16, bool x_bf16, int grid, size_t smem,
