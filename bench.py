@@ -298,6 +298,166 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# ------------------------------------------------- secondary workloads
+# (measured on request with --workload; the default line is the decode step)
+
+def _time_graph_simple(g, stream, steps, warmup):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_batched(args, dev):
+    """Batched decode over the 40-layer stack, T in {1,...,64}."""
+    cfg = W.CONFIGS[2]
+    per_expert = W.routed_bytes_per_expert(cfg)
+    out = []
+    stack = None
+    for T in (1, 2, 4, 8, 16, 32, 64):
+        if stack is None:
+            stack = DecodeStack(cfg, dev, T=T, layers=args.layers)
+        else:  # same weights, new token batch
+            old = stack
+            stack = DecodeStack.__new__(DecodeStack)
+            stack.__dict__.update(old.__dict__)
+            stack.T = T
+            stack.X = [torch.empty(T, cfg.D, dtype=cfg.x_dtype, device=dev) for _ in range(old.L + 1)]
+            stack.X[0].copy_(W.make_tokens(cfg, T, 0, dev))
+            stack.idx = [torch.empty(T, cfg.k, dtype=torch.int32, device=dev) for _ in range(old.L)]
+            stack.w = [torch.empty(T, cfg.k, dtype=torch.float32, device=dev) for _ in range(old.L)]
+            stack.y = [torch.empty(T, cfg.D, dtype=torch.float32, device=dev) for _ in range(old.L)]
+            stack.ws = stack.M.workspace(stack.M.MOE_OP_LAYER, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
+        stream = torch.cuda.Stream(dev)
+        stack.capture(stream)
+        ms = _time_graph_simple(stack.graph, stream, max(10, args.steps // 4), max(3, args.warmup))
+        U = [int(torch.unique(stack.idx[l]).numel()) for l in range(stack.L)]
+        routed = sum(U) * per_expert
+        out.append({"T": T, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+                    "union_experts_mean": round(sum(U) / len(U), 2), "union_min": min(U), "union_max": max(U),
+                    "routed_gbs": round(routed / (ms * 1e-3) / 1e9, 1)})
+        assert stack.M.moe_check_status(stack.ws) == 0
+    return {"workload": "batched decode sweep, 40 layers E=256 top-8 D=2048 F=768 int8", "points": out}
+
+
+def run_substitution(args, dev):
+    """Residency substitution (0.15 rule) + int4 decode, 512 experts top-10, 16 layers."""
+    import moe_routed_expert_route_gb300 as M
+    cfg = W.CONFIGS[3]
+    L = args.layers or cfg.layers
+    layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(L)]
+    masks = [W.make_resident_mask(cfg, l, dev) for l in range(L)]
+    per_expert = W.routed_bytes_per_expert(cfg)
+    res = []
+    for T in (1, 16):
+        k = cfg.k
+        X = [torch.empty(T, cfg.D, dtype=cfg.x_dtype, device=dev) for _ in range(L + 1)]
+        X[0].copy_(W.make_tokens(cfg, T, 0, dev))
+        bufs = [dict(idx=torch.empty(T, k, dtype=torch.int32, device=dev), w=torch.empty(T, k, device=dev),
+                     probs=torch.empty(T, cfg.E, device=dev), idx2=torch.empty(T, k, dtype=torch.int32, device=dev),
+                     w2=torch.empty(T, k, device=dev), flag=torch.empty(T, k, dtype=torch.uint8, device=dev),
+                     mass=torch.empty(T, device=dev), y=torch.empty(T, cfg.D, device=dev)) for _ in range(L)]
+        ws_r = M.workspace(M.MOE_OP_ROUTE, T, k, cfg.E, cfg.D, cfg.F, dev)
+        ws_d = M.workspace(M.MOE_OP_DECODE, T, k, cfg.E, cfg.D, cfg.F, dev)
+        routers = [M.Router(lw["Wr"], lw["bias"], k) for lw in layers]
+        experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
+
+        def step():
+            for l in range(L):
+                b = bufs[l]
+                M.moe_route(routers[l], X[l], b["idx"], b["w"], b["probs"], ws_r)
+                M.moe_substitute(b["probs"], b["idx"], b["w"], masks[l], cfg.threshold, b["idx2"], b["w2"],
+                                 b["flag"], b["mass"])
+                M.moe_decode(experts[l], X[l], b["idx2"], b["w2"], b["y"], X[l + 1], ws_d)
+            X[0].copy_(X[L])
+
+        stream = torch.cuda.Stream(dev)
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        ms = _time_graph_simple(g, stream, max(10, args.steps // 4), max(3, args.warmup))
+        U = [int(torch.unique(bufs[l]["idx2"]).numel()) for l in range(L)]
+        flags = torch.stack([b["flag"] for b in bufs]).cpu()
+        mass = torch.stack([b["mass"] for b in bufs]).cpu()
+        res.append({"T": T, "layers": L, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+                    "us_per_layer": round(ms * 1e3 / L, 2), "distinct_experts_mean": round(sum(U) / L, 2),
+                    "routed_gbs": round(sum(U) * per_expert / (ms * 1e-3) / 1e9, 1),
+                    "substituted_frac": round(float((flags == 2).float().mean()), 4),
+                    "fetched_miss_frac": round(float((flags == 1).float().mean()), 4),
+                    "mass_mean": round(float(mass.mean()), 4), "mass_max": round(float(mass.max()), 4)})
+        assert M.moe_check_status(ws_d) == 0
+    return {"workload": "substitution 0.15 rule + int4 decode, E=512 top-10 D=2048 F=512, 25% resident",
+            "points": res}
+
+
+def run_prefill(args, dev, T=None):
+    """Prefill of T tokens (default 2048), rotating over 4 layers (5 GB of weights)."""
+    import moe_routed_expert_route_gb300 as M
+    cfg = W.CONFIGS[4]
+    T = T or cfg.T
+    L = args.layers or 4
+    layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(L)]
+    routers = [M.Router(lw["Wr"], lw["bias"], cfg.k) for lw in layers]
+    experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
+    x = W.make_tokens(cfg, T, 0, dev)
+    y = torch.empty(T, cfg.D, device=dev)
+    idx = torch.empty(T, cfg.k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, cfg.k, device=dev)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    ws = M.workspace(M.MOE_OP_PREFILL, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(l):
+        M.moe_prefill(routers[l], experts[l], x, y, idx, w, counts, None, ws)
+
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            step(l)
+    torch.cuda.synchronize()
+    U = int((counts > 0).sum())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for l in range(L):
+            step(l)
+    ms = _time_graph_simple(g, stream, max(5, args.steps // 40), max(3, args.warmup)) / L
+    flops = 2.0 * T * cfg.k * 3 * cfg.D * cfg.F
+    wbytes = U * W.routed_bytes_per_expert(cfg)
+    hbm, tf, kind = peaks()
+    assert M.moe_check_status(ws) == 0
+    return {"workload": f"prefill T={T} E=256 top-8 D=2048 F=768 int8 (fp16 tensor-core operands)",
+            "T": T, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_layer": round(ms, 4),
+            "distinct_experts": U, "expert_weight_gb": round(wbytes / 1e9, 3),
+            "expert_tflops": round(flops / (ms * 1e-3) / 1e12, 1), "tensor_frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / tf, 4),
+            "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1), "weight_frac_of_hbm_peak": round(wbytes / (ms * 1e-3) / 1e9 / hbm, 4)}
+
+
+def run_workload(args):
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import __graft_entry__
+    __graft_entry__.build()
+    if args.workload == "batched":
+        r = run_batched(args, dev)
+    elif args.workload == "substitution":
+        r = run_substitution(args, dev)
+    else:
+        r = run_prefill(args, dev)
+        if args.prefill_extra:
+            r["extra"] = run_prefill(args, dev, T=16384)
+    print(json.dumps(r), flush=True)
+
+
 def run_reference(args):
     """The CPU oracle on a bounded sample of the same workload."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -352,11 +512,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--workload", default="decode", choices=["decode", "batched", "substitution", "prefill"],
+                    help="decode (default, the headline line) or a secondary workload")
+    ap.add_argument("--prefill-extra", action="store_true", help="also time a 16384-token prefill")
     ap.add_argument("--layers", type=int, default=None,
                     help="stacked layers (default: the workload's 40); fewer only for profiling captures")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "decode":
+        run_workload(args)
     else:
         run_ours(args)
 
