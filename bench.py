@@ -4,9 +4,9 @@ Default workload: decode of one token through 40 stacked independent MoE layers
 of 256 experts, top-8, d_model 2048, d_ff 768 (Qwen3.6-35B-A3B-shaped), int8
 symmetric per-block-32 weights with fp16 scales, bf16 activations, Zipf(1.1)
 router bias. One step = router GEMV + fp32 softmax + top-k + gathered gate/up +
-SwiGLU + per-slot down + weighted combine + residual, for all 40 layers; the
-last layer's output is fed back as the next step's input (a new token each
-step). Inputs are seeded and synthetic (data="synthetic").
+SwiGLU + per-slot down + weighted combine + residual, for all 40 layers. Each
+step decodes the next token of a device-resident bank of 64 distinct seeded
+tokens (data="synthetic").
 
 Prints ONE JSON line (rank 0). With --impl reference the CPU oracle is timed on
 a bounded sample of the same workload instead.
@@ -121,15 +121,22 @@ class DecodeStack:
         self.w = [torch.empty(T, cfg.k, dtype=torch.float32, device=dev) for _ in range(self.L)]
         self.y = [torch.empty(T, D, dtype=torch.float32, device=dev) for _ in range(self.L)]
         self.ws = M.workspace(M.MOE_OP_LAYER, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
-        self.graph = None
+        # a bank of distinct tokens on the device: step i decodes token i mod NB,
+        # so every step routes a new token and nothing drifts from step to step
+        self.NB = 64
+        self.bank = W.make_tokens(cfg, T * self.NB, 1, dev).reshape(self.NB, T, D)
+        self.ctr = torch.zeros(1, dtype=torch.long, device=dev)
+        self.graph = self.graph_e2e = None
+        torch.cuda.synchronize()  # setup ran on the default stream; the steps run on another
 
-    def forward(self, feedback: bool = True):
+    def forward(self, from_bank: bool = True):
         M = self.M
+        if from_bank:
+            torch.index_select(self.bank, 0, self.ctr, out=self.X[0].view(1, self.T, -1))
+            self.ctr.add_(1).remainder_(self.NB)
         for l in range(self.L):
             M.moe_layer(self.routers[l], self.experts[l], self.X[l], self.idx[l], self.w[l], None,
                         self.y[l], self.X[l + 1], self.ws)
-        if feedback:
-            self.X[0].copy_(self.X[self.L])
 
     def capture(self, stream):
         with torch.cuda.stream(stream):
@@ -139,6 +146,10 @@ class DecodeStack:
         with torch.cuda.graph(g, stream=stream):
             self.forward()
         self.graph = g
+        g2 = torch.cuda.CUDAGraph()  # the same layers without the bank: input comes from the host
+        with torch.cuda.graph(g2, stream=stream):
+            self.forward(from_bank=False)
+        self.graph_e2e = g2
         return g
 
     def kernels_per_step(self):
@@ -187,7 +198,7 @@ def time_e2e(stack, stream, steps, warmup):
 
     def one(i):
         stack.X[0].copy_(xin[i % n], non_blocking=True)
-        stack.graph.replay()
+        stack.graph_e2e.replay()
         xout[i % n].copy_(stack.X[stack.L], non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -336,6 +347,9 @@ def run_batched(args, dev):
             stack.w = [torch.empty(T, cfg.k, dtype=torch.float32, device=dev) for _ in range(old.L)]
             stack.y = [torch.empty(T, cfg.D, dtype=torch.float32, device=dev) for _ in range(old.L)]
             stack.ws = stack.M.workspace(stack.M.MOE_OP_LAYER, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
+            stack.bank = W.make_tokens(cfg, T * stack.NB, 1, dev).reshape(stack.NB, T, cfg.D)
+            stack.ctr = torch.zeros(1, dtype=torch.long, device=dev)
+            torch.cuda.synchronize()
         stream = torch.cuda.Stream(dev)
         stack.capture(stream)
         ms = _time_graph_simple(stack.graph, stream, max(10, args.steps // 4), max(3, args.warmup))
@@ -369,15 +383,20 @@ def run_substitution(args, dev):
         ws_d = M.workspace(M.MOE_OP_DECODE, T, k, cfg.E, cfg.D, cfg.F, dev)
         routers = [M.Router(lw["Wr"], lw["bias"], k) for lw in layers]
         experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
+        NB = 64
+        bank = W.make_tokens(cfg, T * NB, 1, dev).reshape(NB, T, cfg.D)
+        ctr = torch.zeros(1, dtype=torch.long, device=dev)
+        torch.cuda.synchronize()  # setup ran on the default stream; the steps run on another
 
         def step():
+            torch.index_select(bank, 0, ctr, out=X[0].view(1, T, -1))
+            ctr.add_(1).remainder_(NB)
             for l in range(L):
                 b = bufs[l]
                 M.moe_route(routers[l], X[l], b["idx"], b["w"], b["probs"], ws_r)
                 M.moe_substitute(b["probs"], b["idx"], b["w"], masks[l], cfg.threshold, b["idx2"], b["w2"],
                                  b["flag"], b["mass"])
                 M.moe_decode(experts[l], X[l], b["idx2"], b["w2"], b["y"], X[l + 1], ws_d)
-            X[0].copy_(X[L])
 
         stream = torch.cuda.Stream(dev)
         with torch.cuda.stream(stream):
@@ -416,6 +435,7 @@ def run_prefill(args, dev, T=None):
     w = torch.empty(T, cfg.k, device=dev)
     counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
     ws = M.workspace(M.MOE_OP_PREFILL, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
+    torch.cuda.synchronize()  # setup ran on the default stream; the steps run on another
     stream = torch.cuda.Stream(dev)
 
     def step(l):
