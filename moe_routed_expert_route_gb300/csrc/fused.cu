@@ -21,9 +21,10 @@
 //      of the k down matrices into shared memory, and the CTA arrives on a
 //      completion counter (polling ~150 KB of tagged activations from every
 //      CTA would flood L2 while other CTAs still stream)
-//   4  every CTA reads all k*F activations into fixed-point planes; each warp
-//      owns one slot and some of the CTA's rows, dots them against the staged
-//      down rows; the CTA combines the k slots in slot order,
+//   4  each warp owns one slot: it reads that slot's activations into
+//      registers and dots them (fp32, codes widened exactly) against the staged
+//      down rows of its share of the CTA's rows; the CTA combines the k slots
+//      in slot order,
 //      y[d] = sum_r w[r] * o_r[d], and writes x_next = x + y.
 // Without a router (moe_decode) phases 0-2 are replaced by reading idx/w.
 #include "dots.cuh"
@@ -37,12 +38,10 @@ constexpr int kFThreads = 512;
 constexpr int kFWarps = 16;
 constexpr int kNRC = 2;  // router 16-byte chunks per lane
 constexpr int kNCH = 4;  // gate/up 16-byte chunks per lane
-constexpr int kNP = 4;   // down 8-byte pieces per lane
-constexpr int kHB = 12;  // activation blocks converted per warp per batch of loads
 constexpr int kRU = 4;   // down rows reduced together
 
 struct FusedLayout {
-    size_t x, xhi, xlo, xs, dq, ds, hhi, hlo, hs, part, total;
+    size_t x, xhi, xlo, xs, dq, ds, part, total;
 };
 
 __host__ __device__ inline size_t fl_align(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -57,9 +56,6 @@ __host__ __device__ inline FusedLayout fused_layout(int D, int F, int k, int qbi
     L.xs = o;   o = fl_align(o + sizeof(float) * (D / kBlk), 16);
     L.dq = o;   o = fl_align(o + (size_t)k * rows * rowF, 16);
     L.ds = o;   o = fl_align(o + (size_t)k * rows * (F / kBlk) * s_bytes, 16);
-    L.hhi = o;  o = fl_align(o + (size_t)k * F, 16);
-    L.hlo = o;  o = fl_align(o + (size_t)k * F, 16);
-    L.hs = o;   o = fl_align(o + sizeof(float) * (size_t)k * (F / kBlk), 16);
     L.part = o; o = fl_align(o + sizeof(float) * (size_t)k * rows, 16);
     L.total = o;
     return L;
@@ -119,9 +115,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     float* s_xs = reinterpret_cast<float*>(sm + L.xs);
     uint8_t* s_dq = sm + L.dq;
     ST* s_ds = reinterpret_cast<ST*>(sm + L.ds);
-    int8_t* s_hhi = reinterpret_cast<int8_t*>(sm + L.hhi);
-    uint8_t* s_hlo = sm + L.hlo;
-    float* s_hs = reinterpret_cast<float*>(sm + L.hs);
     float* s_part = reinterpret_cast<float*>(sm + L.part);
     int* status = &p.hdr->status;
 
@@ -346,44 +339,30 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
 
     // ---------------------------------------------------------- phase 4
     // wait for every CTA's activations (one counter per launch parity; the
-    // other one is cleared for the next launch), then all k*F of them ->
-    // 16-bit fixed point per block of 32 along F; a warp takes kHB blocks per
-    // round, all loads in flight together and their max-reductions interleaved
+    // other one is cleared for the next launch). Each warp owns one slot: it
+    // keeps that slot's activations for its pieces in registers (read once
+    // from L2) and dots them with the staged down rows of its share of rows.
     arrive_and_wait(&p.hdr->hcount[s_seq & 1], (unsigned)G, status, &s_abort);
-    {
-        const int nblk = k * nbF;
-        for (int base = warp; base < nblk; base += kFWarps * kHB) {
-            float hv[kHB];
-            int blk[kHB];
-#pragma unroll
-            for (int i = 0; i < kHB; i++) {
-                blk[i] = base + kFWarps * i;
-                hv[i] = blk[i] < nblk ? ld_cg_f32(p.h + (size_t)blk[i] * kBlk + lane) : 0.f;
-            }
-            fx_store_blocks<kHB>(hv, blk, nblk, lane, QB, s_hhi, s_hlo, s_hs);
-        }
-    }
     mbar_wait(&s_bar, 0, status);
-    __syncthreads();
 
     const int wps = kFWarps / k;  // warps per slot (k <= 16)
     const int slot = warp / wps, sub = warp - slot * wps;
     if (slot < k && s_idx[slot] >= 0) {
-        constexpr int PB = QB == 8 ? 8 : 16;  // elements (= plane bytes) per 8-byte piece of codes
-        constexpr int PW = PB / 4;            // plane words per piece
+        constexpr int EPP = QB == 8 ? 8 : 16;   // codes per 8-byte piece
+        constexpr int NPL = QB == 8 ? 4 : 2;    // pieces per lane (F <= 1024)
         const int npieces = rowF / 8;
-        uint32_t hh[kNP][PW], hl[kNP][PW];
-        float hsc[kNP];
+        float hreg[NPL][EPP];
 #pragma unroll
-        for (int i = 0; i < kNP; i++) {
-            int pc = i * 32 + lane;
-            const bool ok = pc < npieces;
+        for (int i = 0; i < NPL; i++) {
+            const int pc = i * 32 + lane;
 #pragma unroll
-            for (int q = 0; q < PW; q++) {
-                hh[i][q] = ok ? reinterpret_cast<const uint32_t*>(s_hhi + slot * F + PB * pc)[q] : 0u;
-                hl[i][q] = ok ? reinterpret_cast<const uint32_t*>(s_hlo + slot * F + PB * pc)[q] : 0u;
+            for (int q = 0; q < EPP; q += 4) {
+                uint4 v = pc < npieces ? ld_cg16(p.h + (size_t)slot * F + pc * EPP + q) : make_uint4(0, 0, 0, 0);
+                hreg[i][q] = __uint_as_float(v.x);
+                hreg[i][q + 1] = __uint_as_float(v.y);
+                hreg[i][q + 2] = __uint_as_float(v.z);
+                hreg[i][q + 3] = __uint_as_float(v.w);
             }
-            hsc[i] = ok ? s_hs[slot * nbF + (PB * pc) / kBlk] * (QB == 8 ? 1.0f : 1.0f / 16.0f) : 0.f;
         }
         const uint8_t* dq0 = s_dq + (size_t)slot * p.rows * rowF;
         const ST* ds0 = s_ds + (size_t)slot * p.rows * nbF;
@@ -395,20 +374,32 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                 acc[u] = 0.f;
                 if (row < nrows) {
 #pragma unroll
-                    for (int i = 0; i < kNP; i++) {
-                        int pc = i * 32 + lane;
+                    for (int i = 0; i < NPL; i++) {
+                        const int pc = i * 32 + lane;
                         if (pc < npieces) {
-                            uint2 wv = *reinterpret_cast<const uint2*>(dq0 + (size_t)row * rowF + 8 * pc);
-                            float sc = to_f32(ds0[row * nbF + (PB * pc) / kBlk]);
-                            int h = 0, l = 0;
+                            const uint2 wv = *reinterpret_cast<const uint2*>(dq0 + (size_t)row * rowF + 8 * pc);
+                            const float sc = to_f32(ds0[row * nbF + (EPP * pc) / kBlk]);
+                            float dot = 0.f;
                             if constexpr (QB == 8) {
-                                h = dp4a_ss(wv.x, hh[i][0], dp4a_ss(wv.y, hh[i][1], 0));
-                                l = dp4a_su(wv.x, hl[i][0], dp4a_su(wv.y, hl[i][1], 0));
+                                // int8 -> fp32 exactly: 2^23 + (q + 128) from the byte, minus 2^23 + 128
+                                const uint32_t u0 = wv.x ^ 0x80808080u, u1 = wv.y ^ 0x80808080u;
+#pragma unroll
+                                for (int q = 0; q < 8; q++) {
+                                    const uint32_t src = q < 4 ? u0 : u1;
+                                    const float f = __uint_as_float(__byte_perm(src, 0x4B000000u, 0x7540 + (q & 3)));
+                                    dot = fmaf(f - 8388736.0f, hreg[i][q], dot);
+                                }
                             } else {
-                                dot_i4_word(wv.x, hh[i][0], hh[i][1], hl[i][0], hl[i][1], h, l);
-                                dot_i4_word(wv.y, hh[i][2], hh[i][3], hl[i][2], hl[i][3], h, l);
+                                // int4: nibble n of the word (element n) -> 2^23 + (q + 8), minus 2^23 + 8
+                                const uint32_t u0 = wv.x ^ 0x88888888u, u1 = wv.y ^ 0x88888888u;
+#pragma unroll
+                                for (int q = 0; q < 16; q++) {
+                                    const uint32_t src = q < 8 ? u0 : u1;
+                                    const float f = __uint_as_float(((src >> (4 * (q & 7))) & 0xFu) | 0x4B000000u);
+                                    dot = fmaf(f - 8388616.0f, hreg[i][q], dot);
+                                }
                             }
-                            acc[u] = fmaf((float)(h * 256 + l), sc * hsc[i], acc[u]);
+                            acc[u] = fmaf(sc, dot, acc[u]);
                         }
                     }
                 }
@@ -468,7 +459,7 @@ bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes,
     const int rows = (D + G - 1) / G;
     const int rowD = qbits == 8 ? D : D / 2, rowF = qbits == 8 ? F : F / 2;
     if (rowD / 16 > 32 * kNCH) return false;
-    if (rowF / 8 > 32 * kNP) return false;
+    if (rowF / 8 > 32 * (qbits == 8 ? 4 : 2)) return false;
     if (F % 4) return false;
     if (((F / kBlk) * s_bytes) % 16) return false;  // bulk copies of whole scale rows
     if (has_router) {

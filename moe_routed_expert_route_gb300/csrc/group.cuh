@@ -121,7 +121,7 @@ __device__ __forceinline__ void bitonic_sort_desc(uint64_t (&v)[N]) {
 // Softmax and top-k of one token, by one warp, from logits already in
 // registers: lane l holds the logits of experts l, l+32, ... (NJ per lane, a
 // power of two, NJ*32 >= E, NJ >= k; entries e >= E are ignored).
-// Probabilities are p_e = exp(l_e - max) / sum; the k largest are chosen
+// Probabilities are p_e = exp(l_e - max) * (1 / sum); the k largest are chosen
 // largest first, equal fp32 values by lower expert id. Lanes r < k return
 // (sel_e, sel_p) of rank r.
 template <int NJ>
@@ -140,10 +140,11 @@ __device__ __forceinline__ void softmax_topk_regs(float (&p)[NJ], int E, int k, 
         s += p[j];
     }
     s = warp_sum(s);
+    const float inv_s = 1.0f / s;
 #pragma unroll
     for (int j = 0; j < NJ; j++) {
         int e = j * 32 + lane;
-        p[j] = p[j] / s;
+        p[j] = p[j] * inv_s;
         if (e < E && probs_t) probs_t[e] = p[j];
     }
     // selection: order key (fp32 bits + 1 of p >= 0, 0 for padding) in the
