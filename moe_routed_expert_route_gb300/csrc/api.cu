@@ -71,7 +71,7 @@ PLayout prefill_layout(int T, int k, int E, int D, int F) {
     L.logits = take(sizeof(float) * (size_t)T * E);
     L.idx = take(sizeof(int32_t) * n);
     L.w = take(sizeof(float) * n);
-    L.xh = take(2 * (size_t)T * D);
+    L.xh = take(2 * n * D);  // x rows in grouped order (fp16)
     L.chunk_cnt = take(sizeof(int32_t) * (size_t)L.nchunk * E);
     L.chunk_base = take(sizeof(int32_t) * (size_t)L.nchunk * E);
     L.cnt = take(sizeof(int32_t) * E);
@@ -88,6 +88,8 @@ PLayout prefill_layout(int T, int k, int E, int D, int F) {
     return L;
 }
 
+// Grouped GEMM tiling: K stages of 64, gate/up tiles of 64 outputs, down
+// tiles of 128 outputs.
 bool prefill_shape_ok(int E, int D, int F) {
     return D % 128 == 0 && F % 64 == 0 && D >= 128 && F >= 64 && E <= 1024;
 }
@@ -359,13 +361,11 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     // else the CUDA-core router kernel
     if (x_dtype == MOE_BF16 && router->w_dtype == MOE_BF16 && E % 128 == 0 && D % 64 == 0) {
         GemmParams g = {};
-        g.A = x;
+        if (!make_tmap_2d(&g.tmA, 2, x, D, T, 2ull * D, 64, 128, true) ||
+            !make_tmap_2d(&g.tmB0, 2, router->W, D, E, 2ull * D, 64, 128, true))
+            return MOE_ERR_CUDA;
         g.K = D;
-        g.B0 = router->W;
-        g.B1 = router->W;
-        g.b_row_bytes = 2 * D;
         g.rows_per_ntile = 128;
-        g.half_off = 64;
         g.n_mtiles = (T + 127) / 128;
         g.m_total = T;
         g.n_ntiles = E / 128;
@@ -394,10 +394,6 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    void* xh = at<void>(workspace, P.xh);
-    e = launch_to_f16(x, x_dtype == MOE_BF16, xh, (long)T * D, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-
     PermParams pp = {};
     pp.n = T * k;
     pp.k = k;
@@ -420,20 +416,25 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     e = launch_perm(pp, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
+    const long n = (long)T * k;
+    void* xp = at<void>(workspace, P.xh);
+    void* hp = at<void>(workspace, P.hp);
+    void* yp = at<void>(workspace, P.yp);
+    e = launch_gather_f16(x, x_dtype == MOE_BF16, pp.perm_tok, (int)n, D, xp, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
     const int qbits = qbits_of(experts);
-    const int cb = qbits == 8 ? 1 : 2;  // divisor: bytes per element of a code row
+    const int cb = qbits == 8 ? 1 : 2;  // codes per byte
     const bool sf16 = experts->s_dtype == MOE_F16;
     GemmParams g1 = {};
-    g1.A = xh;
-    g1.a_rows = pp.perm_tok;
-    g1.K = D;
-    g1.B0 = experts->gate_q;
-    g1.B1 = experts->up_q;
+    if (!make_tmap_2d(&g1.tmA, 1, xp, D, n, 2ull * D, 64, 128, true) ||
+        !make_tmap_2d(&g1.tmB0, 0, experts->gate_q, D / cb, (unsigned long long)E * F, D / cb, 64 / cb, 64, false) ||
+        !make_tmap_2d(&g1.tmB1, 0, experts->up_q, D / cb, (unsigned long long)E * F, D / cb, 64 / cb, 64, false))
+        return MOE_ERR_CUDA;
     g1.S0 = experts->gate_s;
     g1.S1 = experts->up_s;
-    g1.b_row_bytes = D / cb;
-    g1.b_estride = (size_t)F * (D / cb);
-    g1.s_estride = (size_t)F * (D / kBlk);
+    g1.K = D;
+    g1.b_group_rows = F;
     g1.rows_per_ntile = 64;
     g1.half_off = 0;
     g1.tile_group = pp.tile_group;
@@ -441,32 +442,30 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     g1.group_end = pp.group_end;
     g1.n_mtiles_dev = pp.n_mtiles;
     g1.n_ntiles = F / 64;
-    g1.C = at<void>(workspace, P.hp);
+    g1.C = hp;
     g1.ldc = F;
     g1.hdr = hdr;
     e = launch_gemm(g1, qbits, sf16, true, P.max_mtiles, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     GemmParams g2 = g1;
-    g2.A = at<void>(workspace, P.hp);
-    g2.a_rows = nullptr;
-    g2.K = F;
-    g2.B0 = experts->down_q;
-    g2.B1 = experts->down_q;
+    if (!make_tmap_2d(&g2.tmA, 1, hp, F, n, 2ull * F, 64, 128, true) ||
+        !make_tmap_2d(&g2.tmB0, 0, experts->down_q, F / cb, (unsigned long long)E * D, F / cb, 64 / cb, 64, false))
+        return MOE_ERR_CUDA;
+    g2.tmB1 = g2.tmB0;
     g2.S0 = experts->down_s;
     g2.S1 = experts->down_s;
-    g2.b_row_bytes = F / cb;
-    g2.b_estride = (size_t)D * (F / cb);
-    g2.s_estride = (size_t)D * (F / kBlk);
+    g2.K = F;
+    g2.b_group_rows = D;
     g2.rows_per_ntile = 128;
     g2.half_off = 64;
     g2.n_ntiles = D / 128;
-    g2.C = at<void>(workspace, P.yp);
+    g2.C = yp;
     g2.ldc = D;
     e = launch_gemm(g2, qbits, sf16, false, P.max_mtiles, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    CombineParams cp = {T, D, k, pp.inv, w_buf, at<float>(workspace, P.yp), y};
+    CombineParams cp = {T, D, k, pp.inv, w_buf, static_cast<const float*>(yp), y};
     return from_cuda(launch_combine(cp, s));
 }
 

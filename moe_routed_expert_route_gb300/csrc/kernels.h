@@ -1,6 +1,8 @@
 // Kernel parameter blocks and launchers (internal to the library).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -121,17 +123,15 @@ struct FusedParams {
 };
 
 // Grouped tensor-core matrix product (prefill). Tile (mt, nt): 128 rows of A
-// (positions m0.. of tile mt, gathered through a_rows) times 128 rows of B.
-struct GemmParams {
-    const void* A;              // row-major 16-bit [rows][K]
-    const int32_t* a_rows;      // position -> A row, or null (identity)
+// (positions m0.. of tile mt) times 128 rows of B; operands arrive by TMA.
+struct GemmParams {  // aligned like CUtensorMap
+    CUtensorMap tmA;            // 16-bit [rows][K], box {64, 128}, 128-byte swizzle
+    CUtensorMap tmB0, tmB1;     // codes [rows][row bytes], box {64 or 32 bytes, 64 rows};
+                                // 16-bit B (router): tmB0 only, box {64, 128}, swizzled
+    const void *S0, *S1;        // scales of B0 / B1 rows (quantised B)
     int K;
-    const void *B0, *B1;        // B rows [0,64) of a tile from B0, [64,128) from B1
-    const void *S0, *S1;        // their scales (quantised B), or null
-    size_t b_estride;           // bytes between experts' code matrices
-    size_t s_estride;           // scale elements between experts
-    int b_row_bytes;
-    int rows_per_ntile;         // B row of tile nt, row j: nt*rows_per_ntile + (j&63) + (j>=64)*half_off
+    int b_group_rows;           // B rows per expert (row of expert g = g * b_group_rows + ...)
+    int rows_per_ntile;         // tile nt, row j: nt*rows_per_ntile + (j&63) + (j>=64)*half_off
     int half_off;
     const int32_t* tile_group;  // [mt] expert, or null (group 0)
     const int32_t* tile_m0;     // [mt] first position, or null (mt*128)
@@ -142,6 +142,10 @@ struct GemmParams {
     int ldc;
     WsHeader* hdr;
 };
+
+// 2-D tensor map over a row-major matrix (dtype 0 = uint8, 1 = fp16, 2 = bf16).
+bool make_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long long inner, unsigned long long rows,
+                  unsigned long long row_bytes, unsigned box_inner, unsigned box_rows, bool swizzle128);
 
 struct TopkParams {
     int T, E, k, norm_topk;
@@ -182,7 +186,8 @@ struct CombineParams {
 
 cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu, int max_mtiles, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
-cudaError_t launch_to_f16(const void* x, bool x_bf16, void* out, long n, cudaStream_t s);
+cudaError_t launch_gather_f16(const void* x, bool x_bf16, const int32_t* perm_tok, int n, int D, void* Xp,
+                              cudaStream_t s);
 cudaError_t launch_perm(const PermParams& p, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 

@@ -28,6 +28,8 @@
 // stage and commits to the stage's "empty" barrier; 4 stages of 64 along K are
 // in flight. After the last stage warps 0-3 read the accumulator rows from
 // TMEM (tcgen05.ld) and write the tile. Every wait is bounded.
+#include <mutex>
+
 #include "group.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -37,18 +39,8 @@ namespace moe {
 constexpr int kGM = 128;   // tile rows (tokens)
 constexpr int kGN = 128;   // tile columns (B rows)
 constexpr int kGK = 64;    // K per stage = one 128-byte row of 16-bit values
-constexpr int kGS = 4;     // stages
-constexpr int kGThreads = 160;
-
-template <int BMODE, typename ST>
-struct GemmStage {
-    static constexpr int kA = kGM * 128;
-    static constexpr int kB = kGN * 128;
-    static constexpr int kRaw = BMODE == 8 ? kGN * 64 : (BMODE == 4 ? kGN * 32 : 0);
-    static constexpr int kSc = BMODE == 16 ? 0 : kGN * 2 * (int)sizeof(ST);
-    static constexpr int kBytes = ((kA + kB + kRaw + kSc) + 1023) / 1024 * 1024;
-    static constexpr size_t kSmem = (size_t)kBytes * kGS + 1024;  // + alignment slack
-};
+constexpr int kGS = 4;     // stages of A and B tiles
+constexpr int kGThreads = 224;
 
 // 8 codes (int8) -> 8 fp16 values q*s, rounded once.
 __device__ __forceinline__ uint4 deq8_i8(uint2 w, float s) {
@@ -85,12 +77,37 @@ __device__ __forceinline__ uint4 deq8_i4(uint32_t w, float s) {
     return out;
 }
 
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+template <int BMODE, typename ST>
+struct GemmSmem {
+    static constexpr int kR = BMODE == 16 ? 1 : (BMODE == 8 ? 8 : 12);  // raw code stages
+    static constexpr int kRB = BMODE == 8 ? 64 : 32;                    // raw bytes per row per stage
+    static constexpr int kAB = 2 * 16384;                               // A + B tile of one stage
+    static constexpr int kRaw = BMODE == 16 ? 0 : kGN * kRB;
+    static constexpr size_t kBytes = (size_t)kGS * kAB + (size_t)kR * kRaw + 1024;
+};
+
+// Warp roles (224 threads): warp 0 streams the int8/int4 codes of the B tile
+// (TMA, kR stages ahead); warp 6 streams the A tile (TMA, 128-byte swizzle;
+// also the B tile when B is already 16-bit); warps 1-4 dequantise one B row
+// each into the swizzled layout and later run the epilogue; one thread of
+// warp 5 issues the MMAs and owns the TMEM allocation.
 template <int BMODE, typename ST, bool BF16, bool SWIGLU>
-__global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(GemmParams p) {
-    using Stg = GemmStage<BMODE, ST>;
+__global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+    using L = GemmSmem<BMODE, ST>;
+    constexpr int R = L::kR;
     extern __shared__ unsigned char sm_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ __align__(8) uint64_t full[kGS], empty[kGS], done;
+    unsigned char* ab = sm;                          // [kGS][A 16 KB | B 16 KB]
+    unsigned char* raw = sm + (size_t)kGS * L::kAB;  // [R][128 rows][kRB]
+    __shared__ __align__(8) uint64_t raw_full[R], raw_empty[R], a_full[kGS], b_full[kGS], ab_empty[kGS], done;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -108,14 +125,19 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(GemmParams p) {
 
     if (tid == 0) {
         s_abort = 0;
+        for (int i = 0; i < R; i++) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], 128);
+        }
         for (int i = 0; i < kGS; i++) {
-            mbar_init(&full[i], 128);
-            mbar_init(&empty[i], 1);
+            mbar_init(&a_full[i], 1);
+            mbar_init(&b_full[i], 128);
+            mbar_init(&ab_empty[i], 1);
         }
         mbar_init(&done, 1);
         fence_barrier_init();
     }
-    if (warp == 4) {
+    if (warp == 5) {
         tmem_alloc(&s_tmem, 128);
         tmem_relinquish();
     }
@@ -123,81 +145,103 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(GemmParams p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    const int brow0 = g * p.b_group_rows + nt * p.rows_per_ntile;  // B rows [0,64): brow0.. of map B0
 
-    if (warp < 4) {
-        // ------------------------------------------------ producers
-        const int j = tid;  // A row and B row of the tile owned by this thread
-        const int apos = m0 + j;
-        const bool avalid = apos < m_end;
-        const int arow = p.a_rows ? ld_cg_i32(p.a_rows + (avalid ? apos : m0)) : (avalid ? apos : m0);
-        const uint16_t* Arow = reinterpret_cast<const uint16_t*>(p.A) + (size_t)arow * p.K;
-        const int half = j >> 6;
-        const int brow = nt * p.rows_per_ntile + (j & 63) + half * p.half_off;
-        const unsigned char* Brow = reinterpret_cast<const unsigned char*>(half ? p.B1 : p.B0) +
-                                    (size_t)g * p.b_estride + (size_t)brow * p.b_row_bytes;
-        const ST* Srow = nullptr;
-        if constexpr (BMODE != 16)
-            Srow = reinterpret_cast<const ST*>(half ? p.S1 : p.S0) + (size_t)g * p.s_estride +
-                   (size_t)brow * (p.K / kBlk);
-
-        auto issue = [&](int t) {
-            unsigned char* st = sm + (t % kGS) * Stg::kBytes;
-#pragma unroll
-            for (int c = 0; c < 8; c++) cp_async16(st + sw128_off(j, c), Arow + t * kGK + c * 8);
-            if constexpr (BMODE == 16) {
-#pragma unroll
-                for (int c = 0; c < 8; c++)
-                    cp_async16(st + Stg::kA + sw128_off(j, c), Brow + ((size_t)t * kGK + c * 8) * 2);
-            } else {
-                unsigned char* raw = st + Stg::kA + Stg::kB + j * (BMODE == 8 ? 64 : 32);
-                const unsigned char* src = Brow + (size_t)t * (BMODE == 8 ? 64 : 32);
-#pragma unroll
-                for (int q = 0; q < (BMODE == 8 ? 4 : 2); q++) cp_async16(raw + 16 * q, src + 16 * q);
-                unsigned char* sc = st + Stg::kA + Stg::kB + Stg::kRaw + j * 2 * (int)sizeof(ST);
-#pragma unroll
-                for (int q = 0; q < (int)sizeof(ST) / 2; q++)
-                    cp_async4(sc + 4 * q, reinterpret_cast<const unsigned char*>(Srow + 2 * t) + 4 * q);
+    if (warp == 0) {
+        // ------------------------------------------------ code producer
+        if constexpr (BMODE != 16) {
+            if (lane == 0) {
+                for (int t = 0; t < nk; t++) {
+                    const int s = t % R;
+                    if (t >= R && !mbar_wait(&raw_empty[s], ((t / R) - 1) & 1, status)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&raw_full[s], kGN * L::kRB);
+                    unsigned char* dst = raw + (size_t)s * L::kRaw;
+                    tma_load_2d(dst, &p.tmB0, t * L::kRB, brow0, &raw_full[s]);
+                    tma_load_2d(dst + 64 * L::kRB, &p.tmB1, t * L::kRB, brow0 + p.half_off, &raw_full[s]);
+                }
             }
-        };
-
-#pragma unroll
-        for (int t = 0; t < kGS - 1; t++) {
-            if (t < nk) issue(t);
-            cp_async_commit();
         }
-        for (int s = 0; s < nk && !s_abort; s++) {
-            cp_async_wait<kGS - 2>();
-            unsigned char* st = sm + (s % kGS) * Stg::kBytes;
-            if constexpr (BMODE != 16) {
-                const unsigned char* raw = st + Stg::kA + Stg::kB + j * (BMODE == 8 ? 64 : 32);
-                const ST* sc = reinterpret_cast<const ST*>(st + Stg::kA + Stg::kB + Stg::kRaw +
-                                                           j * 2 * (int)sizeof(ST));
-                const float s0 = to_f32(sc[0]), s1 = to_f32(sc[1]);
+    } else if (warp == 6) {
+        // ------------------------------------------------ A producer
+        if (lane == 0) {
+            for (int t = 0; t < nk; t++) {
+                const int s = t % kGS;
+                if (t >= kGS && !mbar_wait(&ab_empty[s], ((t / kGS) - 1) & 1, status)) {
+                    s_abort = 1;
+                    break;
+                }
+                unsigned char* dst = ab + (size_t)s * L::kAB;
+                mbar_arrive_expect_tx(&a_full[s], BMODE == 16 ? 32768 : 16384);
+                tma_load_2d(dst, &p.tmA, t * kGK, m0, &a_full[s]);
+                if constexpr (BMODE == 16) tma_load_2d(dst + 16384, &p.tmB0, t * kGK, brow0, &a_full[s]);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = umma_idesc_f16(BF16, kGM, kGN);
+            for (int t = 0; t < nk; t++) {
+                const int s = t % kGS;
+                const unsigned ph = (t / kGS) & 1;
+                if (s_abort || !mbar_wait(&a_full[s], ph, status) ||
+                    (BMODE != 16 && !mbar_wait(&b_full[s], ph, status))) {
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_addr(ab + (size_t)s * L::kAB);
+                const uint64_t ad = umma_desc_sw128(a0), bd = umma_desc_sw128(a0 + 16384);
+#pragma unroll
+                for (int kk = 0; kk < kGK / 16; kk++)
+                    umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (t | kk) != 0 ? 1u : 0u);
+                umma_commit(&ab_empty[s]);
+            }
+            umma_commit(&done);  // also after an abort: completes when the issued MMAs are done
+        }
+    } else {
+        // ------------------------------------------------ dequant (warps 1-4)
+        if constexpr (BMODE != 16) {
+            const int j = tid - 32;  // B row of the tile
+            const int half = j >> 6;
+            const ST* Srow = reinterpret_cast<const ST*>(half ? p.S1 : p.S0) +
+                             (size_t)(brow0 + (j & 63) + half * p.half_off) * (p.K / kBlk);
+            float s0n = to_f32(Srow[0]), s1n = to_f32(Srow[1]);
+            for (int t = 0; t < nk; t++) {
+                const int rs = t % R, as = t % kGS;
+                if (s_abort || !mbar_wait(&raw_full[rs], (t / R) & 1, status) ||
+                    (t >= kGS && !mbar_wait(&ab_empty[as], ((t / kGS) - 1) & 1, status))) {
+                    s_abort = 1;
+                    break;
+                }
+                const float s0 = s0n, s1 = s1n;
+                if (t + 1 < nk) {
+                    s0n = to_f32(Srow[2 * t + 2]);
+                    s1n = to_f32(Srow[2 * t + 3]);
+                }
+                const unsigned char* rr = raw + (size_t)rs * L::kRaw + j * L::kRB;
+                unsigned char* bt = ab + (size_t)as * L::kAB + 16384;
 #pragma unroll
                 for (int c = 0; c < 8; c++) {
                     const float scl = c < 4 ? s0 : s1;
                     uint4 v;
-                    if constexpr (BMODE == 8) v = deq8_i8(*reinterpret_cast<const uint2*>(raw + 8 * c), scl);
-                    else v = deq8_i4(*reinterpret_cast<const uint32_t*>(raw + 4 * c), scl);
-                    *reinterpret_cast<uint4*>(st + Stg::kA + sw128_off(j, c)) = v;
+                    if constexpr (BMODE == 8) v = deq8_i8(*reinterpret_cast<const uint2*>(rr + 8 * c), scl);
+                    else v = deq8_i4(*reinterpret_cast<const uint32_t*>(rr + 4 * c), scl);
+                    *reinterpret_cast<uint4*>(bt + sw128_off(j, c)) = v;
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(&raw_empty[rs]);
+                mbar_arrive(&b_full[as]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&full[s % kGS]);
-            const int t = s + kGS - 1;
-            if (t < nk) {
-                if (s >= 1 && !mbar_wait(&empty[(s - 1) % kGS], ((s - 1) / kGS) & 1, status)) s_abort = 1;
-                if (!s_abort) issue(t);
-            }
-            cp_async_commit();
         }
-        cp_async_wait<0>();
-
-        // ------------------------------------------------ epilogue
+        // ------------------------------------------------ epilogue (warps 1-4)
         if (!mbar_wait(&done, 0, status)) s_abort = 1;
         tc_fence_after();
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        const int pos = m0 + j;
+        const int row = 32 * (warp & 3) + lane;  // TMEM lane quarter of this warp
+        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const int pos = m0 + row;
         const bool valid = pos < m_end && !s_abort;
         if constexpr (SWIGLU) {
             __half* C = reinterpret_cast<__half*>(p.C) + (size_t)pos * p.ldc + nt * 64;
@@ -235,34 +279,16 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(GemmParams p) {
                 }
             }
         }
-    } else if (lane == 0) {
-        // ------------------------------------------------ MMA issuer
-        const uint32_t idesc = umma_idesc_f16(BF16, kGM, kGN);
-        for (int s = 0; s < nk; s++) {
-            if (s_abort || !mbar_wait(&full[s % kGS], (s / kGS) & 1, status)) {
-                s_abort = 1;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t a0 = smem_addr(sm + (s % kGS) * Stg::kBytes);
-            const uint64_t ad = umma_desc_sw128(a0), bd = umma_desc_sw128(a0 + Stg::kA);
-#pragma unroll
-            for (int kk = 0; kk < kGK / 16; kk++)
-                umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0 ? 1u : 0u);
-            umma_commit(&empty[s % kGS]);
-        }
-        umma_commit(&done);  // also after an abort: completes when issued MMAs are done
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) tmem_dealloc(tmem, 128);
+    if (warp == 5) tmem_dealloc(tmem, 128);
 }
 
 template <int BMODE, typename ST, bool BF16, bool SWIGLU>
 static cudaError_t launch_gemm_t(const GemmParams& p, int max_mtiles, cudaStream_t s) {
-    size_t smem = GemmStage<BMODE, ST>::kSmem;
     return launch(gemm_tc_kernel<BMODE, ST, BF16, SWIGLU>, dim3(max_mtiles * p.n_ntiles), dim3(kGThreads),
-                  smem, s, true, p);
+                  GemmSmem<BMODE, ST>::kBytes, s, true, p);
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu, int max_mtiles,
@@ -278,6 +304,68 @@ cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu,
                              : launch_gemm_t<4, float, false, true>(p, max_mtiles, s);
     return s_f16 ? launch_gemm_t<4, __half, false, false>(p, max_mtiles, s)
                  : launch_gemm_t<4, float, false, false>(p, max_mtiles, s);
+}
+
+// ---------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool make_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long long inner, unsigned long long rows,
+                  unsigned long long row_bytes, unsigned box_inner, unsigned box_rows, bool swizzle128) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUtensorMapDataType dt = dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                            : dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// x rows in grouped order as fp16: Xp[pos] = fp16(x[perm_tok[pos]]), 8 per thread
+__global__ void __launch_bounds__(256) gather_f16_kernel(const void* x, int x_bf16, const int32_t* perm_tok,
+                                                         int n, int D, __half* Xp) {
+    pdl_wait();
+    pdl_trigger();
+    const int per_row = D / 8;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < (long)n * per_row;
+         i += (long)gridDim.x * blockDim.x) {
+        const int pos = (int)(i / per_row), c = (int)(i - (long)pos * per_row) * 8;
+        const int t = ld_cg_i32(perm_tok + pos);
+        float f[8];
+        if (x_bf16) load_f32_cg<__nv_bfloat16, 8>(reinterpret_cast<const __nv_bfloat16*>(x) + (size_t)t * D + c, f);
+        else load_f32_cg<float, 8>(reinterpret_cast<const float*>(x) + (size_t)t * D + c, f);
+        uint4 o;
+        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            __half2 h = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
+            ow[q] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(Xp + (size_t)pos * D + c) = o;
+    }
+}
+
+cudaError_t launch_gather_f16(const void* x, bool x_bf16, const int32_t* perm_tok, int n, int D, void* Xp,
+                              cudaStream_t s) {
+    long work = (long)n * (D / 8);
+    long blocks = std::min<long>((work + 255) / 256, 152L * 16);
+    return launch(gather_f16_kernel, dim3((unsigned)std::max<long>(blocks, 1)), dim3(256), 0, s, true, x,
+                  x_bf16 ? 1 : 0, perm_tok, n, D, reinterpret_cast<__half*>(Xp));
 }
 
 // ----------------------------------------------------------- routing
@@ -316,26 +404,6 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
         case 16: return launch(topk_kernel<16>, grid, block, 0, s, true, p);
         default: return launch(topk_kernel<32>, grid, block, 0, s, true, p);
     }
-}
-
-// x (bf16 or fp32) -> fp16, 4 elements per thread
-__global__ void __launch_bounds__(256) to_f16_kernel(const void* x, int x_bf16, __half* out, long n) {
-    pdl_wait();
-    pdl_trigger();
-    for (long i = ((long)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n; i += (long)gridDim.x * blockDim.x * 4) {
-        float f[4];
-        if (x_bf16) load_f32_cg<__nv_bfloat16, 4>(reinterpret_cast<const __nv_bfloat16*>(x) + i, f);
-        else load_f32_cg<float, 4>(reinterpret_cast<const float*>(x) + i, f);
-        __half2 a = __floats2half2_rn(f[0], f[1]), b = __floats2half2_rn(f[2], f[3]);
-        uint2 o = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
-        *reinterpret_cast<uint2*>(out + i) = o;
-    }
-}
-
-cudaError_t launch_to_f16(const void* x, bool x_bf16, void* out, long n, cudaStream_t s) {
-    long blocks = std::min<long>((n / 4 + 255) / 256, 152L * 8);
-    return launch(to_f16_kernel, dim3((unsigned)std::max<long>(blocks, 1)), dim3(256), 0, s, true, x,
-                  x_bf16 ? 1 : 0, reinterpret_cast<__half*>(out), n);
 }
 
 // ------------------------------------------------------ grouping by expert
