@@ -15,16 +15,16 @@
 //   2  warp 0 of every CTA polls all E logits and runs the softmax + top-k
 //      (no second exchange is needed to learn the routing); the other warps
 //      turn x into 16-bit fixed-point planes meanwhile
-//   3  the 16 warps stream this CTA's share of the k*F gate/up row pairs from
-//      HBM (two row pairs in flight per warp) and write h = silu(g)*u to the
-//      workspace; one thread then starts bulk (TMA) copies of this CTA's rows
-//      of the k down matrices into shared memory, and the CTA arrives on a
-//      completion counter (polling ~150 KB of tagged activations from every
+//   3  one thread starts bulk (TMA) copies of this CTA's rows of the k down
+//      matrices into shared memory while the 16 warps stream this CTA's share
+//      of the k*F gate/up row pairs from HBM (two row pairs in flight per
+//      warp) and write h = silu(g)*u to the workspace; the CTA then arrives on
+//      a completion counter (polling ~150 KB of tagged activations from every
 //      CTA would flood L2 while other CTAs still stream)
 //   4  each warp owns one slot: it reads that slot's activations into
-//      registers and dots them (fp32, codes widened exactly) against the staged
-//      down rows of its share of the CTA's rows; the CTA combines the k slots
-//      in slot order,
+//      registers as 16-bit fixed point and dots them (integer dp4a) against the
+//      staged down rows of its share of the CTA's rows; the CTA combines the k
+//      slots in slot order,
 //      y[d] = sum_r w[r] * o_r[d], and writes x_next = x + y.
 // Without a router (moe_decode) phases 0-2 are replaced by reading idx/w.
 #include "dots.cuh"
@@ -64,7 +64,7 @@ __host__ __device__ inline FusedLayout fused_layout(int D, int F, int k, int qbi
 template <int QB, typename ST>
 struct RowPair {
     uint4 g[kNCH], u[kNCH];
-    float gs[kNCH], us[kNCH];
+    ST gs[kNCH], us[kNCH];  // widened where used, so no load is waited for early
 };
 
 // Fixed-point conversion of NB blocks of 32 values held one per lane, the
@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     __shared__ int s_abort;
     __shared__ unsigned s_seq;
     __shared__ __align__(8) uint64_t s_bar;
+    __shared__ uint64_t s_tk[kTopkScratch];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x, G = gridDim.x;
@@ -155,11 +156,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     __syncthreads();
     const unsigned tag = seq_tag(s_seq);
 
-    // x -> fixed-point planes, by warps first..15 (warp 0 is busy with the
-    // routing when there is a router)
-    auto convert_x = [&](int first) {
-        const int nw = kFWarps - first;
-        for (int b0 = warp - first; b0 < nb; b0 += nw * 4) {
+    // x -> fixed-point planes. With a router, warp 0 selects the experts
+    // meanwhile and the conversion runs on the 12 warps that do not share its
+    // scheduler (warps w with w % 4 != 0), so the selection is not slowed.
+    auto convert_x = [&](bool routing) {
+        const int nw = routing ? kFWarps - kFWarps / 4 : kFWarps;
+        const int wi = routing ? warp - (warp >> 2) - 1 : warp;
+        for (int b0 = wi; b0 < nb; b0 += nw * 4) {
             float v[4];
             int blk[4];
 #pragma unroll
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
             ld_tagged_all<NJ>(p.logits, lane, 32, p.E, tag, lg, status, &s_abort);
             int sel_e;
             float sel_p;
-            softmax_topk_regs<NJ>(lg, p.E, k, (c == 0) ? p.probs : nullptr, lane, sel_e, sel_p);
+            softmax_topk_regs<NJ>(lg, p.E, k, (c == 0) ? p.probs : nullptr, lane, s_tk, sel_e, sel_p);
             if (sel_e < 0 || sel_e >= p.E) sel_e = -1;  // only after a timed-out poll; never dereferenced
             float norm = warp_sum(lane < k ? sel_p : 0.f);
             float wv = p.norm_topk ? sel_p / norm : sel_p;
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                     p.w[lane] = wv;
                 }
             }
-        } else {
-            convert_x(1);
+        } else if (warp & 3) {
+            convert_x(true);
         }
     } else {
         if (tid < k) {
@@ -228,16 +231,14 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
             s_idx[tid] = e;
             s_w[tid] = ld_cg_f32(p.w_in + tid);
         }
-        convert_x(0);
+        convert_x(false);
     }
     __syncthreads();
 
     // ---------------------------------------------------------- phase 3
     const int d_begin = (int)((long)c * D / G), d_end = (int)((long)(c + 1) * D / G);
     const int nrows = d_end - d_begin;
-    // bulk copies of this CTA's down rows, started after this CTA's gate/up
-    // rows: those bytes are needed first, the down rows only after the
-    // activation exchange, which they overlap
+    // bulk copies of this CTA's down rows and their scales
     auto issue_down = [&]() {
         unsigned bytes = 0;
         for (int r = 0; r < k; r++)
@@ -276,11 +277,11 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                 rp.g[j] = ld_stream16(GQ + row * rowD + 16 * ci);
                 rp.u[j] = ld_stream16(UQ + row * rowD + 16 * ci);
                 int blk = QB == 8 ? (ci >> 1) : ci;
-                rp.gs[j] = to_f32(GS[row * nb + blk]);
-                rp.us[j] = to_f32(US[row * nb + blk]);
+                rp.gs[j] = ldg_nc(GS + row * nb + blk);
+                rp.us[j] = ldg_nc(US + row * nb + blk);
             } else {
                 rp.g[j] = rp.u[j] = make_uint4(0, 0, 0, 0);
-                rp.gs[j] = rp.us[j] = 0.f;
+                rp.gs[j] = rp.us[j] = ST(0.f);
             }
         }
     };
@@ -306,8 +307,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                     iu = dot_i4_chunk(rp.u[j], h0, h1, l0, l1);
                     xs = s_xs[ci] * (1.0f / 16.0f);
                 }
-                ga = fmaf((float)ig, rp.gs[j] * xs, ga);
-                ua = fmaf((float)iu, rp.us[j] * xs, ua);
+                ga = fmaf((float)ig, to_f32(rp.gs[j]) * xs, ga);
+                ua = fmaf((float)iu, to_f32(rp.us[j]) * xs, ua);
             }
         }
 #pragma unroll
@@ -322,6 +323,10 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
         RowPair<QB, ST> A, B;
         int g = g_begin + warp;
         load_pair(g, A);
+        // the down rows are requested together with the first gate/up rows so
+        // that they stream concurrently; issued by a thread that never runs the
+        // release fence of the exchange below (a fence may wait for them)
+        if (tid == 32) issue_down();
         while (g < g_end) {
             int g2 = g + kFWarps;
             load_pair(g2, B);
@@ -334,9 +339,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
         }
     }
 
-    // the down rows stream while the CTAs exchange activations
-    if (tid == 0) issue_down();
-
     // ---------------------------------------------------------- phase 4
     // wait for every CTA's activations (one counter per launch parity; the
     // other one is cleared for the next launch). Each warp owns one slot: it
@@ -348,20 +350,52 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
     const int wps = kFWarps / k;  // warps per slot (k <= 16)
     const int slot = warp / wps, sub = warp - slot * wps;
     if (slot < k && s_idx[slot] >= 0) {
+        // The slot's activations, 8-byte pieces of codes per lane: piece pc
+        // covers EPP consecutive units. They are turned into 16-bit fixed
+        // point (as x is) with one power-of-two scale per block of 32 units,
+        // the block max taken over the lanes holding the block, so that each
+        // piece is dotted with integer dp4a.
         constexpr int EPP = QB == 8 ? 8 : 16;   // codes per 8-byte piece
         constexpr int NPL = QB == 8 ? 4 : 2;    // pieces per lane (F <= 1024)
-        const int npieces = rowF / 8;
-        float hreg[NPL][EPP];
+        constexpr int LPB = kBlk / EPP;         // lanes per block: 4 or 2
+        constexpr int NW = EPP / 4;             // plane words per piece and plane
+        const int npieces = (QB == 8 ? F : F / 2) / 8;
+        uint32_t hp[NPL][NW], lp[NPL][NW];
+        float hsc[NPL];
 #pragma unroll
         for (int i = 0; i < NPL; i++) {
             const int pc = i * 32 + lane;
+            float v[EPP];
 #pragma unroll
             for (int q = 0; q < EPP; q += 4) {
-                uint4 v = pc < npieces ? ld_cg16(p.h + (size_t)slot * F + pc * EPP + q) : make_uint4(0, 0, 0, 0);
-                hreg[i][q] = __uint_as_float(v.x);
-                hreg[i][q + 1] = __uint_as_float(v.y);
-                hreg[i][q + 2] = __uint_as_float(v.z);
-                hreg[i][q + 3] = __uint_as_float(v.w);
+                uint4 t = pc < npieces ? ld_cg16(p.h + (size_t)slot * F + pc * EPP + q) : make_uint4(0, 0, 0, 0);
+                v[q] = __uint_as_float(t.x);
+                v[q + 1] = __uint_as_float(t.y);
+                v[q + 2] = __uint_as_float(t.z);
+                v[q + 3] = __uint_as_float(t.w);
+            }
+            float m = 0.f;
+#pragma unroll
+            for (int q = 0; q < EPP; q++) m = fmaxf(m, fabsf(v[q]));
+#pragma unroll
+            for (int o = 1; o < LPB; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+            const Fx f = fx_of_blockmax(m);
+            hsc[i] = QB == 8 ? f.scale : f.scale * (1.0f / 16.0f);
+#pragma unroll
+            for (int w = 0; w < NW; w++) {
+                uint32_t hw = 0, lw = 0;
+#pragma unroll
+                for (int bq = 0; bq < 4; bq++) {
+                    // int8: byte bq of word w is unit 4w + bq; int4: word w
+                    // holds the even units of its 8-unit group (w even) or the
+                    // odd ones (w odd), as dot_i4_word expects
+                    const int q = QB == 8 ? 4 * w + bq : 8 * (w >> 1) + 2 * bq + (w & 1);
+                    const int X = fx_code(v[q], f.mul);
+                    hw |= (uint32_t)((X >> 8) & 0xff) << (8 * bq);
+                    lw |= (uint32_t)(X & 0xff) << (8 * bq);
+                }
+                hp[i][w] = hw;
+                lp[i][w] = lw;
             }
         }
         const uint8_t* dq0 = s_dq + (size_t)slot * p.rows * rowF;
@@ -379,27 +413,17 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(FusedParams p
                         if (pc < npieces) {
                             const uint2 wv = *reinterpret_cast<const uint2*>(dq0 + (size_t)row * rowF + 8 * pc);
                             const float sc = to_f32(ds0[row * nbF + (EPP * pc) / kBlk]);
-                            float dot = 0.f;
+                            int hd = 0, ld = 0;
                             if constexpr (QB == 8) {
-                                // int8 -> fp32 exactly: 2^23 + (q + 128) from the byte, minus 2^23 + 128
-                                const uint32_t u0 = wv.x ^ 0x80808080u, u1 = wv.y ^ 0x80808080u;
-#pragma unroll
-                                for (int q = 0; q < 8; q++) {
-                                    const uint32_t src = q < 4 ? u0 : u1;
-                                    const float f = __uint_as_float(__byte_perm(src, 0x4B000000u, 0x7540 + (q & 3)));
-                                    dot = fmaf(f - 8388736.0f, hreg[i][q], dot);
-                                }
+                                hd = dp4a_ss(wv.x, hp[i][0], hd);
+                                hd = dp4a_ss(wv.y, hp[i][1], hd);
+                                ld = dp4a_su(wv.x, lp[i][0], ld);
+                                ld = dp4a_su(wv.y, lp[i][1], ld);
                             } else {
-                                // int4: nibble n of the word (element n) -> 2^23 + (q + 8), minus 2^23 + 8
-                                const uint32_t u0 = wv.x ^ 0x88888888u, u1 = wv.y ^ 0x88888888u;
-#pragma unroll
-                                for (int q = 0; q < 16; q++) {
-                                    const uint32_t src = q < 8 ? u0 : u1;
-                                    const float f = __uint_as_float(((src >> (4 * (q & 7))) & 0xFu) | 0x4B000000u);
-                                    dot = fmaf(f - 8388616.0f, hreg[i][q], dot);
-                                }
+                                dot_i4_word(wv.x, hp[i][0], hp[i][1], lp[i][0], lp[i][1], hd, ld);
+                                dot_i4_word(wv.y, hp[i][2], hp[i][3], lp[i][2], lp[i][3], hd, ld);
                             }
-                            acc[u] = fmaf(sc, dot, acc[u]);
+                            acc[u] = fmaf(sc * hsc[i], (float)(hd * 256 + ld), acc[u]);
                         }
                     }
                 }

@@ -118,20 +118,79 @@ __device__ __forceinline__ void bitonic_sort_desc(uint64_t (&v)[N]) {
             }
 }
 
+// The same networks on fp32 values (largest first).
+template <int N>
+__device__ __forceinline__ void bitonic_merge_desc_f(float (&v)[N]) {
+#pragma unroll
+    for (int stride = N / 2; stride > 0; stride >>= 1)
+#pragma unroll
+        for (int i = 0; i < N; i++)
+            if ((i & stride) == 0) {
+                const float hi = fmaxf(v[i], v[i + stride]), lo = fminf(v[i], v[i + stride]);
+                v[i] = hi;
+                v[i + stride] = lo;
+            }
+}
+template <int N>
+__device__ __forceinline__ void bitonic_sort_desc_f(float (&v)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+        for (int stride = size / 2; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < N; i++) {
+                const int j = i + stride;
+                if ((i & stride) == 0) {
+                    const float hi = fmaxf(v[i], v[j]), lo = fminf(v[i], v[j]);
+                    if ((i & size) == 0) { v[i] = hi; v[j] = lo; }   // descending run
+                    else { v[i] = lo; v[j] = hi; }                   // ascending run
+                }
+            }
+}
+
+// Scratch of softmax_topk_regs: 2 * 32 keys per warp, warp-private.
+constexpr int kTopkScratch = 64;
+
 // Softmax and top-k of one token, by one warp, from logits already in
 // registers: lane l holds the logits of experts l, l+32, ... (NJ per lane, a
 // power of two, NJ*32 >= E, NJ >= k; entries e >= E are ignored).
 // Probabilities are p_e = exp(l_e - max) * (1 / sum); the k largest are chosen
 // largest first, equal fp32 values by lower expert id. Lanes r < k return
-// (sel_e, sel_p) of rank r.
+// (sel_e, sel_p) of rank r. `scratch` holds kTopkScratch 64-bit words of
+// shared memory private to the warp.
+//
+// The selection works in two passes so that the long networks run on 32-bit
+// values: the k-th largest logit l_k is found first (a per-lane sort and a
+// butterfly that keeps the NJ largest of each union; its first entry is also
+// the max the softmax needs). p is a non-decreasing function of l, so the k-th
+// largest p is p* = p(l_k), read from an expert whose logit is l_k; the chosen
+// experts are then every e with p_e > p* and, of those with p_e == p*, the
+// lowest ids up to k. Only those k are ranked, by (p desc, id asc).
 template <int NJ>
 __device__ __forceinline__ void softmax_topk_regs(float (&p)[NJ], int E, int k, float* __restrict__ probs_t,
-                                                  int lane, int& sel_e, float& sel_p) {
-    float mx = -INFINITY;
+                                                  int lane, uint64_t* scratch, int& sel_e, float& sel_p) {
+    float t[NJ];
 #pragma unroll
-    for (int j = 0; j < NJ; j++)
-        if (j * 32 + lane < E) mx = fmaxf(mx, p[j]);
-    mx = warp_max(mx);
+    for (int j = 0; j < NJ; j++) t[j] = (j * 32 + lane < E) ? p[j] : -INFINITY;
+    bitonic_sort_desc_f<NJ>(t);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float b[NJ];
+#pragma unroll
+        for (int i = 0; i < NJ; i++) b[i] = __shfl_xor_sync(kFull, t[i], o);
+#pragma unroll
+        for (int i = 0; i < NJ; i++) t[i] = fmaxf(t[i], b[NJ - 1 - i]);
+        bitonic_merge_desc_f<NJ>(t);
+    }
+    const float mx = t[0];
+    float lk = t[0];
+#pragma unroll
+    for (int i = 0; i < NJ; i++)
+        if (i == k - 1) lk = t[i];
+    unsigned at_lk[NJ];  // which lanes hold an expert whose logit is l_k
+#pragma unroll
+    for (int j = 0; j < NJ; j++) at_lk[j] = __ballot_sync(kFull, j * 32 + lane < E && p[j] == lk);
+
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < NJ; j++) {
@@ -147,46 +206,66 @@ __device__ __forceinline__ void softmax_topk_regs(float (&p)[NJ], int E, int k, 
         p[j] = p[j] * inv_s;
         if (e < E && probs_t) probs_t[e] = p[j];
     }
-    // selection: order key (fp32 bits + 1 of p >= 0, 0 for padding) in the
-    // high word, ~id in the low word, so that one unsigned 64-bit comparison
-    // ranks "larger p first, lower id on equal p"
-    uint64_t v[NJ];
+    float pk = 0.f;
+    bool found = false;
+#pragma unroll
+    for (int j = 0; j < NJ; j++)  // warp-uniform
+        if (!found && at_lk[j]) {
+            pk = __shfl_sync(kFull, p[j], __ffs(at_lk[j]) - 1);
+            found = true;
+        }
+
+    // the chosen set, written in id order to scratch[0..k)
+    const unsigned lt = (1u << lane) - 1u;
+    int n_gt = 0;
+    unsigned eqm[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; j++) {
-        int e = j * 32 + lane;
-        unsigned key = (e < E) ? __float_as_uint(p[j]) + 1u : 0u;
-        v[j] = ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (unsigned)e);
+        const bool valid = j * 32 + lane < E;
+        n_gt += __popc(__ballot_sync(kFull, valid && p[j] > pk));
+        eqm[j] = __ballot_sync(kFull, valid && p[j] == pk);
     }
-    bitonic_sort_desc<NJ>(v);  // this lane's values, best first
-    constexpr int KP = NJ;  // list length kept while merging (>= k)
-    // butterfly over the lanes: two sorted lists -> the KP best of their union
-    // (max of A[i] and B[KP-1-i] is bitonic, then a bitonic merge sorts it);
-    // both partners get the same list, so after 5 rounds every lane holds the
-    // warp's KP best, sorted
+    const int need = k - n_gt;  // >= 1 when the logits are finite
+    int eq_before = 0, pos = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        uint64_t b[KP];
-#pragma unroll
-        for (int i = 0; i < KP; i++) b[i] = __shfl_xor_sync(kFull, v[i], o);
-#pragma unroll
-        for (int i = 0; i < KP; i++) v[i] = v[i] > b[KP - 1 - i] ? v[i] : b[KP - 1 - i];
-        bitonic_merge_desc<KP>(v);
+    for (int j = 0; j < NJ; j++) {
+        const int e = j * 32 + lane;
+        const bool valid = e < E;
+        const bool take = valid && (p[j] > pk || (p[j] == pk && eq_before + __popc(eqm[j] & lt) < need));
+        eq_before += __popc(eqm[j]);
+        const unsigned tm = __ballot_sync(kFull, take);
+        const int at = pos + __popc(tm & lt);
+        // order key: fp32 bits + 1 of p >= 0 in the high word, ~id in the low
+        // word: one unsigned comparison ranks "larger p first, lower id on equal p"
+        if (take && at < k)
+            scratch[at] = ((uint64_t)(__float_as_uint(p[j]) + 1u) << 32) | (uint64_t)(0xffffffffu - (unsigned)e);
+        pos += __popc(tm);
     }
+    __syncwarp();
+    const int nsel = pos < k ? pos : k;
+    uint64_t mine = 0;
+    int rank = 0;
+    if (lane < nsel) {
+        mine = scratch[lane];
+        for (int i = 0; i < nsel; i++) rank += scratch[i] > mine ? 1 : 0;
+    }
+    __syncwarp();
+    if (lane < nsel) scratch[32 + rank] = mine;
+    __syncwarp();
     sel_e = -1;
     sel_p = 0.f;
-#pragma unroll
-    for (int i = 0; i < KP; i++) {
-        if (i == lane && i < k && (unsigned)(v[i] >> 32) != 0u) {
-            sel_e = (int)(0xffffffffu - (unsigned)v[i]);
-            sel_p = __uint_as_float((unsigned)(v[i] >> 32) - 1u);
-        }
+    if (lane < nsel) {
+        const uint64_t v = scratch[32 + lane];
+        sel_e = (int)(0xffffffffu - (unsigned)v);
+        sel_p = __uint_as_float((unsigned)(v >> 32) - 1u);
     }
+    __syncwarp();
 }
 
 // The same, reading the logits (written by an earlier kernel) through L2.
 template <int NJ>
 __device__ __forceinline__ void softmax_topk_warp(const float* __restrict__ logits_t, int E, int k,
-                                                  float* __restrict__ probs_t, int lane,
+                                                  float* __restrict__ probs_t, int lane, uint64_t* scratch,
                                                   int& sel_e, float& sel_p) {
     float p[NJ];
 #pragma unroll
@@ -194,7 +273,7 @@ __device__ __forceinline__ void softmax_topk_warp(const float* __restrict__ logi
         int e = j * 32 + lane;
         p[j] = (e < E) ? ld_cg_f32(logits_t + e) : -INFINITY;
     }
-    softmax_topk_regs<NJ>(p, E, k, probs_t, lane, sel_e, sel_p);
+    softmax_topk_regs<NJ>(p, E, k, probs_t, lane, scratch, sel_e, sel_p);
 }
 
 }  // namespace moe

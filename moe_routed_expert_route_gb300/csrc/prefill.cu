@@ -77,13 +77,6 @@ __device__ __forceinline__ uint4 deq8_i4(uint32_t w, float s) {
     return out;
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-        : "memory");
-}
 
 template <int BMODE, typename ST>
 struct GemmSmem {
@@ -375,6 +368,7 @@ template <int NJ>
 __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    __shared__ uint64_t s_tk[8][kTopkScratch];
     pdl_wait();
     pdl_trigger();
     if (t >= p.T) return;
@@ -386,7 +380,8 @@ __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
     }
     int sel_e;
     float sel_p;
-    softmax_topk_regs<NJ>(v, p.E, p.k, p.probs ? p.probs + (size_t)t * p.E : nullptr, lane, sel_e, sel_p);
+    softmax_topk_regs<NJ>(v, p.E, p.k, p.probs ? p.probs + (size_t)t * p.E : nullptr, lane, s_tk[threadIdx.x >> 5],
+                          sel_e, sel_p);
     float norm = warp_sum(lane < p.k ? sel_p : 0.f);
     if (lane < p.k) {
         p.idx[(size_t)t * p.k + lane] = sel_e;

@@ -18,6 +18,7 @@ template <typename WT, typename XT, int NCH, int NJ>
 __global__ void __launch_bounds__(256) router_kernel(RouterParams p) {
     extern __shared__ int s_mem[];
     __shared__ int s_last;
+    __shared__ uint64_t s_tk[8][kTopkScratch];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int e = blockIdx.x * 8 + warp;
     constexpr int EPC = 16 / sizeof(WT);  // weights per 16-byte chunk
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(256) router_kernel(RouterParams p) {
         int sel_e;
         float sel_p;
         softmax_topk_warp<NJ>(p.logits + (size_t)t * p.E, p.E, p.k,
-                              p.probs ? p.probs + (size_t)t * p.E : nullptr, lane, sel_e, sel_p);
+                              p.probs ? p.probs + (size_t)t * p.E : nullptr, lane, s_tk[warp], sel_e, sel_p);
         float norm = warp_sum(lane < p.k ? sel_p : 0.f);
         if (lane < p.k) {
             p.idx[(size_t)t * p.k + lane] = sel_e;

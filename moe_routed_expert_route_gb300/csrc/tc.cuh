@@ -2,6 +2,8 @@
 // (inline PTX for sm_100a-family targets, here sm_103a).
 #pragma once
 
+#include <cuda.h>
+
 #include "sync.cuh"
 
 namespace moe {
@@ -80,6 +82,17 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
 // Byte offset of 16-byte chunk c (0..7) of row r in such a tile.
 __host__ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
     return (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4);
+}
+
+// 2-D tiled TMA load of one box at element coordinates (x, y) of `map` into
+// shared memory; completion counted on `bar`. x * element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
 }
 
 // Makes generic-proxy writes to shared memory visible to the async proxy

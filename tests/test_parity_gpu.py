@@ -344,3 +344,54 @@ def test_bad_expert_id_is_reported_and_skipped():
     idx.fill_(1)
     M.moe_decode(experts, x, idx, w, y, None, ws)
     assert M.moe_check_status(ws) == M.MOE_OK
+
+
+# ------------------------------------------------------------ exact ties
+def _tied_router(E, D, n_distinct, seed):
+    """Router rows drawn from only n_distinct rows, scattered over the experts,
+    so that many experts get bit-identical logits: the top-k is then decided by
+    the lowest-index rule alone."""
+    g = torch.Generator().manual_seed(seed)
+    base = torch.randn(n_distinct, D, generator=g) * 0.1
+    pick = (torch.arange(E) * 37 + 11) % n_distinct
+    return base[pick].to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("E,k,n_distinct", [(256, 8, 16), (512, 10, 24), (64, 4, 3), (128, 1, 5)])
+def test_exact_ties_take_lowest_ids(E, k, n_distinct):
+    """Exact ties in fp32 probabilities: ids must equal the oracle's (lowest id
+    first) in the single-token layer kernel, the multi-token router kernel and
+    the prefill top-k; no near-tie exclusion applies to exact ties."""
+    D, F = 256, 64
+    cfg = small_cfg(E, k, D, F, zipf=None, sigma=0.1, cfg_id=90 + k)
+    layer = W.make_layer(cfg, 0, DEV)
+    layer["Wr"] = _tied_router(E, D, n_distinct, seed=E + k).to(DEV)
+    layer["bias"] = None
+    x = W.make_tokens(cfg, 5, 0, DEV)
+    ref = oracle.router(x.cpu(), layer["Wr"].cpu(), None, k)
+    # the fixture really has ties inside the top k + 1
+    srt = np.sort(ref["probs32"], axis=1)[:, ::-1]
+    assert (srt[:, :k + 1][:, 1:] == srt[:, :k + 1][:, :-1]).any()
+    router = M.Router(layer["Wr"], None, k)
+    # single token, fused layer kernel
+    for t in range(2):
+        got = gpu_layer(cfg, layer, x[t:t + 1].contiguous())
+        assert np.array_equal(got["idx"].numpy()[0], ref["idx"][t])
+        np.testing.assert_allclose(got["w"].numpy()[0], ref["w"][t], rtol=0, atol=1e-5)
+    # several tokens, router kernel
+    idx = torch.empty(5, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(5, k, device=DEV)
+    ws = M.workspace(M.MOE_OP_ROUTE, 5, k, E, D, F, DEV)
+    M.moe_route(router, x, idx, w, None, ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    # prefill (tensor-core router + warp top-k)
+    T = 5
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    out = dict(y=torch.empty(T, D, device=DEV), idx=torch.empty(T, k, dtype=torch.int32, device=DEV),
+               w=torch.empty(T, k, device=DEV), counts=torch.empty(E, dtype=torch.int32, device=DEV),
+               perm=torch.empty(T * k, dtype=torch.int32, device=DEV))
+    wsp = M.workspace(M.MOE_OP_PREFILL, T, k, E, D, F, DEV)
+    M.moe_prefill(router, experts, x, out["y"], out["idx"], out["w"], out["counts"], out["perm"], wsp)
+    assert M.moe_check_status(wsp) == M.MOE_OK
+    assert np.array_equal(out["idx"].cpu().numpy(), ref["idx"])
