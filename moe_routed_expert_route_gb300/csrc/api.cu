@@ -361,8 +361,8 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     // else the CUDA-core router kernel
     if (x_dtype == MOE_BF16 && router->w_dtype == MOE_BF16 && E % 128 == 0 && D % 64 == 0) {
         GemmParams g = {};
-        if (!make_tmap_2d(&g.tmA, 2, x, D, T, 2ull * D, 64, 128, true) ||
-            !make_tmap_2d(&g.tmB0, 2, router->W, D, E, 2ull * D, 64, 128, true))
+        if (!make_tmap_2d(&g.tmA, 2, x, D, T, 2ull * D, 64, 128, 128) ||
+            !make_tmap_2d(&g.tmB0, 2, router->W, D, E, 2ull * D, 64, 128, 128))
             return MOE_ERR_CUDA;
         g.K = D;
         g.rows_per_ntile = 128;
@@ -394,7 +394,11 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
+    // token tiles of the expert products: 256 positions when experts average
+    // more than 128 tokens, else 128
+    const int nt = (long)T * k > 128L * E ? 256 : 128;
     PermParams pp = {};
+    pp.tile_rows = nt;
     pp.n = T * k;
     pp.k = k;
     pp.E = E;
@@ -425,44 +429,46 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
 
     const int qbits = qbits_of(experts);
     const int cb = qbits == 8 ? 1 : 2;  // codes per byte
+    const unsigned rb = 64 / cb;        // code bytes per row per K stage
     const bool sf16 = experts->s_dtype == MOE_F16;
-    GemmParams g1 = {};
-    if (!make_tmap_2d(&g1.tmA, 1, xp, D, n, 2ull * D, 64, 128, true) ||
-        !make_tmap_2d(&g1.tmB0, 0, experts->gate_q, D / cb, (unsigned long long)E * F, D / cb, 64 / cb, 64, false) ||
-        !make_tmap_2d(&g1.tmB1, 0, experts->up_q, D / cb, (unsigned long long)E * F, D / cb, 64 / cb, 64, false))
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    EgParams g1 = {};
+    if (!make_tmap_2d(&g1.tmX, 1, xp, D, n, 2ull * D, 64, nt, 128) ||
+        !make_tmap_2d(&g1.tmXh, 1, xp, D, n, 2ull * D, 64, nt / 2, 128) ||
+        !make_tmap_2d(&g1.tmW0, 0, experts->gate_q, D / cb, (unsigned long long)E * F, D / cb, rb, 64, rb) ||
+        !make_tmap_2d(&g1.tmW1, 0, experts->up_q, D / cb, (unsigned long long)E * F, D / cb, rb, 64, rb))
         return MOE_ERR_CUDA;
     g1.S0 = experts->gate_s;
     g1.S1 = experts->up_s;
     g1.K = D;
-    g1.b_group_rows = F;
-    g1.rows_per_ntile = 64;
-    g1.half_off = 0;
+    g1.w_rows = F;
+    g1.nwb = F / 64;
     g1.tile_group = pp.tile_group;
     g1.tile_m0 = pp.tile_m0;
     g1.group_end = pp.group_end;
-    g1.n_mtiles_dev = pp.n_mtiles;
-    g1.n_ntiles = F / 64;
+    g1.n_tiles_dev = pp.n_mtiles;
     g1.C = hp;
     g1.ldc = F;
     g1.hdr = hdr;
-    e = launch_gemm(g1, qbits, sf16, true, P.max_mtiles, s);
+    e = launch_egemm(g1, qbits, sf16, true, nt, sms, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    GemmParams g2 = g1;
-    if (!make_tmap_2d(&g2.tmA, 1, hp, F, n, 2ull * F, 64, 128, true) ||
-        !make_tmap_2d(&g2.tmB0, 0, experts->down_q, F / cb, (unsigned long long)E * D, F / cb, 64 / cb, 64, false))
+    EgParams g2 = g1;
+    if (!make_tmap_2d(&g2.tmX, 1, hp, F, n, 2ull * F, 64, nt, 128) ||
+        !make_tmap_2d(&g2.tmXh, 1, hp, F, n, 2ull * F, 64, nt / 2, 128) ||
+        !make_tmap_2d(&g2.tmW0, 0, experts->down_q, F / cb, (unsigned long long)E * D, F / cb, rb, 64, rb))
         return MOE_ERR_CUDA;
-    g2.tmB1 = g2.tmB0;
+    g2.tmW1 = g2.tmW0;
     g2.S0 = experts->down_s;
     g2.S1 = experts->down_s;
     g2.K = F;
-    g2.b_group_rows = D;
-    g2.rows_per_ntile = 128;
-    g2.half_off = 64;
-    g2.n_ntiles = D / 128;
+    g2.w_rows = D;
+    g2.nwb = D / 128;
     g2.C = yp;
     g2.ldc = D;
-    e = launch_gemm(g2, qbits, sf16, false, P.max_mtiles, s);
+    e = launch_egemm(g2, qbits, sf16, false, nt, sms, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     CombineParams cp = {T, D, k, pp.inv, w_buf, static_cast<const float*>(yp), y};

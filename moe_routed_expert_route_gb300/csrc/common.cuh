@@ -58,7 +58,9 @@ __device__ __forceinline__ uint4 ld_cg16(const void* p) {
     return v;
 }
 __device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
-// read-only (non-coherent) load of data no kernel writes during the launch
+// read-only (non-coherent) loads of data no kernel writes during the launch
+template <typename T>
+__device__ __forceinline__ uint4 ld_nc16(const T* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 __device__ __forceinline__ float ldg_nc(const float* p) { return __ldg(p); }
 __device__ __forceinline__ __half ldg_nc(const __half* p) { return __ldg(p); }
 __device__ __forceinline__ int ld_cg_i32(const int* p) { return __ldcg(p); }

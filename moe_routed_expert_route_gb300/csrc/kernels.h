@@ -143,9 +143,30 @@ struct GemmParams {  // aligned like CUtensorMap
     WsHeader* hdr;
 };
 
-// 2-D tensor map over a row-major matrix (dtype 0 = uint8, 1 = fp16, 2 = bf16).
+// Weight-stationary grouped expert projection (prefill): item i = (token tile
+// i / nwb, weight block i % nwb); the A operand is a block of 128 dequantised
+// weight rows, the B operand a tile of up to NT tokens' 16-bit rows.
+struct EgParams {  // aligned like CUtensorMap
+    CUtensorMap tmW0, tmW1;     // codes [rows][row bytes], box {64 or 32 bytes, 64 rows}, swizzled
+                                // across the box's width (64 or 32 bytes)
+    CUtensorMap tmX, tmXh;      // 16-bit B rows [positions][K], box {64, NT} / {64, NT/2}, 128-byte swizzle
+    const void *S0, *S1;        // scales of W0 / W1 rows, [rows][K/32]
+    int K;                      // reduction length
+    int w_rows;                 // weight rows per expert in W0/W1
+    int nwb;                    // weight blocks per expert
+    const int32_t* tile_group;  // [tile] expert
+    const int32_t* tile_m0;     // [tile] first position
+    const int32_t* group_end;   // [expert] end position
+    const int* n_tiles_dev;     // number of tiles
+    void* C;                    // fp16 H [pos][ldc] (SwiGLU) or fp32 Y [pos][ldc]
+    int ldc;
+    WsHeader* hdr;
+};
+
+// 2-D tensor map over a row-major matrix (dtype 0 = uint8, 1 = fp16, 2 = bf16),
+// swizzle 0 (none) or 32, 64, 128 (bytes).
 bool make_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long long inner, unsigned long long rows,
-                  unsigned long long row_bytes, unsigned box_inner, unsigned box_rows, bool swizzle128);
+                  unsigned long long row_bytes, unsigned box_inner, unsigned box_rows, int swizzle);
 
 struct TopkParams {
     int T, E, k, norm_topk;
@@ -160,6 +181,7 @@ constexpr int kPermChunk = 1024;  // assignments per histogram/placement CTA
 
 struct PermParams {
     int n, k, E, nchunk;
+    int tile_rows;              // positions per tile of the tile list
     const int32_t* idx;         // [n] expert of assignment i = t*k + r
     WsHeader* hdr;
     int32_t* chunk_cnt;         // [nchunk][E]
@@ -185,6 +207,7 @@ struct CombineParams {
 };
 
 cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu, int max_mtiles, cudaStream_t s);
+cudaError_t launch_egemm(const EgParams& p, int qbits, bool s_f16, bool swiglu, int nt, int grid, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 cudaError_t launch_gather_f16(const void* x, bool x_bf16, const int32_t* perm_tok, int n, int D, void* Xp,
                               cudaStream_t s);

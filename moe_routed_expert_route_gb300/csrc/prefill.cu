@@ -315,7 +315,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 }
 
 bool make_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long long inner, unsigned long long rows,
-                  unsigned long long row_bytes, unsigned box_inner, unsigned box_rows, bool swizzle128) {
+                  unsigned long long row_bytes, unsigned box_inner, unsigned box_rows, int swizzle) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, rows};
@@ -324,8 +324,10 @@ bool make_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long lon
     cuuint32_t es[2] = {1, 1};
     CUtensorMapDataType dt = dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                             : dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+    CUtensorMapSwizzle sw = swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : swizzle == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                          : swizzle == 32  ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(PermParams p) {
     int cnt = 0;
     if (e < p.E)
         for (int c = 0; c < p.nchunk; c++) cnt += ld_cg_i32(p.chunk_cnt + (size_t)c * p.E + e);
-    const int tiles = (cnt + kGM - 1) / kGM;
+    const int tiles = (cnt + p.tile_rows - 1) / p.tile_rows;
     // block exclusive scan of (cnt, tiles) over e
     int a = cnt, b = tiles;
 #pragma unroll
@@ -465,7 +467,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(PermParams p) {
         }
         for (int i = 0; i < tiles; i++) {
             p.tile_group[toff + i] = e;
-            p.tile_m0[toff + i] = off + i * kGM;
+            p.tile_m0[toff + i] = off + i * p.tile_rows;
         }
         if (e == p.E - 1) {
             p.off[p.E] = off + cnt;
