@@ -52,7 +52,7 @@ Layout layout(int op, int T, int k, int E, int D, int F) {
 
 // Prefill workspace sections.
 struct PLayout {
-    size_t logits, idx, w, xh, chunk_cnt, chunk_base, cnt, off, gend, tgroup, tm0, nmt, perm_tok, inv, hp, yp;
+    size_t logits, idx, w, xh, chunk_cnt, chunk_base, cnt, off, gend, tgroup, tm0, tn, nmt, perm_tok, inv, hp, yp;
     size_t total;
     int nchunk, max_mtiles;
 };
@@ -79,6 +79,7 @@ PLayout prefill_layout(int T, int k, int E, int D, int F) {
     L.gend = take(sizeof(int32_t) * E);
     L.tgroup = take(sizeof(int32_t) * L.max_mtiles);
     L.tm0 = take(sizeof(int32_t) * L.max_mtiles);
+    L.tn = take(sizeof(int32_t) * L.max_mtiles);
     L.nmt = take(sizeof(int));
     L.perm_tok = take(sizeof(int32_t) * n);
     L.inv = take(sizeof(int32_t) * n);
@@ -394,9 +395,7 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    // token tiles of the expert products: 256 positions when experts average
-    // more than 128 tokens, else 128
-    const int nt = (long)T * k > 128L * E ? 256 : 128;
+    const int nt = kEgTile;  // token tile of the expert products
     PermParams pp = {};
     pp.tile_rows = nt;
     pp.n = T * k;
@@ -413,6 +412,7 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     pp.counts_out = counts;
     pp.tile_group = at<int32_t>(workspace, P.tgroup);
     pp.tile_m0 = at<int32_t>(workspace, P.tm0);
+    pp.tile_n = at<int32_t>(workspace, P.tn);
     pp.n_mtiles = at<int>(workspace, P.nmt);
     pp.perm_tok = at<int32_t>(workspace, P.perm_tok);
     pp.perm_out = perm;
@@ -447,12 +447,12 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     g1.nwb = F / 64;
     g1.tile_group = pp.tile_group;
     g1.tile_m0 = pp.tile_m0;
-    g1.group_end = pp.group_end;
+    g1.tile_n = pp.tile_n;
     g1.n_tiles_dev = pp.n_mtiles;
     g1.C = hp;
     g1.ldc = F;
     g1.hdr = hdr;
-    e = launch_egemm(g1, qbits, sf16, true, nt, sms, s);
+    e = launch_egemm(g1, qbits, sf16, true, sms, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     EgParams g2 = g1;
@@ -468,7 +468,7 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     g2.nwb = D / 128;
     g2.C = yp;
     g2.ldc = D;
-    e = launch_egemm(g2, qbits, sf16, false, nt, sms, s);
+    e = launch_egemm(g2, qbits, sf16, false, sms, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     CombineParams cp = {T, D, k, pp.inv, w_buf, static_cast<const float*>(yp), y};

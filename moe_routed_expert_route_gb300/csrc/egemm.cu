@@ -6,13 +6,20 @@
 // activation back, and only routed experts' weights are read. With many tokens
 // per expert these are dense contractions, one per (expert, projection).
 //
-// Work item = (tile of up to NT consecutive grouped positions of one expert,
+// Work item = (tile of up to 128 consecutive grouped positions of one expert,
 // block of 128 weight rows). The weight block is the MMA's A operand (M = 128):
-// its int8/int4 codes arrive by TMA and are dequantised to fp16 in shared
-// memory once per K stage; the tokens' 16-bit rows are the B operand
-// (N = the tile's token count rounded up to 16, at most NT), also by TMA; the
-// fp32 accumulator D[weight row][token] lives in tensor memory, two buffers of
-// NT columns, so that the epilogue of one item overlaps the MMAs of the next.
+// its int8/int4 codes arrive by TMA, are dequantised to fp16 in registers and
+// written to TENSOR MEMORY (tcgen05.st), from where the MMA reads them; the
+// tokens' 16-bit rows are the B operand (N = the tile's token count rounded up
+// to 16), from shared memory by TMA. Keeping A out of shared memory matters:
+// staged through shared memory, every K stage moved ~64-80 KB through it (code
+// tile in and out, A out and in, B in and out) and the shared-memory bandwidth,
+// not the HBM stream or the tensor pipe, set the pace.
+// Tensor memory (512 columns): two fp32 accumulators of 128 columns, so that
+// the epilogue of one item overlaps the MMAs of the next, and a ring of 6 A
+// stages of 32 columns (128 rows x 64 fp16). Each tcgen05 instruction costs
+// the single issuing thread tens of cycles, so the issuer commits once per
+// pair of stages (freeing both stages' A and B slots).
 // The grid is persistent: CTA c takes items c, c + G, ...; consecutive items
 // share their token tile (read from L2) and cover the expert's weight blocks.
 //
@@ -25,27 +32,32 @@
 // Warp roles (15 warps): 0 code producer (TMA, R stages ahead; the code tiles
 // are swizzled across their 64- or 32-byte rows so that the dequantising
 // reads hit all banks), 1 token producer (TMA) and TMEM owner, 2 MMA issuer,
-// 3-10 dequantisation (two threads per A row, each one 32-code scale block of
-// the stage), 11-14 epilogue (TMEM lane quarter = warp % 4). Every wait is
-// bounded; a timeout records MOE_ERR_DEVICE_TIMEOUT and ends the CTA's loops.
+// 3-10 dequantisation (TMEM lane quarter = warp % 4, one A row per thread;
+// warps 3-6 take the even stages, 7-10 the odd ones), 11-14 epilogue (lane
+// quarter = warp % 4). Every wait is bounded; a timeout records
+// MOE_ERR_DEVICE_TIMEOUT and ends the CTA's loops.
+#include <type_traits>
+
 #include "kernels.h"
 #include "tc.cuh"
 
 namespace moe {
 
-constexpr int kEK = 64;          // K per stage: one 128-byte row of 16-bit values
+constexpr int kEK = 64;          // K per stage: 64 16-bit values = 32 TMEM columns
+constexpr int kENT = 128;        // token tile (MMA N at most)
 constexpr int kEThreads = 480;   // 15 warps
 constexpr int kEDeq = 256;       // dequantising threads
+constexpr int kES = 6;           // A stages (tensor memory) = B stages (shared memory); even
+constexpr uint32_t kEAcc = 2 * kENT;  // first TMEM column of the A stages
 
-template <int QB, int NT>
+template <int QB>
 struct EgSmem {
     static constexpr int kRB = QB == 8 ? 64 : 32;        // code bytes per row per stage
     static constexpr int kRaw = 128 * kRB;               // one code stage
-    static constexpr int kS = NT == 256 ? 3 : 4;         // A/B stages
-    static constexpr int kR = NT == 256 ? (QB == 8 ? 8 : 12) : (QB == 8 ? 10 : 16);  // code stages
-    static constexpr int kA = 128 * 128;                 // 128 rows x 64 fp16
-    static constexpr int kB = NT * 128;                  // NT rows x 64 fp16
-    static constexpr size_t kBytes = (size_t)kS * (kA + kB) + (size_t)kR * kRaw + 1024;
+    static constexpr int kSB = kES;                      // token (B) stages
+    static constexpr int kR = QB == 8 ? 12 : 20;         // code stages
+    static constexpr int kB = kENT * 128;                // 128 rows x 64 fp16
+    static constexpr size_t kBytes = (size_t)kSB * kB + (size_t)kR * kRaw + 1024;
 };
 
 // 8 int8 codes -> 8 fp16 values q*s (exact q, one rounding of the product).
@@ -114,31 +126,32 @@ __device__ __forceinline__ uint4 deq8_i4(uint32_t w, float s) {
 struct EgItem {
     int e, wb, m0, n;  // expert, weight block, first position, positions (1..NT)
 };
-template <int NT>
-__device__ __forceinline__ EgItem eg_item(const EgParams& p, int i) {
+__device__ __forceinline__ EgItem eg_item_load(const EgParams& p, int i) {
     EgItem it;
     const int ti = i / p.nwb;
     it.wb = i - ti * p.nwb;
     it.e = ld_cg_i32(p.tile_group + ti);
     it.m0 = ld_cg_i32(p.tile_m0 + ti);
-    const int end = ld_cg_i32(p.group_end + it.e);
-    it.n = min(NT, end - it.m0);
+    it.n = ld_cg_i32(p.tile_n + ti);
     return it;
 }
+constexpr int kEgItems = 256;  // items of one CTA kept in shared memory
 
-template <int QB, typename ST, int NT, bool SWIGLU>
+template <int QB, typename ST, bool SWIGLU>
 __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_constant__ EgParams p) {
-    using L = EgSmem<QB, NT>;
-    constexpr int R = L::kR, S = L::kS;
+    using L = EgSmem<QB>;
+    constexpr int R = L::kR, S = kES, NT = kENT;
     extern __shared__ unsigned char sm_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* sa = sm;                                   // [S][A 16 KB]
-    unsigned char* sb = sm + (size_t)S * L::kA;               // [S][B NT*128 B]
+    unsigned char* sb = sm;                                   // [S][B 16 KB]
     unsigned char* raw = sb + (size_t)S * L::kB;              // [R][128 rows][kRB]
-    __shared__ __align__(8) uint64_t raw_full[R], raw_empty[R], a_full[S], b_full[S], ab_empty[S];
+    // ab_empty[s/2]: both A and B slots of stages s and s+1 (s even) free again;
+    // the MMA issuer commits once per pair of stages
+    __shared__ __align__(8) uint64_t raw_full[R], raw_empty[R], a_full[S], b_full[S], ab_empty[S / 2];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
+    __shared__ EgItem s_items[kEgItems];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int* status = &p.hdr->status;
@@ -149,13 +162,13 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
         s_abort = 0;
         for (int i = 0; i < R; i++) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kEDeq);
+            mbar_init(&raw_empty[i], kEDeq / 2);  // one group of dequantising warps per stage
         }
         for (int i = 0; i < S; i++) {
-            mbar_init(&a_full[i], kEDeq);
+            mbar_init(&a_full[i], kEDeq / 2);
             mbar_init(&b_full[i], 1);
-            mbar_init(&ab_empty[i], 1);
         }
+        for (int i = 0; i < S / 2; i++) mbar_init(&ab_empty[i], 1);
         for (int i = 0; i < 2; i++) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 128);
@@ -163,7 +176,7 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(&s_tmem, 2 * NT);
+        tmem_alloc(&s_tmem, 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -174,13 +187,25 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
     pdl_wait();
     pdl_trigger();
     const int n_items = ld_cg_i32(p.n_tiles_dev) * p.nwb;
+    // this CTA's items c, c + G, ... : the first kEgItems decoded once into
+    // shared memory (all loads in flight together), later ones on the fly
+    if (warp == 3)
+        for (int li = lane; li < kEgItems; li += 32) {
+            const int i = blockIdx.x + li * G;
+            if (i < n_items) s_items[li] = eg_item_load(p, i);
+        }
+    __syncthreads();
+    auto eg_item = [&](int i) -> EgItem {
+        const int li = (i - (int)blockIdx.x) / G;
+        return li < kEgItems ? s_items[li] : eg_item_load(p, i);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ code producer
         if (lane == 0) {
             int kt = 0;
             for (int i = blockIdx.x; i < n_items && !s_abort; i += G) {
-                const EgItem it = eg_item<NT>(p, i);
+                const EgItem it = eg_item(i);
                 const int row0 = it.e * p.w_rows + it.wb * (SWIGLU ? 64 : 128);
                 const int row1 = SWIGLU ? row0 : row0 + 64;
                 for (int t = 0; t < nk; t++, kt++) {
@@ -201,14 +226,14 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
         if (lane == 0) {
             int kt = 0;
             for (int i = blockIdx.x; i < n_items && !s_abort; i += G) {
-                const EgItem it = eg_item<NT>(p, i);
+                const EgItem it = eg_item(i);
+                const bool half = it.n <= NT / 2;  // the MMA reads only N <= NT/2 rows then
                 for (int t = 0; t < nk; t++, kt++) {
                     const int s = kt % S;
-                    if (kt >= S && !mbar_wait(&ab_empty[s], ((kt / S) - 1) & 1, status)) {
+                    if (kt >= S && !mbar_wait(&ab_empty[s >> 1], ((kt / S) - 1) & 1, status)) {
                         s_abort = 1;
                         break;
                     }
-                    const bool half = it.n <= NT / 2;  // the MMA reads only N <= NT/2 rows then
                     mbar_arrive_expect_tx(&b_full[s], half ? L::kB / 2 : L::kB);
                     tma_load_2d(sb + (size_t)s * L::kB, half ? &p.tmXh : &p.tmX, t * kEK, it.m0, &b_full[s]);
                 }
@@ -219,7 +244,7 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
         if (lane == 0) {
             int kt = 0, li = 0;
             for (int i = blockIdx.x; i < n_items && !s_abort; i += G, li++) {
-                const EgItem it = eg_item<NT>(p, i);
+                const EgItem it = eg_item(i);
                 const int buf = li & 1;
                 if (li >= 2 && !mbar_wait(&acc_empty[buf], ((li >> 1) - 1) & 1, status)) {
                     s_abort = 1;
@@ -231,117 +256,116 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
                 const uint32_t d = tmem + (uint32_t)(buf * NT);
                 for (int t = 0; t < nk; t++, kt++) {
                     const int s = kt % S;
-                    const unsigned ph = (kt / S) & 1;
-                    if (s_abort || !mbar_wait(&a_full[s], ph, status) || !mbar_wait(&b_full[s], ph, status)) {
+                    if (s_abort || !mbar_wait(&a_full[s], (kt / S) & 1, status) ||
+                        !mbar_wait(&b_full[s], (kt / S) & 1, status)) {
                         s_abort = 1;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = umma_desc_sw128(smem_addr(sa + (size_t)s * L::kA));
+                    const uint32_t at = tmem + kEAcc + (uint32_t)(32 * s);
                     const uint64_t bd = umma_desc_sw128(smem_addr(sb + (size_t)s * L::kB));
 #pragma unroll
                     for (int kk = 0; kk < kEK / 16; kk++)
-                        umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (t | kk) != 0 ? 1u : 0u);
-                    umma_commit(&ab_empty[s]);
+                        umma_f16_ts(d, at + 8 * kk, bd + 2 * kk, idesc, (t | kk) != 0 ? 1u : 0u);
+                    if (s & 1) umma_commit(&ab_empty[s >> 1]);  // frees stages s-1 and s
                 }
                 umma_commit(&acc_full[buf]);  // also after an abort: completes when the issued MMAs are done
             }
         }
     } else if (warp >= 3 && warp <= 10) {
         // ------------------------------------------------ dequantisation
-        const int j = tid - 96;                                   // 0 .. 255
-        const int row = j >> 1, h = j & 1;                        // A row; 32-code half of the stage
+        // two groups of four warps take alternate stages, so that one stage's
+        // latency (waits, loads, conversion, TMEM store) overlaps the other's
+        const int q = warp & 3;                                   // TMEM lane quarter
+        const int row = 32 * q + lane;                            // A row = TMEM lane
+        const int grp = (warp - 3) >> 2;                          // stages kt with kt % 2 == grp
         const int rr = SWIGLU ? ((row & 1) * 64 + (row >> 1)) : row;  // its code row in a stage
         // 16-byte chunk c of code row r sits at chunk c ^ swz(r) (TMA swizzle)
         const int swz = QB == 8 ? ((rr >> 1) & 3) : ((rr >> 2) & 1);
-        const int nsb = p.K / kBlk;                               // scales per weight row
-        constexpr int SPV = 16 / (int)sizeof(ST);                 // scales per 16-byte vector
-        constexpr int TPV = SPV / 2;                              // stages per vector
-        const bool vec = (nsb * (int)sizeof(ST)) % 16 == 0;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + kEAcc;
+        const int nsb = p.K / kBlk;                               // scales per weight row (2 per stage)
         int kt = 0;
         for (int i = blockIdx.x; i < n_items && !s_abort; i += G) {
-            const EgItem it = eg_item<NT>(p, i);
+            const EgItem it = eg_item(i);
             const int wrow = it.e * p.w_rows + (SWIGLU ? it.wb * 64 + (row >> 1) : it.wb * 128 + row);
             const ST* srow = reinterpret_cast<const ST*>(SWIGLU && (row & 1) ? p.S1 : p.S0) + (size_t)wrow * nsb;
-            // this thread's scale (block 2t + h) per stage: from 16-byte vectors
-            // loaded two ahead, or one value loaded one stage ahead
-            uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0;
-            const int nvec = (nsb + SPV - 1) / SPV;
-            float snext = 0.f;
-            if (vec) {
-                v0 = ld_nc16(srow);
-                if (nvec > 1) v1 = ld_nc16(srow + SPV);
-                if (nvec > 2) v2 = ld_nc16(srow + 2 * SPV);
-            } else {
-                snext = to_f32(srow[h]);
-            }
+            // the two scales of stage t as one 4-byte (fp16) or 8-byte (fp32) load
+            using SP = typename std::conditional<sizeof(ST) == 2, uint32_t, uint2>::type;
+            auto ld_sp = [&](int t) -> SP { return __ldg(reinterpret_cast<const SP*>(srow + 2 * t)); };
+            // this group's first two stages of the item, loaded ahead
+            int t0 = ((kt & 1) == grp) ? 0 : 1;
+            SP sq0 = {}, sq1 = {};
+            if (t0 < nk) sq0 = ld_sp(t0);
+            if (t0 + 2 < nk) sq1 = ld_sp(t0 + 2);
             for (int t = 0; t < nk; t++, kt++) {
+                if ((kt & 1) != grp) continue;
                 const int rs = kt % R, as = kt % S;
                 if (s_abort || !mbar_wait(&raw_full[rs], (kt / R) & 1, status) ||
-                    (kt >= S && !mbar_wait(&ab_empty[as], ((kt / S) - 1) & 1, status))) {
+                    (kt >= S && !mbar_wait(&ab_empty[as >> 1], ((kt / S) - 1) & 1, status))) {
                     s_abort = 1;
                     break;
                 }
-                float sc;
-                if (vec) {
-                    if (t > 0 && t % TPV == 0) {
-                        v0 = v1;
-                        v1 = v2;
-                        const int vn = t / TPV + 2;
-                        if (vn < nvec) v2 = ld_nc16(srow + vn * SPV);
-                    }
-                    const int q = t % TPV;
-                    if constexpr (sizeof(ST) == 2) {
-                        const uint32_t w2 = q == 0 ? v0.x : q == 1 ? v0.y : q == 2 ? v0.z : v0.w;
-                        sc = __half2float(__ushort_as_half((unsigned short)(h ? (w2 >> 16) : (w2 & 0xFFFFu))));
-                    } else {
-                        const uint32_t w2 = q == 0 ? (h ? v0.y : v0.x) : (h ? v0.w : v0.z);
-                        sc = __uint_as_float(w2);
-                    }
+                tc_fence_after();
+                const SP sp = sq0;
+                sq0 = sq1;
+                if (t + 4 < nk) sq1 = ld_sp(t + 4);
+                float s0, s1;
+                if constexpr (sizeof(ST) == 2) {
+                    s0 = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
+                    s1 = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
                 } else {
-                    sc = snext;
-                    if (t + 1 < nk) snext = to_f32(srow[2 * t + 2 + h]);
+                    s0 = __uint_as_float(sp.x);
+                    s1 = __uint_as_float(sp.y);
                 }
                 const unsigned char* rp = raw + (size_t)rs * L::kRaw + rr * L::kRB;
-                unsigned char* at = sa + (size_t)as * L::kA;
-                uint4 c0, c1;
+                uint32_t cols[32];
                 if constexpr (QB == 8) {
-                    c0 = *reinterpret_cast<const uint4*>(rp + 16 * ((2 * h) ^ swz));
-                    c1 = *reinterpret_cast<const uint4*>(rp + 16 * ((2 * h + 1) ^ swz));
-                } else {
-                    c0 = *reinterpret_cast<const uint4*>(rp + 16 * (h ^ swz));
-                }
-                uint4 o[4];
-                if constexpr (sizeof(ST) == 2) {
-                    const __half2 s2 = __float2half2_rn(sc);  // exact: sc is an fp16 value
-                    if constexpr (QB == 8) {
-                        o[0] = deq8_i8(make_uint2(c0.x, c0.y), s2);
-                        o[1] = deq8_i8(make_uint2(c0.z, c0.w), s2);
-                        o[2] = deq8_i8(make_uint2(c1.x, c1.y), s2);
-                        o[3] = deq8_i8(make_uint2(c1.z, c1.w), s2);
-                    } else {
-                        o[0] = deq8_i4(c0.x, s2);
-                        o[1] = deq8_i4(c0.y, s2);
-                        o[2] = deq8_i4(c0.z, s2);
-                        o[3] = deq8_i4(c0.w, s2);
-                    }
-                } else {
-                    if constexpr (QB == 8) {
-                        o[0] = deq8_i8(make_uint2(c0.x, c0.y), sc);
-                        o[1] = deq8_i8(make_uint2(c0.z, c0.w), sc);
-                        o[2] = deq8_i8(make_uint2(c1.x, c1.y), sc);
-                        o[3] = deq8_i8(make_uint2(c1.z, c1.w), sc);
-                    } else {
-                        o[0] = deq8_i4(c0.x, sc);
-                        o[1] = deq8_i4(c0.y, sc);
-                        o[2] = deq8_i4(c0.z, sc);
-                        o[3] = deq8_i4(c0.w, sc);
-                    }
-                }
+                    uint4 c[4];
 #pragma unroll
-                for (int c = 0; c < 4; c++) *reinterpret_cast<uint4*>(at + sw128_off(row, 4 * h + c)) = o[c];
-                fence_proxy_async_smem();
-                mbar_arrive(&raw_empty[rs]);
+                    for (int cc = 0; cc < 4; cc++) c[cc] = *reinterpret_cast<const uint4*>(rp + 16 * (cc ^ swz));
+                    mbar_arrive(&raw_empty[rs]);  // the code tile is read
+#pragma unroll
+                    for (int cc = 0; cc < 4; cc++) {
+                        uint4 o0, o1;
+                        if constexpr (sizeof(ST) == 2) {
+                            const __half2 s2 = __float2half2_rn(cc < 2 ? s0 : s1);  // exact: fp16 values
+                            o0 = deq8_i8(make_uint2(c[cc].x, c[cc].y), s2);
+                            o1 = deq8_i8(make_uint2(c[cc].z, c[cc].w), s2);
+                        } else {
+                            o0 = deq8_i8(make_uint2(c[cc].x, c[cc].y), cc < 2 ? s0 : s1);
+                            o1 = deq8_i8(make_uint2(c[cc].z, c[cc].w), cc < 2 ? s0 : s1);
+                        }
+                        cols[8 * cc] = o0.x; cols[8 * cc + 1] = o0.y; cols[8 * cc + 2] = o0.z; cols[8 * cc + 3] = o0.w;
+                        cols[8 * cc + 4] = o1.x; cols[8 * cc + 5] = o1.y; cols[8 * cc + 6] = o1.z; cols[8 * cc + 7] = o1.w;
+                    }
+                } else {
+                    uint4 c[2];
+#pragma unroll
+                    for (int cc = 0; cc < 2; cc++) c[cc] = *reinterpret_cast<const uint4*>(rp + 16 * (cc ^ swz));
+                    mbar_arrive(&raw_empty[rs]);
+#pragma unroll
+                    for (int cc = 0; cc < 2; cc++) {
+                        const uint32_t w4[4] = {c[cc].x, c[cc].y, c[cc].z, c[cc].w};
+#pragma unroll
+                        for (int wq = 0; wq < 4; wq++) {
+                            uint4 o;
+                            if constexpr (sizeof(ST) == 2) o = deq8_i4(w4[wq], __float2half2_rn(cc ? s1 : s0));
+                            else o = deq8_i4(w4[wq], cc ? s1 : s0);
+                            cols[16 * cc + 4 * wq] = o.x; cols[16 * cc + 4 * wq + 1] = o.y;
+                            cols[16 * cc + 4 * wq + 2] = o.z; cols[16 * cc + 4 * wq + 3] = o.w;
+                        }
+                    }
+                }
+                uint32_t lo[16], hi[16];
+#pragma unroll
+                for (int c2 = 0; c2 < 16; c2++) {
+                    lo[c2] = cols[c2];
+                    hi[c2] = cols[16 + c2];
+                }
+                tmem_st16(tq + (uint32_t)(32 * as), lo);
+                tmem_st16(tq + (uint32_t)(32 * as + 16), hi);
+                tmem_st_wait();
+                tc_fence_before();
                 mbar_arrive(&a_full[as]);
             }
         }
@@ -351,7 +375,7 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
         const int j = 32 * q + lane;          // A row = TMEM lane
         int li = 0;
         for (int i = blockIdx.x; i < n_items && !s_abort; i += G, li++) {
-            const EgItem it = eg_item<NT>(p, i);
+            const EgItem it = eg_item(i);
             const int buf = li & 1;
             if (!mbar_wait(&acc_full[buf], (li >> 1) & 1, status)) {
                 s_abort = 1;
@@ -395,31 +419,21 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, 2 * NT);
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int QB, typename ST, int NT, bool SWIGLU>
+template <int QB, typename ST, bool SWIGLU>
 static cudaError_t launch_egemm_t(const EgParams& p, int grid, cudaStream_t s) {
-    return launch(egemm_kernel<QB, ST, NT, SWIGLU>, dim3(grid), dim3(kEThreads), EgSmem<QB, NT>::kBytes, s, true, p);
+    return launch(egemm_kernel<QB, ST, SWIGLU>, dim3(grid), dim3(kEThreads), EgSmem<QB>::kBytes, s, true, p);
 }
 
-template <int NT>
-static cudaError_t launch_egemm_nt(const EgParams& p, int qbits, bool s_f16, bool swiglu, int grid, cudaStream_t s) {
+cudaError_t launch_egemm(const EgParams& p, int qbits, bool s_f16, bool swiglu, int grid, cudaStream_t s) {
     if (qbits == 8) {
-        if (swiglu) return s_f16 ? launch_egemm_t<8, __half, NT, true>(p, grid, s)
-                                 : launch_egemm_t<8, float, NT, true>(p, grid, s);
-        return s_f16 ? launch_egemm_t<8, __half, NT, false>(p, grid, s)
-                     : launch_egemm_t<8, float, NT, false>(p, grid, s);
+        if (swiglu) return s_f16 ? launch_egemm_t<8, __half, true>(p, grid, s) : launch_egemm_t<8, float, true>(p, grid, s);
+        return s_f16 ? launch_egemm_t<8, __half, false>(p, grid, s) : launch_egemm_t<8, float, false>(p, grid, s);
     }
-    if (swiglu) return s_f16 ? launch_egemm_t<4, __half, NT, true>(p, grid, s)
-                             : launch_egemm_t<4, float, NT, true>(p, grid, s);
-    return s_f16 ? launch_egemm_t<4, __half, NT, false>(p, grid, s)
-                 : launch_egemm_t<4, float, NT, false>(p, grid, s);
-}
-
-cudaError_t launch_egemm(const EgParams& p, int qbits, bool s_f16, bool swiglu, int nt, int grid, cudaStream_t s) {
-    return nt == 256 ? launch_egemm_nt<256>(p, qbits, s_f16, swiglu, grid, s)
-                     : launch_egemm_nt<128>(p, qbits, s_f16, swiglu, grid, s);
+    if (swiglu) return s_f16 ? launch_egemm_t<4, __half, true>(p, grid, s) : launch_egemm_t<4, float, true>(p, grid, s);
+    return s_f16 ? launch_egemm_t<4, __half, false>(p, grid, s) : launch_egemm_t<4, float, false>(p, grid, s);
 }
 
 }  // namespace moe

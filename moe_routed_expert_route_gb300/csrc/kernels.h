@@ -149,14 +149,14 @@ struct GemmParams {  // aligned like CUtensorMap
 struct EgParams {  // aligned like CUtensorMap
     CUtensorMap tmW0, tmW1;     // codes [rows][row bytes], box {64 or 32 bytes, 64 rows}, swizzled
                                 // across the box's width (64 or 32 bytes)
-    CUtensorMap tmX, tmXh;      // 16-bit B rows [positions][K], box {64, NT} / {64, NT/2}, 128-byte swizzle
+    CUtensorMap tmX, tmXh;      // 16-bit B rows [positions][K], box {64, 128} / {64, 64}, 128-byte swizzle
     const void *S0, *S1;        // scales of W0 / W1 rows, [rows][K/32]
     int K;                      // reduction length
     int w_rows;                 // weight rows per expert in W0/W1
     int nwb;                    // weight blocks per expert
     const int32_t* tile_group;  // [tile] expert
     const int32_t* tile_m0;     // [tile] first position
-    const int32_t* group_end;   // [expert] end position
+    const int32_t* tile_n;      // [tile] positions in the tile
     const int* n_tiles_dev;     // number of tiles
     void* C;                    // fp16 H [pos][ldc] (SwiGLU) or fp32 Y [pos][ldc]
     int ldc;
@@ -192,6 +192,7 @@ struct PermParams {
     int32_t* counts_out;        // [E] or null
     int32_t* tile_group;        // [n/128 + E]
     int32_t* tile_m0;
+    int32_t* tile_n;            // positions per tile (or null)
     int* n_mtiles;
     int32_t* perm_tok;          // [n] position -> token
     int32_t* perm_out;          // [n] position -> assignment id, or null
@@ -207,7 +208,8 @@ struct CombineParams {
 };
 
 cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu, int max_mtiles, cudaStream_t s);
-cudaError_t launch_egemm(const EgParams& p, int qbits, bool s_f16, bool swiglu, int nt, int grid, cudaStream_t s);
+cudaError_t launch_egemm(const EgParams& p, int qbits, bool s_f16, bool swiglu, int grid, cudaStream_t s);
+constexpr int kEgTile = 128;  // token tile of the expert products
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 cudaError_t launch_gather_f16(const void* x, bool x_bf16, const int32_t* perm_tok, int n, int D, void* Xp,
                               cudaStream_t s);

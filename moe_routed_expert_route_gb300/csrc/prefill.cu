@@ -468,6 +468,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(PermParams p) {
         for (int i = 0; i < tiles; i++) {
             p.tile_group[toff + i] = e;
             p.tile_m0[toff + i] = off + i * p.tile_rows;
+            if (p.tile_n) p.tile_n[toff + i] = min(p.tile_rows, cnt - i * p.tile_rows);
         }
         if (e == p.E - 1) {
             p.off[p.E] = off + cnt;
