@@ -4,9 +4,9 @@ Default workload: decode of one token through 40 stacked independent MoE layers
 of 256 experts, top-8, d_model 2048, d_ff 768 (Qwen3.6-35B-A3B-shaped), int8
 symmetric per-block-32 weights with fp16 scales, bf16 activations, Zipf(1.1)
 router bias. One step = router GEMV + fp32 softmax + top-k + gathered gate/up +
-SwiGLU + per-slot down + weighted combine + residual, for all 40 layers. Each
-step decodes the next token of a device-resident bank of 64 distinct seeded
-tokens (data="synthetic").
+SwiGLU + per-slot down + weighted combine + residual, for all 40 layers. The
+layers are independent: in each step every layer takes its own token, drawn
+from a device-resident bank of distinct seeded tokens (data="synthetic").
 
 Prints ONE JSON line (rank 0). With --impl reference the CPU oracle is timed on
 a bounded sample of the same workload instead.
@@ -102,7 +102,7 @@ class ClockSampler:
 # ------------------------------------------------------------------ decode
 
 class DecodeStack:
-    """40 layers resident in HBM, one token per step, residual chain."""
+    """40 layers resident in HBM; per step every layer decodes its own token."""
 
     def __init__(self, cfg: W.LayerConfig, dev, T: int = 1, layers: int = None):
         import moe_routed_expert_route_gb300 as M
@@ -114,29 +114,39 @@ class DecodeStack:
         self.layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(self.L)]
         self.routers = [M.Router(lw["Wr"], lw["bias"], cfg.k) for lw in self.layers]
         self.experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in self.layers]
-        D = cfg.D
-        self.X = [torch.empty(T, D, dtype=cfg.x_dtype, device=dev) for _ in range(self.L + 1)]
-        self.X[0].copy_(W.make_tokens(cfg, T, 0, dev))
-        self.idx = [torch.empty(T, cfg.k, dtype=torch.int32, device=dev) for _ in range(self.L)]
-        self.w = [torch.empty(T, cfg.k, dtype=torch.float32, device=dev) for _ in range(self.L)]
-        self.y = [torch.empty(T, D, dtype=torch.float32, device=dev) for _ in range(self.L)]
-        self.ws = M.workspace(M.MOE_OP_LAYER, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
-        # a bank of distinct tokens on the device: step i decodes token i mod NB,
-        # so every step routes a new token and nothing drifts from step to step
-        self.NB = 64
-        self.bank = W.make_tokens(cfg, T * self.NB, 1, dev).reshape(self.NB, T, D)
-        self.ctr = torch.zeros(1, dtype=torch.long, device=dev)
+        self._buffers(T)
         self.graph = self.graph_e2e = None
         torch.cuda.synchronize()  # setup ran on the default stream; the steps run on another
+
+    def _buffers(self, T):
+        """Per-step buffers for T tokens. The layers are independent (each has
+        its own weights): layer l of a step takes its own token batch, drawn
+        from a bank of distinct synthetic tokens on the device, and writes
+        x_next = x + y. (Feeding x_next of one layer into the next, without the
+        normalisation a real model applies between layers, lets the residual
+        stream of some tokens grow without bound through 40 random layers.)"""
+        cfg, dev, M, L, D = self.cfg, self.dev, self.M, self.L, self.cfg.D
+        self.T = T
+        self.XIN = torch.empty(L, T, D, dtype=cfg.x_dtype, device=dev)
+        self.XN = torch.empty(L, T, D, dtype=cfg.x_dtype, device=dev)
+        self.idx = [torch.empty(T, cfg.k, dtype=torch.int32, device=dev) for _ in range(L)]
+        self.w = [torch.empty(T, cfg.k, dtype=torch.float32, device=dev) for _ in range(L)]
+        self.y = [torch.empty(T, D, dtype=torch.float32, device=dev) for _ in range(L)]
+        self.ws = M.workspace(M.MOE_OP_LAYER, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
+        # step i uses bank entry i mod NB: every step routes new tokens
+        self.NB = 16 if T > 8 else 64
+        self.bank = W.make_tokens(cfg, self.NB * L * T, 1, dev).reshape(self.NB, L, T, D)
+        self.XIN.copy_(self.bank[0])
+        self.ctr = torch.zeros(1, dtype=torch.long, device=dev)
 
     def forward(self, from_bank: bool = True):
         M = self.M
         if from_bank:
-            torch.index_select(self.bank, 0, self.ctr, out=self.X[0].view(1, self.T, -1))
+            torch.index_select(self.bank, 0, self.ctr, out=self.XIN.view(1, self.L, self.T, -1))
             self.ctr.add_(1).remainder_(self.NB)
         for l in range(self.L):
-            M.moe_layer(self.routers[l], self.experts[l], self.X[l], self.idx[l], self.w[l], None,
-                        self.y[l], self.X[l + 1], self.ws)
+            M.moe_layer(self.routers[l], self.experts[l], self.XIN[l], self.idx[l], self.w[l], None,
+                        self.y[l], self.XN[l], self.ws)
 
     def capture(self, stream):
         with torch.cuda.stream(stream):
@@ -146,7 +156,7 @@ class DecodeStack:
         with torch.cuda.graph(g, stream=stream):
             self.forward()
         self.graph = g
-        g2 = torch.cuda.CUDAGraph()  # the same layers without the bank: input comes from the host
+        g2 = torch.cuda.CUDAGraph()  # the same layers without the bank: inputs come from the host
         with torch.cuda.graph(g2, stream=stream):
             self.forward(from_bank=False)
         self.graph_e2e = g2
@@ -190,16 +200,17 @@ def time_graph(stack, stream, steps, warmup, world):
 
 
 def time_e2e(stack, stream, steps, warmup):
-    """Host buffers: pinned x in, last layer's output back to the host, per step."""
-    T, D = stack.T, stack.cfg.D
-    n = max(1, min(steps, 256))
-    xin = W.make_tokens(stack.cfg, T * n, 5, "cpu").reshape(n, T, D).pin_memory()
+    """Host buffers: each step's layer inputs copied in from pinned host memory,
+    the last layer's x_next read back to the host."""
+    T, D, L = stack.T, stack.cfg.D, stack.L
+    n = max(1, min(steps, 16))
+    xin = W.make_tokens(stack.cfg, n * L * T, 5, "cpu").reshape(n, L, T, D).pin_memory()
     xout = torch.empty(n, T, D, dtype=stack.cfg.x_dtype).pin_memory()
 
     def one(i):
-        stack.X[0].copy_(xin[i % n], non_blocking=True)
+        stack.XIN.copy_(xin[i % n], non_blocking=True)
         stack.graph_e2e.replay()
-        xout[i % n].copy_(stack.X[stack.L], non_blocking=True)
+        xout[i % n].copy_(stack.XN[L - 1], non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     with torch.cuda.stream(stream):
@@ -222,20 +233,17 @@ def cpu_baseline_decode(stack, budget_s=15.0):
     cfg = stack.cfg
     nth = os.cpu_count() or 1
     host = [(lw["Wr"].cpu(), lw["bias"].cpu() if lw["bias"] is not None else None) for lw in stack.layers]
-    x = W.make_tokens(cfg, stack.T, 9, "cpu").double().numpy()
+    xs = W.make_tokens(cfg, stack.T * stack.L, 9, "cpu").double().numpy().reshape(stack.L, stack.T, -1)
     tokens = 0
     t0 = time.perf_counter()
     while True:
-        xl = x
-        for l in range(stack.L):
-            r = oracle.router(xl, host[l][0], host[l][1], cfg.k)
-            y = oracle.moe(stack.layers[l], xl, r["idx"], r["w"], cfg.qbits, nthreads=nth)
-            xl = torch.from_numpy(xl + y).to(torch.bfloat16).double().numpy()
+        for l in range(stack.L):  # independent layers, each with its own token batch
+            r = oracle.router(xs[l], host[l][0], host[l][1], cfg.k)
+            oracle.moe(stack.layers[l], xs[l], r["idx"], r["w"], cfg.qbits, nthreads=nth)
         tokens += stack.T
         el = time.perf_counter() - t0
         if el >= budget_s or tokens >= 64:
             break
-        x = xl
     return tokens / el, nth, f"{tokens} token(s) x {stack.L} layers (router + routed experts), {el:.1f} s"
 
 
@@ -287,6 +295,7 @@ def run_ours(args):
                    "routed_gbs": round(routed / (ms_step * 1e-3) / 1e9, 1),
                    "l2": f"no flush: {routed / 1e9:.2f} GB of distinct weights per step > "
                          f"{L2_BYTES / 2**20:.0f} MiB L2",
+                   "inputs": "independent layers: each layer decodes its own bank token every step",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "graph": "one CUDA graph per step, programmatic dependent launch between kernels"},
         "roofline": {"bound": "hbm", "kernel": "fused_layer_kernel (one launch = one whole layer)",
@@ -337,18 +346,7 @@ def run_batched(args, dev):
         if stack is None:
             stack = DecodeStack(cfg, dev, T=T, layers=args.layers)
         else:  # same weights, new token batch
-            old = stack
-            stack = DecodeStack.__new__(DecodeStack)
-            stack.__dict__.update(old.__dict__)
-            stack.T = T
-            stack.X = [torch.empty(T, cfg.D, dtype=cfg.x_dtype, device=dev) for _ in range(old.L + 1)]
-            stack.X[0].copy_(W.make_tokens(cfg, T, 0, dev))
-            stack.idx = [torch.empty(T, cfg.k, dtype=torch.int32, device=dev) for _ in range(old.L)]
-            stack.w = [torch.empty(T, cfg.k, dtype=torch.float32, device=dev) for _ in range(old.L)]
-            stack.y = [torch.empty(T, cfg.D, dtype=torch.float32, device=dev) for _ in range(old.L)]
-            stack.ws = stack.M.workspace(stack.M.MOE_OP_LAYER, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
-            stack.bank = W.make_tokens(cfg, T * stack.NB, 1, dev).reshape(stack.NB, T, cfg.D)
-            stack.ctr = torch.zeros(1, dtype=torch.long, device=dev)
+            stack._buffers(T)
             torch.cuda.synchronize()
         stream = torch.cuda.Stream(dev)
         stack.capture(stream)
@@ -358,7 +356,8 @@ def run_batched(args, dev):
         out.append({"T": T, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
                     "union_experts_mean": round(sum(U) / len(U), 2), "union_min": min(U), "union_max": max(U),
                     "routed_gbs": round(routed / (ms * 1e-3) / 1e9, 1)})
-        assert stack.M.moe_check_status(stack.ws) == 0
+        st = stack.M.moe_check_status(stack.ws)
+        assert st == 0, f"T={T}: device status {st} ({stack.M.status_string(st)})"
     return {"workload": "batched decode sweep, 40 layers E=256 top-8 D=2048 F=768 int8", "points": out}
 
 
@@ -373,8 +372,9 @@ def run_substitution(args, dev):
     res = []
     for T in (1, 16):
         k = cfg.k
-        X = [torch.empty(T, cfg.D, dtype=cfg.x_dtype, device=dev) for _ in range(L + 1)]
-        X[0].copy_(W.make_tokens(cfg, T, 0, dev))
+        # independent layers: each takes its own token batch from a device bank
+        XIN = torch.empty(L, T, cfg.D, dtype=cfg.x_dtype, device=dev)
+        XN = torch.empty(L, T, cfg.D, dtype=cfg.x_dtype, device=dev)
         bufs = [dict(idx=torch.empty(T, k, dtype=torch.int32, device=dev), w=torch.empty(T, k, device=dev),
                      probs=torch.empty(T, cfg.E, device=dev), idx2=torch.empty(T, k, dtype=torch.int32, device=dev),
                      w2=torch.empty(T, k, device=dev), flag=torch.empty(T, k, dtype=torch.uint8, device=dev),
@@ -383,20 +383,20 @@ def run_substitution(args, dev):
         ws_d = M.workspace(M.MOE_OP_DECODE, T, k, cfg.E, cfg.D, cfg.F, dev)
         routers = [M.Router(lw["Wr"], lw["bias"], k) for lw in layers]
         experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
-        NB = 64
-        bank = W.make_tokens(cfg, T * NB, 1, dev).reshape(NB, T, cfg.D)
+        NB = 16 if T > 8 else 64
+        bank = W.make_tokens(cfg, NB * L * T, 1, dev).reshape(NB, L, T, cfg.D)
         ctr = torch.zeros(1, dtype=torch.long, device=dev)
         torch.cuda.synchronize()  # setup ran on the default stream; the steps run on another
 
         def step():
-            torch.index_select(bank, 0, ctr, out=X[0].view(1, T, -1))
+            torch.index_select(bank, 0, ctr, out=XIN.view(1, L, T, -1))
             ctr.add_(1).remainder_(NB)
             for l in range(L):
                 b = bufs[l]
-                M.moe_route(routers[l], X[l], b["idx"], b["w"], b["probs"], ws_r)
+                M.moe_route(routers[l], XIN[l], b["idx"], b["w"], b["probs"], ws_r)
                 M.moe_substitute(b["probs"], b["idx"], b["w"], masks[l], cfg.threshold, b["idx2"], b["w2"],
                                  b["flag"], b["mass"])
-                M.moe_decode(experts[l], X[l], b["idx2"], b["w2"], b["y"], X[l + 1], ws_d)
+                M.moe_decode(experts[l], XIN[l], b["idx2"], b["w2"], b["y"], XN[l], ws_d)
 
         stream = torch.cuda.Stream(dev)
         with torch.cuda.stream(stream):
@@ -487,27 +487,25 @@ def run_reference(args):
     import oracle
     oracle.build()
     cfg = W.CONFIGS[1]
-    L = cfg.layers
+    L = args.layers or cfg.layers
     nth = os.cpu_count() or 1
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(L)]
     host = [(lw["Wr"].cpu(), lw["bias"].cpu()) for lw in layers]
-    x0 = W.make_tokens(cfg, 1, 0, "cpu").double().numpy()
+    # independent layers, each with its own token, as in the GPU arm
+    xs = W.make_tokens(cfg, L, 0, "cpu").double().numpy().reshape(L, 1, -1)
 
-    def step(x):
+    def step():
         for l in range(L):
-            r = oracle.router(x, host[l][0], host[l][1], cfg.k)
-            y = oracle.moe(layers[l], x, r["idx"], r["w"], cfg.qbits, nthreads=nth)
-            x = torch.from_numpy(x + y).to(torch.bfloat16).double().numpy()
-        return x
+            r = oracle.router(xs[l], host[l][0], host[l][1], cfg.k)
+            oracle.moe(layers[l], xs[l], r["idx"], r["w"], cfg.qbits, nthreads=nth)
 
-    x = x0
     for _ in range(max(0, min(args.warmup, 1))):
-        x = step(x)
+        step()
     steps = max(1, min(args.steps, 8))
     t0 = time.perf_counter()
     for _ in range(steps):
-        x = step(x)
+        step()
     el = time.perf_counter() - t0
     v = steps / el
     print(json.dumps({
@@ -515,8 +513,9 @@ def run_reference(args):
         "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "decode: 1 token x 40 layers, E=256 top-8 D=2048 F=768, int8 sym "
-                               "blk32 fp16 scales, bf16 x, Zipf(1.1) router bias"},
+        "config": {"workload": f"decode: 1 token x {L} layers, E=256 top-8 D=2048 F=768, int8 sym "
+                               "blk32 fp16 scales, bf16 x, Zipf(1.1) router bias",
+                   "inputs": "independent layers: each layer decodes its own token every step"},
         "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
                          "sample": f"{steps} token(s) x {L} layers"},
         "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -52,7 +52,7 @@ Layout layout(int op, int T, int k, int E, int D, int F) {
 
 // Prefill workspace sections.
 struct PLayout {
-    size_t logits, idx, w, xh, chunk_cnt, chunk_base, cnt, off, gend, tgroup, tm0, tn, nmt, perm_tok, inv, hp, yp;
+    size_t logits, idx, w, xh, pexp, chunk_cnt, chunk_base, cnt, off, gend, tgroup, tm0, tn, nmt, perm_tok, inv, hp, yp;
     size_t total;
     int nchunk, max_mtiles;
 };
@@ -72,6 +72,7 @@ PLayout prefill_layout(int T, int k, int E, int D, int F) {
     L.idx = take(sizeof(int32_t) * n);
     L.w = take(sizeof(float) * n);
     L.xh = take(2 * n * D);  // x rows in grouped order (fp16)
+    L.pexp = take(sizeof(int32_t) * n);  // their power-of-two scale exponents
     L.chunk_cnt = take(sizeof(int32_t) * (size_t)L.nchunk * E);
     L.chunk_base = take(sizeof(int32_t) * (size_t)L.nchunk * E);
     L.cnt = take(sizeof(int32_t) * E);
@@ -209,6 +210,142 @@ FusedParams fused_params(const moe_experts_t* X, const void* x, int k, float* y,
 int qbits_of(const moe_experts_t* X) { return X->q == MOE_Q_INT8_SYM_B32 ? 8 : 4; }
 int scale_bytes(const moe_experts_t* X) { return X->s_dtype == MOE_F16 ? 2 : 4; }
 
+// Routing of many tokens: tensor-core logits + one warp per token when the
+// shapes allow, else the CUDA-core router kernel.
+moe_status_t route_many(const moe_router_t* router, const void* x, moe_dtype_t x_dtype, int T, int32_t* idx_buf,
+                        float* w_buf, float* probs, float* logits, WsHeader* hdr, cudaStream_t s) {
+    const int E = router->E, D = router->D, k = router->k;
+    cudaError_t e;
+    if (x_dtype == MOE_BF16 && router->w_dtype == MOE_BF16 && E % 128 == 0 && D % 64 == 0) {
+        GemmParams g = {};
+        if (!make_tmap_2d(&g.tmA, 2, x, D, T, 2ull * D, 64, 128, 128) ||
+            !make_tmap_2d(&g.tmB0, 2, router->W, D, E, 2ull * D, 64, 128, 128))
+            return MOE_ERR_CUDA;
+        g.K = D;
+        g.rows_per_ntile = 128;
+        g.n_mtiles = (T + 127) / 128;
+        g.m_total = T;
+        g.n_ntiles = E / 128;
+        g.C = logits;
+        g.ldc = E;
+        g.hdr = hdr;
+        e = launch_gemm(g, 16, false, false, g.n_mtiles, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        TopkParams tp = {T, E, k, router->norm_topk ? 1 : 0, logits, router->bias, idx_buf, w_buf, probs};
+        e = launch_topk(tp, s);
+    } else {
+        RouterParams rp = {};
+        rp.T = T;
+        rp.E = E;
+        rp.D = D;
+        rp.k = k;
+        rp.norm_topk = router->norm_topk ? 1 : 0;
+        rp.W = router->W;
+        rp.bias = router->bias;
+        rp.x = x;
+        rp.logits = logits;
+        rp.idx = idx_buf;
+        rp.w = w_buf;
+        rp.probs = probs;
+        rp.hdr = hdr;
+        e = launch_router(rp, router->w_dtype == MOE_BF16, x_dtype == MOE_BF16, s, true);
+    }
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+// The routed experts of many tokens as grouped tensor-core products: stable
+// grouping of the (token, slot) assignments by expert, x gathered in grouped
+// order, gate/up with SwiGLU, down, and the weighted un-permute (y, and
+// x_next = x + y when x_next is given).
+moe_status_t grouped_experts(const moe_experts_t* experts, const void* x, moe_dtype_t x_dtype, int T, int k,
+                             const int32_t* idx_buf, const float* w_buf, float* y, void* x_next, int32_t* counts,
+                             int32_t* perm, void* workspace, const PLayout& P, cudaStream_t s) {
+    const int E = experts->E, D = experts->D, F = experts->F;
+    WsHeader* hdr = at<WsHeader>(workspace, 0);
+    cudaError_t e;
+    const int nt = kEgTile;  // token tile of the expert products
+    PermParams pp = {};
+    pp.tile_rows = nt;
+    pp.n = T * k;
+    pp.k = k;
+    pp.E = E;
+    pp.nchunk = P.nchunk;
+    pp.idx = idx_buf;
+    pp.hdr = hdr;
+    pp.chunk_cnt = at<int32_t>(workspace, P.chunk_cnt);
+    pp.chunk_base = at<int32_t>(workspace, P.chunk_base);
+    pp.cnt = at<int32_t>(workspace, P.cnt);
+    pp.off = at<int32_t>(workspace, P.off);
+    pp.group_end = at<int32_t>(workspace, P.gend);
+    pp.counts_out = counts;
+    pp.tile_group = at<int32_t>(workspace, P.tgroup);
+    pp.tile_m0 = at<int32_t>(workspace, P.tm0);
+    pp.tile_n = at<int32_t>(workspace, P.tn);
+    pp.n_mtiles = at<int>(workspace, P.nmt);
+    pp.perm_tok = at<int32_t>(workspace, P.perm_tok);
+    pp.perm_out = perm;
+    pp.inv = at<int32_t>(workspace, P.inv);
+    e = launch_perm(pp, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    const long n = (long)T * k;
+    void* xp = at<void>(workspace, P.xh);
+    void* hp = at<void>(workspace, P.hp);
+    void* yp = at<void>(workspace, P.yp);
+    int32_t* pexp = at<int32_t>(workspace, P.pexp);
+    e = launch_gather_f16(x, x_dtype == MOE_BF16, pp.perm_tok, (int)n, D, xp, pexp, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    const int qbits = qbits_of(experts);
+    const int cb = qbits == 8 ? 1 : 2;  // codes per byte
+    const unsigned rb = 64 / cb;        // code bytes per row per K stage
+    const bool sf16 = experts->s_dtype == MOE_F16;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    EgParams g1 = {};
+    if (!make_tmap_2d(&g1.tmX, 1, xp, D, n, 2ull * D, 64, nt, 128) ||
+        !make_tmap_2d(&g1.tmXh, 1, xp, D, n, 2ull * D, 64, nt / 2, 128) ||
+        !make_tmap_2d(&g1.tmW0, 0, experts->gate_q, D / cb, (unsigned long long)E * F, D / cb, rb, 64, rb) ||
+        !make_tmap_2d(&g1.tmW1, 0, experts->up_q, D / cb, (unsigned long long)E * F, D / cb, rb, 64, rb))
+        return MOE_ERR_CUDA;
+    g1.S0 = experts->gate_s;
+    g1.S1 = experts->up_s;
+    g1.K = D;
+    g1.w_rows = F;
+    g1.nwb = F / 64;
+    g1.tile_group = pp.tile_group;
+    g1.tile_m0 = pp.tile_m0;
+    g1.tile_n = pp.tile_n;
+    g1.n_tiles_dev = pp.n_mtiles;
+    g1.C = hp;
+    g1.ldc = F;
+    g1.pexp = pexp;
+    g1.hdr = hdr;
+    e = launch_egemm(g1, qbits, sf16, true, sms, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    EgParams g2 = g1;
+    if (!make_tmap_2d(&g2.tmX, 1, hp, F, n, 2ull * F, 64, nt, 128) ||
+        !make_tmap_2d(&g2.tmXh, 1, hp, F, n, 2ull * F, 64, nt / 2, 128) ||
+        !make_tmap_2d(&g2.tmW0, 0, experts->down_q, F / cb, (unsigned long long)E * D, F / cb, rb, 64, rb))
+        return MOE_ERR_CUDA;
+    g2.tmW1 = g2.tmW0;
+    g2.S0 = experts->down_s;
+    g2.S1 = experts->down_s;
+    g2.K = F;
+    g2.w_rows = D;
+    g2.nwb = D / 128;
+    g2.C = yp;
+    g2.ldc = D;
+    e = launch_egemm(g2, qbits, sf16, false, sms, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    CombineParams cp = {T, D, k, pp.inv, w_buf, static_cast<const float*>(yp), y, x, x_dtype == MOE_BF16 ? 1 : 0, x_next};
+    return from_cuda(launch_combine(cp, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -218,7 +355,11 @@ size_t moe_workspace_bytes(int op, int T, int k, int E, int D, int F) {
     if ((op == MOE_OP_DECODE || op == MOE_OP_LAYER || op == MOE_OP_PREFILL) && (F < kBlk || F % kBlk)) return 0;
     if (op == MOE_OP_PREFILL) return prefill_shape_ok(E, D, F) ? prefill_layout(T, k, E, D, F).total : 0;
     if (op < MOE_OP_ROUTE || op > MOE_OP_LAYER) return 0;
-    return layout(op, T, k, E, D, F).total;
+    size_t bytes = layout(op, T, k, E, D, F).total;
+    // several tokens through the grouped products (see moe_decode / moe_layer)
+    if (op != MOE_OP_ROUTE && T >= 2 && prefill_shape_ok(E, D, F))
+        bytes = std::max(bytes, prefill_layout(T, k, E, D, F).total);
+    return bytes;
 }
 
 moe_status_t moe_route(const moe_router_t* router, const void* x, moe_dtype_t x_dtype, int T,
@@ -268,6 +409,13 @@ moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t
             return from_cuda(launch_fused(fp, qbits_of(experts), experts->s_dtype == MOE_F16,
                                           x_dtype == MOE_BF16, grid, smem, s));
         }
+    }
+    if (T >= 2 && prefill_shape_ok(experts->E, experts->D, experts->F)) {
+        // several tokens: each distinct expert's weights are read once, by the
+        // grouped tensor-core products
+        PLayout P = prefill_layout(T, k, experts->E, experts->D, experts->F);
+        if (ws_bytes < P.total) return MOE_ERR_WORKSPACE;
+        return grouped_experts(experts, x, x_dtype, T, k, idx, w, y, x_next, nullptr, nullptr, workspace, P, s);
     }
     ExpertParams ep = expert_params(experts, x, x_dtype, T, k, idx, w, y, x_next, workspace, L);
     PrepParams pp = {};
@@ -322,6 +470,14 @@ moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts,
                                           x_dtype == MOE_BF16, grid, smem, s));
         }
     }
+    if (T >= 2 && prefill_shape_ok(experts->E, experts->D, experts->F)) {
+        PLayout P = prefill_layout(T, k, experts->E, experts->D, experts->F);
+        if (ws_bytes < P.total) return MOE_ERR_WORKSPACE;
+        moe_status_t rs = route_many(router, x, x_dtype, T, idx, w, probs, at<float>(workspace, P.logits),
+                                     at<WsHeader>(workspace, 0), s);
+        if (rs != MOE_OK) return rs;
+        return grouped_experts(experts, x, x_dtype, T, k, idx, w, y, x_next, nullptr, nullptr, workspace, P, s);
+    }
     RouterParams rp = router_params(router, x, T, idx, w, probs, workspace, L);
     ExpertParams ep = expert_params(experts, x, x_dtype, T, k, idx, w, y, x_next, workspace, L);
     rp.xq_hi = const_cast<int8_t*>(ep.xq_hi);
@@ -358,121 +514,9 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     float* logits = at<float>(workspace, P.logits);
     cudaError_t e;
 
-    // routing: tensor-core logits + one warp per token when the shapes allow,
-    // else the CUDA-core router kernel
-    if (x_dtype == MOE_BF16 && router->w_dtype == MOE_BF16 && E % 128 == 0 && D % 64 == 0) {
-        GemmParams g = {};
-        if (!make_tmap_2d(&g.tmA, 2, x, D, T, 2ull * D, 64, 128, 128) ||
-            !make_tmap_2d(&g.tmB0, 2, router->W, D, E, 2ull * D, 64, 128, 128))
-            return MOE_ERR_CUDA;
-        g.K = D;
-        g.rows_per_ntile = 128;
-        g.n_mtiles = (T + 127) / 128;
-        g.m_total = T;
-        g.n_ntiles = E / 128;
-        g.C = logits;
-        g.ldc = E;
-        g.hdr = hdr;
-        e = launch_gemm(g, 16, false, false, g.n_mtiles, s);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-        TopkParams tp = {T, E, k, router->norm_topk ? 1 : 0, logits, router->bias, idx_buf, w_buf, nullptr};
-        e = launch_topk(tp, s);
-    } else {
-        RouterParams rp = {};
-        rp.T = T;
-        rp.E = E;
-        rp.D = D;
-        rp.k = k;
-        rp.norm_topk = router->norm_topk ? 1 : 0;
-        rp.W = router->W;
-        rp.bias = router->bias;
-        rp.x = x;
-        rp.logits = logits;
-        rp.idx = idx_buf;
-        rp.w = w_buf;
-        rp.hdr = hdr;
-        e = launch_router(rp, router->w_dtype == MOE_BF16, x_dtype == MOE_BF16, s, true);
-    }
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-    const int nt = kEgTile;  // token tile of the expert products
-    PermParams pp = {};
-    pp.tile_rows = nt;
-    pp.n = T * k;
-    pp.k = k;
-    pp.E = E;
-    pp.nchunk = P.nchunk;
-    pp.idx = idx_buf;
-    pp.hdr = hdr;
-    pp.chunk_cnt = at<int32_t>(workspace, P.chunk_cnt);
-    pp.chunk_base = at<int32_t>(workspace, P.chunk_base);
-    pp.cnt = at<int32_t>(workspace, P.cnt);
-    pp.off = at<int32_t>(workspace, P.off);
-    pp.group_end = at<int32_t>(workspace, P.gend);
-    pp.counts_out = counts;
-    pp.tile_group = at<int32_t>(workspace, P.tgroup);
-    pp.tile_m0 = at<int32_t>(workspace, P.tm0);
-    pp.tile_n = at<int32_t>(workspace, P.tn);
-    pp.n_mtiles = at<int>(workspace, P.nmt);
-    pp.perm_tok = at<int32_t>(workspace, P.perm_tok);
-    pp.perm_out = perm;
-    pp.inv = at<int32_t>(workspace, P.inv);
-    e = launch_perm(pp, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-    const long n = (long)T * k;
-    void* xp = at<void>(workspace, P.xh);
-    void* hp = at<void>(workspace, P.hp);
-    void* yp = at<void>(workspace, P.yp);
-    e = launch_gather_f16(x, x_dtype == MOE_BF16, pp.perm_tok, (int)n, D, xp, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-    const int qbits = qbits_of(experts);
-    const int cb = qbits == 8 ? 1 : 2;  // codes per byte
-    const unsigned rb = 64 / cb;        // code bytes per row per K stage
-    const bool sf16 = experts->s_dtype == MOE_F16;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    EgParams g1 = {};
-    if (!make_tmap_2d(&g1.tmX, 1, xp, D, n, 2ull * D, 64, nt, 128) ||
-        !make_tmap_2d(&g1.tmXh, 1, xp, D, n, 2ull * D, 64, nt / 2, 128) ||
-        !make_tmap_2d(&g1.tmW0, 0, experts->gate_q, D / cb, (unsigned long long)E * F, D / cb, rb, 64, rb) ||
-        !make_tmap_2d(&g1.tmW1, 0, experts->up_q, D / cb, (unsigned long long)E * F, D / cb, rb, 64, rb))
-        return MOE_ERR_CUDA;
-    g1.S0 = experts->gate_s;
-    g1.S1 = experts->up_s;
-    g1.K = D;
-    g1.w_rows = F;
-    g1.nwb = F / 64;
-    g1.tile_group = pp.tile_group;
-    g1.tile_m0 = pp.tile_m0;
-    g1.tile_n = pp.tile_n;
-    g1.n_tiles_dev = pp.n_mtiles;
-    g1.C = hp;
-    g1.ldc = F;
-    g1.hdr = hdr;
-    e = launch_egemm(g1, qbits, sf16, true, sms, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-    EgParams g2 = g1;
-    if (!make_tmap_2d(&g2.tmX, 1, hp, F, n, 2ull * F, 64, nt, 128) ||
-        !make_tmap_2d(&g2.tmXh, 1, hp, F, n, 2ull * F, 64, nt / 2, 128) ||
-        !make_tmap_2d(&g2.tmW0, 0, experts->down_q, F / cb, (unsigned long long)E * D, F / cb, rb, 64, rb))
-        return MOE_ERR_CUDA;
-    g2.tmW1 = g2.tmW0;
-    g2.S0 = experts->down_s;
-    g2.S1 = experts->down_s;
-    g2.K = F;
-    g2.w_rows = D;
-    g2.nwb = D / 128;
-    g2.C = yp;
-    g2.ldc = D;
-    e = launch_egemm(g2, qbits, sf16, false, sms, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-    CombineParams cp = {T, D, k, pp.inv, w_buf, static_cast<const float*>(yp), y};
-    return from_cuda(launch_combine(cp, s));
+    moe_status_t rs = route_many(router, x, x_dtype, T, idx_buf, w_buf, nullptr, logits, hdr, s);
+    if (rs != MOE_OK) return rs;
+    return grouped_experts(experts, x, x_dtype, T, k, idx_buf, w_buf, y, nullptr, counts, perm, workspace, P, s);
 }
 
 moe_status_t moe_check_status(void* workspace, void* stream) {

@@ -384,13 +384,20 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
             const int N = (it.n + 15) & ~15;
+            // 2^k as an exact fp32 factor (|k| <= 120, split in two steps)
+            auto pow2 = [](int kk) {
+                const int a = kk / 2;
+                return __int_as_float((127 + a) << 23) * __int_as_float((127 + kk - a) << 23);
+            };
             for (int c0 = 0; c0 < N; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(tb + c0, v);
                 tmem_ld_wait();
                 if constexpr (SWIGLU) {
                     // even lane: gate of unit f, columns c0..c0+7; odd lane: up
-                    // of unit f, columns c0+8..c0+15 (each gets the other half)
+                    // of unit f, columns c0+8..c0+15 (each gets the other half).
+                    // The accumulators are x*2^-e products: g, u = acc * 2^e; h
+                    // is stored as h * 2^-2e (the down product undoes it).
                     const bool odd = lane & 1;
                     const int f = it.wb * 64 + (j >> 1);
                     __half* H = reinterpret_cast<__half*>(p.C);
@@ -398,10 +405,13 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
                     for (int i2 = 0; i2 < 8; i2++) {
                         const uint32_t mine = odd ? v[i2] : v[8 + i2];
                         const uint32_t other = __shfl_xor_sync(kFull, mine, 1);
-                        const float g = __uint_as_float(odd ? other : v[i2]);
-                        const float u = __uint_as_float(odd ? v[8 + i2] : other);
                         const int col = c0 + (odd ? 8 : 0) + i2;
-                        if (col < it.n) H[(size_t)(it.m0 + col) * p.ldc + f] = __float2half_rn(silu_mul(g, u));
+                        const int ex = col < it.n ? ld_cg_i32(p.pexp + it.m0 + col) : 0;
+                        const float up = pow2(ex);
+                        const float g = __uint_as_float(odd ? other : v[i2]) * up;
+                        const float u = __uint_as_float(odd ? v[8 + i2] : other) * up;
+                        if (col < it.n)
+                            H[(size_t)(it.m0 + col) * p.ldc + f] = __float2half_rn(silu_mul(g, u) * pow2(-2 * ex));
                     }
                 } else {
                     float* Y = reinterpret_cast<float*>(p.C);
@@ -409,7 +419,10 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
 #pragma unroll
                     for (int i2 = 0; i2 < 16; i2++) {
                         const int col = c0 + i2;
-                        if (col < it.n) Y[(size_t)(it.m0 + col) * p.ldc + dcol] = __uint_as_float(v[i2]);
+                        if (col < it.n) {
+                            const int ex = ld_cg_i32(p.pexp + it.m0 + col);
+                            Y[(size_t)(it.m0 + col) * p.ldc + dcol] = __uint_as_float(v[i2]) * pow2(2 * ex);
+                        }
                     }
                 }
             }

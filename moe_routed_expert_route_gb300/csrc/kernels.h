@@ -160,6 +160,8 @@ struct EgParams {  // aligned like CUtensorMap
     const int* n_tiles_dev;     // number of tiles
     void* C;                    // fp16 H [pos][ldc] (SwiGLU) or fp32 Y [pos][ldc]
     int ldc;
+    const int32_t* pexp;        // [pos] e: the B rows of position pos carry a factor 2^-e (SwiGLU:
+                                // x rows; H is stored times 2^-2e) or 2^-2e (down: H rows)
     WsHeader* hdr;
 };
 
@@ -205,6 +207,9 @@ struct CombineParams {
     const float* w;
     const float* Y;             // [n][D]
     float* y;                   // [T][D]
+    const void* x;              // [T][D] residual source (x_next only)
+    int x_bf16;
+    void* x_next;               // [T][D] x + y in x's dtype, or null
 };
 
 cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu, int max_mtiles, cudaStream_t s);
@@ -212,7 +217,7 @@ cudaError_t launch_egemm(const EgParams& p, int qbits, bool s_f16, bool swiglu, 
 constexpr int kEgTile = 128;  // token tile of the expert products
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 cudaError_t launch_gather_f16(const void* x, bool x_bf16, const int32_t* perm_tok, int n, int D, void* Xp,
-                              cudaStream_t s);
+                              int32_t* pexp, cudaStream_t s);
 cudaError_t launch_perm(const PermParams& p, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 

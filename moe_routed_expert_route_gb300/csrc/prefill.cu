@@ -331,36 +331,63 @@ bool make_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long lon
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// x rows in grouped order as fp16: Xp[pos] = fp16(x[perm_tok[pos]]), 8 per thread
+// x rows in grouped order as fp16, each scaled by a power of two so that its
+// largest magnitude lies in (1/2, 1]: Xp[pos] = fp16(x[t] * 2^-e), t =
+// perm_tok[pos], e = pexp[pos]. Scaling by 2^-e is exact, and fp16 keeps its
+// relative precision at any scale, so this only keeps rows whose values exceed
+// the fp16 range (a residual stream that has grown) finite; the products undo
+// it exactly in their epilogues. One CTA per position.
 __global__ void __launch_bounds__(256) gather_f16_kernel(const void* x, int x_bf16, const int32_t* perm_tok,
-                                                         int n, int D, __half* Xp) {
+                                                         int n, int D, __half* Xp, int32_t* pexp) {
+    __shared__ float s_m[8];
     pdl_wait();
     pdl_trigger();
-    const int per_row = D / 8;
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < (long)n * per_row;
-         i += (long)gridDim.x * blockDim.x) {
-        const int pos = (int)(i / per_row), c = (int)(i - (long)pos * per_row) * 8;
-        const int t = ld_cg_i32(perm_tok + pos);
+    const int pos = blockIdx.x, tid = threadIdx.x;
+    if (pos >= n) return;
+    const int t = ld_cg_i32(perm_tok + pos);
+    const int nv = D / 8;
+    float m = 0.f;
+    for (int v = tid; v < nv; v += 256) {
         float f[8];
-        if (x_bf16) load_f32_cg<__nv_bfloat16, 8>(reinterpret_cast<const __nv_bfloat16*>(x) + (size_t)t * D + c, f);
-        else load_f32_cg<float, 8>(reinterpret_cast<const float*>(x) + (size_t)t * D + c, f);
+        if (x_bf16) load_f32_cg<__nv_bfloat16, 8>(reinterpret_cast<const __nv_bfloat16*>(x) + (size_t)t * D + 8 * v, f);
+        else load_f32_cg<float, 8>(reinterpret_cast<const float*>(x) + (size_t)t * D + 8 * v, f);
+#pragma unroll
+        for (int q = 0; q < 8; q++) m = fmaxf(m, fabsf(f[q]));
+    }
+    m = warp_max(m);
+    if ((tid & 31) == 0) s_m[tid >> 5] = m;
+    __syncthreads();
+    m = s_m[0];
+#pragma unroll
+    for (int i = 1; i < 8; i++) m = fmaxf(m, s_m[i]);
+    // e with m * 2^-e in (1/2, 1] (0 for a zero or non-finite row)
+    int e = 0;
+    if (m > 0.f && m <= 3.0e38f) {
+        e = ((__float_as_int(m) >> 23) & 0xff) - 126;
+        if ((__float_as_int(m) & 0x7fffff) == 0) e -= 1;  // m a power of two: m * 2^-e = 1
+        e = max(-60, min(60, e));  // 2^(2e) stays a normal fp32 factor
+    }
+    const float sc = __int_as_float((127 - e) << 23);  // 2^-e
+    if (tid == 0) pexp[pos] = e;
+    for (int v = tid; v < nv; v += 256) {
+        float f[8];
+        if (x_bf16) load_f32_cg<__nv_bfloat16, 8>(reinterpret_cast<const __nv_bfloat16*>(x) + (size_t)t * D + 8 * v, f);
+        else load_f32_cg<float, 8>(reinterpret_cast<const float*>(x) + (size_t)t * D + 8 * v, f);
         uint4 o;
         uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            __half2 h = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
+            __half2 h = __floats2half2_rn(f[2 * q] * sc, f[2 * q + 1] * sc);
             ow[q] = *reinterpret_cast<uint32_t*>(&h);
         }
-        *reinterpret_cast<uint4*>(Xp + (size_t)pos * D + c) = o;
+        *reinterpret_cast<uint4*>(Xp + (size_t)pos * D + 8 * v) = o;
     }
 }
 
 cudaError_t launch_gather_f16(const void* x, bool x_bf16, const int32_t* perm_tok, int n, int D, void* Xp,
-                              cudaStream_t s) {
-    long work = (long)n * (D / 8);
-    long blocks = std::min<long>((work + 255) / 256, 152L * 16);
-    return launch(gather_f16_kernel, dim3((unsigned)std::max<long>(blocks, 1)), dim3(256), 0, s, true, x,
-                  x_bf16 ? 1 : 0, perm_tok, n, D, reinterpret_cast<__half*>(Xp));
+                              int32_t* pexp, cudaStream_t s) {
+    return launch(gather_f16_kernel, dim3((unsigned)std::max(n, 1)), dim3(256), 0, s, true, x, x_bf16 ? 1 : 0,
+                  perm_tok, n, D, reinterpret_cast<__half*>(Xp), pexp);
 }
 
 // ----------------------------------------------------------- routing
@@ -535,6 +562,22 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
         acc.w = fmaf(w, __uint_as_float(v.w), acc.w);
     }
     *reinterpret_cast<float4*>(p.y + (size_t)t * p.D + d) = acc;
+    if (p.x_next) {
+        const size_t o = (size_t)t * p.D + d;
+        if (p.x_bf16) {
+            float xv[4];
+            load_f32_cg<__nv_bfloat16, 4>(reinterpret_cast<const __nv_bfloat16*>(p.x) + o, xv);
+            __nv_bfloat16* xn = reinterpret_cast<__nv_bfloat16*>(p.x_next) + o;
+            xn[0] = __float2bfloat16_rn(xv[0] + acc.x);
+            xn[1] = __float2bfloat16_rn(xv[1] + acc.y);
+            xn[2] = __float2bfloat16_rn(xv[2] + acc.z);
+            xn[3] = __float2bfloat16_rn(xv[3] + acc.w);
+        } else {
+            const float4 xv = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.x) + o);
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.x_next) + o) =
+                make_float4(xv.x + acc.x, xv.y + acc.y, xv.z + acc.z, xv.w + acc.w);
+        }
+    }
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {

@@ -5,7 +5,9 @@ Criteria (kept identical everywhere):
     two neighbours among the first k+1 within 1e-6 (a near tie: another
     summation order may rank them differently); the number skipped is asserted
     to be small and printed;
-  * routing weights and probabilities: |gpu - oracle| <= 1e-5 / 1e-6;
+  * routing weights: |gpu - oracle| <= 1e-5; probabilities: |gpu - oracle| <=
+    1e-6 + 1e-5 * p (the 2048-term router dot is accumulated in fp32 in
+    another order by the tensor-core router of the multi-token paths);
   * layer output y (fp32): max |y_gpu - y_oracle| <= 2e-3 * max |y_oracle| per
     tensor, where the oracle is evaluated on the routing the GPU chose (the
     routing itself is checked separately above), so near-tie tokens are checked
@@ -64,7 +66,7 @@ def check_routing(ref, got, k, max_skip_frac=0.1):
     assert np.array_equal(gi[keep], ref["idx"][keep]), "routing ids differ from the oracle"
     np.testing.assert_allclose(got["w"].numpy()[keep], ref["w"][keep], rtol=0, atol=1e-5)
     if got.get("probs") is not None:
-        np.testing.assert_allclose(got["probs"].numpy(), ref["probs"], rtol=0, atol=1e-6)
+        np.testing.assert_allclose(got["probs"].numpy(), ref["probs"], rtol=1e-5, atol=1e-6)
     return len(skip)
 
 
