@@ -93,7 +93,7 @@ PLayout prefill_layout(int T, int k, int E, int D, int F) {
 // Grouped GEMM tiling: K stages of 64, gate/up tiles of 64 outputs, down
 // tiles of 128 outputs.
 bool prefill_shape_ok(int E, int D, int F) {
-    return D % 128 == 0 && F % 64 == 0 && D >= 128 && F >= 64 && E <= 1024;
+    return D % 128 == 0 && F % 64 == 0 && D >= 128 && F >= 64 && E <= 1024 && D <= 8192;
 }
 
 bool al16(const void* p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }

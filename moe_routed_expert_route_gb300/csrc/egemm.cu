@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ EgItem s_items[kEgItems];
+    __shared__ int s_pexp[2][kENT];  // scale exponents of the item's positions, per accumulator buffer
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int* status = &p.hdr->status;
@@ -384,6 +385,10 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
             const int N = (it.n + 15) & ~15;
+            // the item's position exponents, once, into shared memory (the four
+            // epilogue warps meet on named barrier 1)
+            s_pexp[buf][j] = j < it.n ? ld_cg_i32(p.pexp + it.m0 + j) : 0;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
             // 2^k as an exact fp32 factor (|k| <= 120, split in two steps)
             auto pow2 = [](int kk) {
                 const int a = kk / 2;
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
                         const uint32_t mine = odd ? v[i2] : v[8 + i2];
                         const uint32_t other = __shfl_xor_sync(kFull, mine, 1);
                         const int col = c0 + (odd ? 8 : 0) + i2;
-                        const int ex = col < it.n ? ld_cg_i32(p.pexp + it.m0 + col) : 0;
+                        const int ex = s_pexp[buf][col];
                         const float up = pow2(ex);
                         const float g = __uint_as_float(odd ? other : v[i2]) * up;
                         const float u = __uint_as_float(odd ? v[8 + i2] : other) * up;
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(kEThreads, 1) egemm_kernel(const __grid_consta
                     for (int i2 = 0; i2 < 16; i2++) {
                         const int col = c0 + i2;
                         if (col < it.n) {
-                            const int ex = ld_cg_i32(p.pexp + it.m0 + col);
+                            const int ex = s_pexp[buf][col];
                             Y[(size_t)(it.m0 + col) * p.ldc + dcol] = __uint_as_float(v[i2]) * pow2(2 * ex);
                         }
                     }

@@ -339,6 +339,7 @@ bool make_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long lon
 // it exactly in their epilogues. One CTA per position.
 __global__ void __launch_bounds__(256) gather_f16_kernel(const void* x, int x_bf16, const int32_t* perm_tok,
                                                          int n, int D, __half* Xp, int32_t* pexp) {
+    constexpr int kV = 4;  // 8-element vectors per thread (D <= 8192)
     __shared__ float s_m[8];
     pdl_wait();
     pdl_trigger();
@@ -346,13 +347,19 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(const void* x, int x_bf
     if (pos >= n) return;
     const int t = ld_cg_i32(perm_tok + pos);
     const int nv = D / 8;
+    float f[kV][8];
     float m = 0.f;
-    for (int v = tid; v < nv; v += 256) {
-        float f[8];
-        if (x_bf16) load_f32_cg<__nv_bfloat16, 8>(reinterpret_cast<const __nv_bfloat16*>(x) + (size_t)t * D + 8 * v, f);
-        else load_f32_cg<float, 8>(reinterpret_cast<const float*>(x) + (size_t)t * D + 8 * v, f);
 #pragma unroll
-        for (int q = 0; q < 8; q++) m = fmaxf(m, fabsf(f[q]));
+    for (int i = 0; i < kV; i++) {
+        const int v = tid + 256 * i;
+#pragma unroll
+        for (int q = 0; q < 8; q++) f[i][q] = 0.f;
+        if (v < nv) {
+            if (x_bf16) load_f32_cg<__nv_bfloat16, 8>(reinterpret_cast<const __nv_bfloat16*>(x) + (size_t)t * D + 8 * v, f[i]);
+            else load_f32_cg<float, 8>(reinterpret_cast<const float*>(x) + (size_t)t * D + 8 * v, f[i]);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; q++) m = fmaxf(m, fabsf(f[i][q]));
     }
     m = warp_max(m);
     if ((tid & 31) == 0) s_m[tid >> 5] = m;
@@ -369,18 +376,19 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(const void* x, int x_bf
     }
     const float sc = __int_as_float((127 - e) << 23);  // 2^-e
     if (tid == 0) pexp[pos] = e;
-    for (int v = tid; v < nv; v += 256) {
-        float f[8];
-        if (x_bf16) load_f32_cg<__nv_bfloat16, 8>(reinterpret_cast<const __nv_bfloat16*>(x) + (size_t)t * D + 8 * v, f);
-        else load_f32_cg<float, 8>(reinterpret_cast<const float*>(x) + (size_t)t * D + 8 * v, f);
-        uint4 o;
-        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            __half2 h = __floats2half2_rn(f[2 * q] * sc, f[2 * q + 1] * sc);
-            ow[q] = *reinterpret_cast<uint32_t*>(&h);
+    for (int i = 0; i < kV; i++) {
+        const int v = tid + 256 * i;
+        if (v < nv) {
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                __half2 h = __floats2half2_rn(f[i][2 * q] * sc, f[i][2 * q + 1] * sc);
+                ow[q] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(Xp + (size_t)pos * D + 8 * v) = o;
         }
-        *reinterpret_cast<uint4*>(Xp + (size_t)pos * D + 8 * v) = o;
     }
 }
 
