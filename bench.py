@@ -28,6 +28,10 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
+# DRAM bytes (read + write) of one launch of the single-token layer kernel on
+# the default workload, from ncu (profiles/fused_layer_kernel_decode_E256_k8.md)
+LAYER_KERNEL_DRAM_BYTES = 41_244_928 + 5_120
+
 import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer decode tokens/s and routed-expert HBM GB/s (% of GB300 peak), 1 GPU"
@@ -302,7 +306,9 @@ def run_ours(args):
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                      "per_launch_bytes": int(per_layer_bytes), "per_launch_us": round(layer_us, 3),
-                     "traffic": None},
+                     # dram__bytes_read.sum + dram__bytes_write.sum of one launch of this
+                     # kernel (ncu capture summarised in profiles/), per launch like achieved
+                     "traffic": LAYER_KERNEL_DRAM_BYTES, "traffic_unit": "bytes per launch"},
         "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": stack.kernels_per_step() * steps,
