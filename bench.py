@@ -29,7 +29,8 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 # DRAM bytes (read + write) of one launch of the single-token layer kernel on
-# the default workload, from ncu (profiles/fused_layer_kernel_decode_E256_k8.md)
+# the default workload: dram__bytes_read.sum + dram__bytes_write.sum from one
+# ncu capture of that launch
 LAYER_KERNEL_DRAM_BYTES = 41_244_928 + 5_120
 
 import workloads as W  # noqa: E402
@@ -306,8 +307,7 @@ def run_ours(args):
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                      "per_launch_bytes": int(per_layer_bytes), "per_launch_us": round(layer_us, 3),
-                     # dram__bytes_read.sum + dram__bytes_write.sum of one launch of this
-                     # kernel (ncu capture summarised in profiles/), per launch like achieved
+                     # measured DRAM bytes of one launch of this kernel, per launch like achieved
                      "traffic": LAYER_KERNEL_DRAM_BYTES, "traffic_unit": "bytes per launch"},
         "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -97,7 +97,8 @@ enum { MOE_OP_ROUTE = 0, MOE_OP_DECODE = 1, MOE_OP_LAYER = 2, MOE_OP_PREFILL = 3
 
 /*
  * Bytes of workspace an operation needs for T tokens (T >= 1). Returns 0 for an
- * invalid combination.
+ * invalid combination. For MOE_OP_DECODE / MOE_OP_LAYER with T >= 2 this covers
+ * the grouped products (see moe_decode).
  */
 size_t moe_workspace_bytes(int op, int T, int k, int E, int D, int F);
 
@@ -142,6 +143,12 @@ moe_status_t moe_substitute(int T, int E, int k, const float* probs, const int32
  *   idx, w  [T][k] routing (int32 ids in [0, E), fp32 weights)
  *   y       [T][D] fp32 out
  *   x_next  [T][D] in x_dtype out, or NULL: x + y rounded to x_dtype (residual)
+ * T = 1 runs one persistent kernel (integer dot products, fp32 accumulation).
+ * T >= 2 with D % 128 == 0, F % 64 == 0, D <= 8192 and E <= 1024 runs the same
+ * grouped tensor-core products as moe_prefill (fp16 operands with exact
+ * per-token power-of-two scaling, fp32 accumulation); other shapes run
+ * CUDA-core kernels. Ids outside [0, E) are skipped and reported by
+ * moe_check_status as MOE_ERR_BAD_INDEX.
  */
 moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t x_dtype, int T,
                         int k, const int32_t* idx, const float* w, float* y, void* x_next,
@@ -151,6 +158,9 @@ moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t
  * One whole layer for T tokens: moe_route followed by moe_decode, with the
  * router's outputs handed to the expert kernels on the device.
  *   idx, w  [T][k] out    probs [T][E] out or NULL    y, x_next as moe_decode
+ * With T >= 2 and bf16 x and router weights (E % 128 == 0), the logits come
+ * from the tensor cores (fp32 accumulation in another order than moe_route;
+ * probabilities may differ in the last bits).
  */
 moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts, const void* x,
                        moe_dtype_t x_dtype, int T, int32_t* idx, float* w, float* probs,
