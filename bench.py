@@ -197,11 +197,23 @@ def time_graph(stack, stream, steps, warmup, world):
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
     if world > 1:
-        t = torch.tensor([ms], device=stack.dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-        torch.distributed.barrier()
+        ms = max_over_ranks(ms, stack.dev)
     return ms
+
+
+def max_over_ranks(ms: float, dev) -> float:
+    """The slowest rank's time (replicas: the job ends when the last one does);
+    every rank returns it. Needs an initialised process group."""
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput of N replicas: units all ranks processed / the
+    slowest rank's time."""
+    return world * units_per_rank / (ms / 1e3)
 
 
 def time_e2e(stack, stream, steps, warmup):
@@ -272,7 +284,7 @@ def run_ours(args):
     status = stack.M.moe_check_status(stack.ws)
     assert status == 0, f"device status {status}"
     ms_step = ms / steps
-    tok_s = world * stack.T * steps / (ms / 1e3)
+    tok_s = job_throughput(stack.T * steps, world, ms)
     routed = stack.routed_bytes_per_step()
     hbm_peak, tf_peak, peak_kind = peaks()
     layer_us = ms_step * 1e3 / stack.L
