@@ -229,7 +229,7 @@ moe_status_t route_many(const moe_router_t* router, const void* x, moe_dtype_t x
         g.C = logits;
         g.ldc = E;
         g.hdr = hdr;
-        e = launch_gemm(g, 16, false, false, g.n_mtiles, s);
+        e = launch_router_gemm(g, s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
         TopkParams tp = {T, E, k, router->norm_topk ? 1 : 0, logits, router->bias, idx_buf, w_buf, probs};
         e = launch_topk(tp, s);

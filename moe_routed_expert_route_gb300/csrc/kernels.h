@@ -122,23 +122,15 @@ struct FusedParams {
     float* h;                 // workspace [k][F]
 };
 
-// Grouped tensor-core matrix product (prefill). Tile (mt, nt): 128 rows of A
-// (positions m0.. of tile mt) times 128 rows of B; operands arrive by TMA.
+// Router logits on the tensor cores: tile (mt, nt) = 128 token rows of x times
+// 128 expert rows of Wr, both bf16 by TMA.
 struct GemmParams {  // aligned like CUtensorMap
-    CUtensorMap tmA;            // 16-bit [rows][K], box {64, 128}, 128-byte swizzle
-    CUtensorMap tmB0, tmB1;     // codes [rows][row bytes], box {64 or 32 bytes, 64 rows};
-                                // 16-bit B (router): tmB0 only, box {64, 128}, swizzled
-    const void *S0, *S1;        // scales of B0 / B1 rows (quantised B)
-    int K;
-    int b_group_rows;           // B rows per expert (row of expert g = g * b_group_rows + ...)
-    int rows_per_ntile;         // tile nt, row j: nt*rows_per_ntile + (j&63) + (j>=64)*half_off
-    int half_off;
-    const int32_t* tile_group;  // [mt] expert, or null (group 0)
-    const int32_t* tile_m0;     // [mt] first position, or null (mt*128)
-    const int32_t* group_end;   // [g] end position, or null (m_total)
-    const int* n_mtiles_dev;    // number of m-tiles on the device, or null (n_mtiles)
+    CUtensorMap tmA;            // x [T][D] bf16, box {64, 128}, 128-byte swizzle
+    CUtensorMap tmB0;           // Wr [E][D] bf16, box {64, 128}, 128-byte swizzle
+    int K;                      // D
+    int rows_per_ntile;         // 128
     int n_mtiles, m_total, n_ntiles;
-    void* C;                    // fp32 [pos][ldc] (plain) or fp16 [pos][ldc] (SwiGLU)
+    void* C;                    // fp32 logits [T][ldc]
     int ldc;
     WsHeader* hdr;
 };
@@ -212,7 +204,7 @@ struct CombineParams {
     void* x_next;               // [T][D] x + y in x's dtype, or null
 };
 
-cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu, int max_mtiles, cudaStream_t s);
+cudaError_t launch_router_gemm(const GemmParams& p, cudaStream_t s);
 cudaError_t launch_egemm(const EgParams& p, int qbits, bool s_f16, bool swiglu, int grid, cudaStream_t s);
 constexpr int kEgTile = 128;  // token tile of the expert products
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);

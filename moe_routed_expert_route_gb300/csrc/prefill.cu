@@ -1,33 +1,25 @@
-// Prefill of many tokens: routing, grouping of the (token, slot) assignments
-// by expert, one grouped matrix product per projection on the 5th-generation
-// tensor cores, and the weighted un-permute.
-//
-// With thousands of tokens every routed expert serves a batch of tokens, so
-// its projections are dense contractions: X_e [m_e x D] times the expert's
-// dequantised weights. Kernels, in stream order:
+// Grouping and routing for many tokens (prefill, and decode of T >= 2):
+// router logits on the tensor cores, the warp top-k, the stable grouping of the
+// (token, slot) assignments by expert, the scaled fp16 gather of x in grouped
+// order and the weighted un-permute. The expert products themselves are in
+// egemm.cu. Kernels, in stream order:
 //   router_gemm  logits = X Wr^T on the tensor cores (bf16 x bf16 -> fp32)
 //   topk         bias, fp32 softmax and top-k per token (one warp per token)
-//   to_f16       x -> fp16 copy (the A operand of the expert products)
 //   hist/scan/place  stable counting sort of the T*k assignments by expert:
 //                per-chunk histograms, one scan (offsets, per-chunk bases and
-//                the list of 128-row tiles per expert), then placement in
-//                (t, r) order inside every expert
-//   gemm gate/up A rows gathered by token index, B = dequantised gate rows and
-//                up rows side by side; the epilogue applies SwiGLU and writes
-//                H (fp16) in grouped order
-//   gemm down    A = H, B = dequantised down rows -> Y (fp32) in grouped order
-//   combine      y[t] = sum_r w[t][r] * Y[inv[t][r]], slot order fixed
+//                the list of token tiles per expert), then placement in (t, r)
+//                order inside every expert
+//   gather_f16   x rows in grouped order, fp16, one power-of-two scale per row
+//   (egemm gate/up with SwiGLU, egemm down)
+//   combine      y[t] = sum_r w[t][r] * Y[inv[t][r]], slot order fixed, and
+//                x_next = x + y
 //
-// The grouped product (one CTA per 128 x 128 output tile, 160 threads):
-// warps 0-3 each own one row of the A tile and one row of the B tile: they
-// copy A with cp.async straight into the 128-byte swizzled K-major layout,
-// copy the int8/int4 codes and scales of their B row, dequantise them to fp16
-// (exact q*s rounded once) into the same layout, fence the writes for the
-// async proxy and arrive on the stage's "full" barrier. One thread of warp 4
-// issues tcgen05.mma (M=128, N=128, K=16, fp32 accumulator in TMEM) for each
-// stage and commits to the stage's "empty" barrier; 4 stages of 64 along K are
-// in flight. After the last stage warps 0-3 read the accumulator rows from
-// TMEM (tcgen05.ld) and write the tile. Every wait is bounded.
+// The router product (one CTA per 128 x 128 tile of logits): one thread
+// streams the x and Wr tiles by TMA (128-byte swizzle, 4 stages of 64 along
+// K), one thread issues tcgen05.mma.cta_group::1.kind::f16 (bf16, M = N = 128,
+// K = 16) into a 128-column TMEM accumulator and commits to per-stage
+// mbarriers; four warps read TMEM with tcgen05.ld for the fp32 epilogue.
+// Every wait is bounded.
 #include <mutex>
 
 #include "group.cuh"
@@ -37,70 +29,19 @@
 namespace moe {
 
 constexpr int kGM = 128;   // tile rows (tokens)
-constexpr int kGN = 128;   // tile columns (B rows)
+constexpr int kGN = 128;   // tile columns (experts)
 constexpr int kGK = 64;    // K per stage = one 128-byte row of 16-bit values
-constexpr int kGS = 4;     // stages of A and B tiles
+constexpr int kGS = 4;     // stages
 constexpr int kGThreads = 224;
+constexpr size_t kGSmem = (size_t)kGS * 2 * 16384 + 1024;  // A + B tile per stage, 1 KB alignment
 
-// 8 codes (int8) -> 8 fp16 values q*s, rounded once.
-__device__ __forceinline__ uint4 deq8_i8(uint2 w, float s) {
-    uint32_t u0 = w.x ^ 0x80808080u, u1 = w.y ^ 0x80808080u;  // bias: byte = q + 128
-    const __half2 magic = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-    uint32_t p[4] = {__byte_perm(u0, 0x64646464u, 0x4140), __byte_perm(u0, 0x64646464u, 0x4342),
-                     __byte_perm(u1, 0x64646464u, 0x4140), __byte_perm(u1, 0x64646464u, 0x4342)};
-    uint4 out;
-    uint32_t* o = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        __half2 q = __hsub2(*reinterpret_cast<__half2*>(&p[i]), magic);  // exact q (|q| <= 128)
-        float2 f = __half22float2(q);
-        __half2 r = __floats2half2_rn(f.x * s, f.y * s);
-        o[i] = *reinterpret_cast<uint32_t*>(&r);
-    }
-    return out;
-}
-// 8 codes (int4, one 32-bit word, element 2j in the low nibble of byte j).
-__device__ __forceinline__ uint4 deq8_i4(uint32_t w, float s) {
-    uint32_t u = w ^ 0x88888888u;  // nibble = q + 8
-    const __half2 magic = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
-    uint4 out;
-    uint32_t* o = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        uint32_t v = u >> (8 * i);
-        uint32_t p = (v & 0xFu) | ((v & 0xF0u) << 12) | 0x64006400u;
-        __half2 q = __hsub2(*reinterpret_cast<__half2*>(&p), magic);
-        float2 f = __half22float2(q);
-        __half2 r = __floats2half2_rn(f.x * s, f.y * s);
-        o[i] = *reinterpret_cast<uint32_t*>(&r);
-    }
-    return out;
-}
-
-
-template <int BMODE, typename ST>
-struct GemmSmem {
-    static constexpr int kR = BMODE == 16 ? 1 : (BMODE == 8 ? 8 : 12);  // raw code stages
-    static constexpr int kRB = BMODE == 8 ? 64 : 32;                    // raw bytes per row per stage
-    static constexpr int kAB = 2 * 16384;                               // A + B tile of one stage
-    static constexpr int kRaw = BMODE == 16 ? 0 : kGN * kRB;
-    static constexpr size_t kBytes = (size_t)kGS * kAB + (size_t)kR * kRaw + 1024;
-};
-
-// Warp roles (224 threads): warp 0 streams the int8/int4 codes of the B tile
-// (TMA, kR stages ahead); warp 6 streams the A tile (TMA, 128-byte swizzle;
-// also the B tile when B is already 16-bit); warps 1-4 dequantise one B row
-// each into the swizzled layout and later run the epilogue; one thread of
-// warp 5 issues the MMAs and owns the TMEM allocation.
-template <int BMODE, typename ST, bool BF16, bool SWIGLU>
+// Roles (7 warps): warp 6 streams both tiles by TMA, one thread of warp 5
+// issues the MMAs and owns the TMEM allocation, warps 1-4 run the epilogue
+// (TMEM lane quarter = warp % 4).
 __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
-    using L = GemmSmem<BMODE, ST>;
-    constexpr int R = L::kR;
     extern __shared__ unsigned char sm_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* ab = sm;                          // [kGS][A 16 KB | B 16 KB]
-    unsigned char* raw = sm + (size_t)kGS * L::kAB;  // [R][128 rows][kRB]
-    __shared__ __align__(8) uint64_t raw_full[R], raw_empty[R], a_full[kGS], b_full[kGS], ab_empty[kGS], done;
+    unsigned char* ab = reinterpret_cast<unsigned char*>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ __align__(8) uint64_t a_full[kGS], ab_empty[kGS], done;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -108,23 +49,15 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     const int mt = blockIdx.x / p.n_ntiles, nt = blockIdx.x - (blockIdx.x / p.n_ntiles) * p.n_ntiles;
     pdl_wait();
     pdl_trigger();
-    const int n_mt = p.n_mtiles_dev ? ld_cg_i32(p.n_mtiles_dev) : p.n_mtiles;
-    if (mt >= n_mt) return;  // whole CTA, before any barrier or allocation
-    const int g = p.tile_group ? ld_cg_i32(p.tile_group + mt) : 0;
-    const int m0 = p.tile_m0 ? ld_cg_i32(p.tile_m0 + mt) : mt * kGM;
-    const int m_end = p.group_end ? ld_cg_i32(p.group_end + g) : p.m_total;
+    if (mt >= p.n_mtiles) return;  // whole CTA, before any barrier or allocation
+    const int m0 = mt * kGM;
     const int nk = p.K / kGK;
     int* status = &p.hdr->status;
 
     if (tid == 0) {
         s_abort = 0;
-        for (int i = 0; i < R; i++) {
-            mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], 128);
-        }
         for (int i = 0; i < kGS; i++) {
             mbar_init(&a_full[i], 1);
-            mbar_init(&b_full[i], 128);
             mbar_init(&ab_empty[i], 1);
         }
         mbar_init(&done, 1);
@@ -138,27 +71,10 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const int brow0 = g * p.b_group_rows + nt * p.rows_per_ntile;  // B rows [0,64): brow0.. of map B0
+    const int brow0 = nt * p.rows_per_ntile;
 
-    if (warp == 0) {
-        // ------------------------------------------------ code producer
-        if constexpr (BMODE != 16) {
-            if (lane == 0) {
-                for (int t = 0; t < nk; t++) {
-                    const int s = t % R;
-                    if (t >= R && !mbar_wait(&raw_empty[s], ((t / R) - 1) & 1, status)) {
-                        s_abort = 1;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&raw_full[s], kGN * L::kRB);
-                    unsigned char* dst = raw + (size_t)s * L::kRaw;
-                    tma_load_2d(dst, &p.tmB0, t * L::kRB, brow0, &raw_full[s]);
-                    tma_load_2d(dst + 64 * L::kRB, &p.tmB1, t * L::kRB, brow0 + p.half_off, &raw_full[s]);
-                }
-            }
-        }
-    } else if (warp == 6) {
-        // ------------------------------------------------ A producer
+    if (warp == 6) {
+        // ------------------------------------------------ A and B producer
         if (lane == 0) {
             for (int t = 0; t < nk; t++) {
                 const int s = t % kGS;
@@ -166,26 +82,24 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
                     s_abort = 1;
                     break;
                 }
-                unsigned char* dst = ab + (size_t)s * L::kAB;
-                mbar_arrive_expect_tx(&a_full[s], BMODE == 16 ? 32768 : 16384);
+                unsigned char* dst = ab + (size_t)s * 32768;
+                mbar_arrive_expect_tx(&a_full[s], 32768);
                 tma_load_2d(dst, &p.tmA, t * kGK, m0, &a_full[s]);
-                if constexpr (BMODE == 16) tma_load_2d(dst + 16384, &p.tmB0, t * kGK, brow0, &a_full[s]);
+                tma_load_2d(dst + 16384, &p.tmB0, t * kGK, brow0, &a_full[s]);
             }
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_f16(BF16, kGM, kGN);
+            const uint32_t idesc = umma_idesc_f16(true, kGM, kGN);
             for (int t = 0; t < nk; t++) {
                 const int s = t % kGS;
-                const unsigned ph = (t / kGS) & 1;
-                if (s_abort || !mbar_wait(&a_full[s], ph, status) ||
-                    (BMODE != 16 && !mbar_wait(&b_full[s], ph, status))) {
+                if (s_abort || !mbar_wait(&a_full[s], (t / kGS) & 1, status)) {
                     s_abort = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = smem_addr(ab + (size_t)s * L::kAB);
+                const uint32_t a0 = smem_addr(ab + (size_t)s * 32768);
                 const uint64_t ad = umma_desc_sw128(a0), bd = umma_desc_sw128(a0 + 16384);
 #pragma unroll
                 for (int kk = 0; kk < kGK / 16; kk++)
@@ -194,82 +108,25 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
             }
             umma_commit(&done);  // also after an abort: completes when the issued MMAs are done
         }
-    } else {
-        // ------------------------------------------------ dequant (warps 1-4)
-        if constexpr (BMODE != 16) {
-            const int j = tid - 32;  // B row of the tile
-            const int half = j >> 6;
-            const ST* Srow = reinterpret_cast<const ST*>(half ? p.S1 : p.S0) +
-                             (size_t)(brow0 + (j & 63) + half * p.half_off) * (p.K / kBlk);
-            float s0n = to_f32(Srow[0]), s1n = to_f32(Srow[1]);
-            for (int t = 0; t < nk; t++) {
-                const int rs = t % R, as = t % kGS;
-                if (s_abort || !mbar_wait(&raw_full[rs], (t / R) & 1, status) ||
-                    (t >= kGS && !mbar_wait(&ab_empty[as], ((t / kGS) - 1) & 1, status))) {
-                    s_abort = 1;
-                    break;
-                }
-                const float s0 = s0n, s1 = s1n;
-                if (t + 1 < nk) {
-                    s0n = to_f32(Srow[2 * t + 2]);
-                    s1n = to_f32(Srow[2 * t + 3]);
-                }
-                const unsigned char* rr = raw + (size_t)rs * L::kRaw + j * L::kRB;
-                unsigned char* bt = ab + (size_t)as * L::kAB + 16384;
-#pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    const float scl = c < 4 ? s0 : s1;
-                    uint4 v;
-                    if constexpr (BMODE == 8) v = deq8_i8(*reinterpret_cast<const uint2*>(rr + 8 * c), scl);
-                    else v = deq8_i4(*reinterpret_cast<const uint32_t*>(rr + 4 * c), scl);
-                    *reinterpret_cast<uint4*>(bt + sw128_off(j, c)) = v;
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&raw_empty[rs]);
-                mbar_arrive(&b_full[as]);
-            }
-        }
-        // ------------------------------------------------ epilogue (warps 1-4)
+    } else if (warp >= 1 && warp <= 4) {
+        // ------------------------------------------------ epilogue
         if (!mbar_wait(&done, 0, status)) s_abort = 1;
         tc_fence_after();
         const int row = 32 * (warp & 3) + lane;  // TMEM lane quarter of this warp
         const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const int pos = m0 + row;
-        const bool valid = pos < m_end && !s_abort;
-        if constexpr (SWIGLU) {
-            __half* C = reinterpret_cast<__half*>(p.C) + (size_t)pos * p.ldc + nt * 64;
+        const bool valid = pos < p.m_total && !s_abort;
+        float* C = reinterpret_cast<float*>(p.C) + (size_t)pos * p.ldc + nt * kGN;
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t gr[16], ur[16];
-                tmem_ld16(trow + 16 * c, gr);
-                tmem_ld16(trow + 64 + 16 * c, ur);
-                tmem_ld_wait();
-                uint32_t o[8];
+        for (int c = 0; c < 8; c++) {
+            uint32_t v[16];
+            tmem_ld16(trow + 16 * c, v);
+            tmem_ld_wait();
+            if (valid) {
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    float h0 = silu_mul(__uint_as_float(gr[2 * q]), __uint_as_float(ur[2 * q]));
-                    float h1 = silu_mul(__uint_as_float(gr[2 * q + 1]), __uint_as_float(ur[2 * q + 1]));
-                    __half2 hh = __floats2half2_rn(h0, h1);
-                    o[q] = *reinterpret_cast<uint32_t*>(&hh);
-                }
-                if (valid) {
-                    reinterpret_cast<uint4*>(C + 16 * c)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    reinterpret_cast<uint4*>(C + 16 * c)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                }
-            }
-        } else {
-            float* C = reinterpret_cast<float*>(p.C) + (size_t)pos * p.ldc + nt * kGN;
-#pragma unroll
-            for (int c = 0; c < 8; c++) {
-                uint32_t v[16];
-                tmem_ld16(trow + 16 * c, v);
-                tmem_ld_wait();
-                if (valid) {
-#pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        reinterpret_cast<uint4*>(C + 16 * c)[q] =
-                            make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
+                for (int q = 0; q < 4; q++)
+                    reinterpret_cast<uint4*>(C + 16 * c)[q] =
+                        make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
     }
@@ -278,25 +135,8 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     if (warp == 5) tmem_dealloc(tmem, 128);
 }
 
-template <int BMODE, typename ST, bool BF16, bool SWIGLU>
-static cudaError_t launch_gemm_t(const GemmParams& p, int max_mtiles, cudaStream_t s) {
-    return launch(gemm_tc_kernel<BMODE, ST, BF16, SWIGLU>, dim3(max_mtiles * p.n_ntiles), dim3(kGThreads),
-                  GemmSmem<BMODE, ST>::kBytes, s, true, p);
-}
-
-cudaError_t launch_gemm(const GemmParams& p, int bmode, bool s_f16, bool swiglu, int max_mtiles,
-                        cudaStream_t s) {
-    if (bmode == 16) return launch_gemm_t<16, float, true, false>(p, max_mtiles, s);
-    if (bmode == 8) {
-        if (swiglu) return s_f16 ? launch_gemm_t<8, __half, false, true>(p, max_mtiles, s)
-                                 : launch_gemm_t<8, float, false, true>(p, max_mtiles, s);
-        return s_f16 ? launch_gemm_t<8, __half, false, false>(p, max_mtiles, s)
-                     : launch_gemm_t<8, float, false, false>(p, max_mtiles, s);
-    }
-    if (swiglu) return s_f16 ? launch_gemm_t<4, __half, false, true>(p, max_mtiles, s)
-                             : launch_gemm_t<4, float, false, true>(p, max_mtiles, s);
-    return s_f16 ? launch_gemm_t<4, __half, false, false>(p, max_mtiles, s)
-                 : launch_gemm_t<4, float, false, false>(p, max_mtiles, s);
+cudaError_t launch_router_gemm(const GemmParams& p, cudaStream_t s) {
+    return launch(gemm_tc_kernel, dim3(p.n_mtiles * p.n_ntiles), dim3(kGThreads), kGSmem, s, true, p);
 }
 
 // ---------------------------------------------------------- tensor maps
