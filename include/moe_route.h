@@ -137,17 +137,17 @@ moe_status_t moe_substitute(int T, int E, int k, const float* probs, const int32
 
 /*
  * Routed experts for T tokens given the routing (Qiita "custom Metal
- * gather_qmm", sections 4 and 7): only experts named in idx are read, each
- * distinct expert once per call.
+ * gather_qmm", sections 4 and 7): only experts named in idx are read.
  *   x       [T][D] in x_dtype (MOE_F32 or MOE_BF16)
  *   idx, w  [T][k] routing (int32 ids in [0, E), fp32 weights)
  *   y       [T][D] fp32 out
  *   x_next  [T][D] in x_dtype out, or NULL: x + y rounded to x_dtype (residual)
- * T = 1 runs one persistent kernel (integer dot products, fp32 accumulation).
- * T >= 2 with D % 128 == 0, F % 64 == 0, D <= 8192 and E <= 1024 runs the same
- * grouped tensor-core products as moe_prefill (fp16 operands with exact
- * per-token power-of-two scaling, fp32 accumulation); other shapes run
- * CUDA-core kernels. Ids outside [0, E) are skipped and reported by
+ * T <= 3 runs one persistent single-token kernel per token (integer dot
+ * products, fp32 accumulation; an expert shared by tokens is read once per
+ * token). T >= 4 with D % 128 == 0, F % 64 == 0, D <= 8192 and E <= 1024 runs
+ * the same grouped tensor-core products as moe_prefill, reading each distinct
+ * expert once (fp16 operands with exact per-token power-of-two scaling, fp32
+ * accumulation); other shapes run CUDA-core kernels. Ids outside [0, E) are skipped and reported by
  * moe_check_status as MOE_ERR_BAD_INDEX.
  */
 moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t x_dtype, int T,
@@ -158,7 +158,7 @@ moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t
  * One whole layer for T tokens: moe_route followed by moe_decode, with the
  * router's outputs handed to the expert kernels on the device.
  *   idx, w  [T][k] out    probs [T][E] out or NULL    y, x_next as moe_decode
- * With T >= 2 and bf16 x and router weights (E % 128 == 0), the logits come
+ * With T >= 4 and bf16 x and router weights (E % 128 == 0), the logits come
  * from the tensor cores (fp32 accumulation in another order than moe_route;
  * probabilities may differ in the last bits).
  */
