@@ -53,6 +53,19 @@ def test_workspace_sizes():
     assert M.moe_workspace_bytes(M.MOE_OP_DECODE, 1, 8, 256, 2048, 100) == 0
 
 
+def test_several_token_workspace_covers_the_grouped_products():
+    # from 2 tokens on, a layer/decode workspace must also hold everything the
+    # grouped products use (the prefill layout of the same T)
+    for T in (2, 4, 64, 256):
+        p = M.moe_workspace_bytes(M.MOE_OP_PREFILL, T, 8, 256, 2048, 768)
+        assert p > 0
+        assert M.moe_workspace_bytes(M.MOE_OP_LAYER, T, 8, 256, 2048, 768) >= p
+        assert M.moe_workspace_bytes(M.MOE_OP_DECODE, T, 8, 256, 2048, 768) >= p
+    # shapes outside the grouped products keep the smaller CUDA-core layout
+    assert M.moe_workspace_bytes(M.MOE_OP_PREFILL, 8, 3, 13, 96, 160) == 0
+    assert M.moe_workspace_bytes(M.MOE_OP_LAYER, 8, 3, 13, 96, 160) > 0
+
+
 def _router(E=8, D=64, k=2, W=16):
     return L._Router(E, D, k, L.MOE_BF16, W, None, 1)
 
