@@ -1,5 +1,5 @@
-// Grouped expert projections of the prefill on the 5th-generation tensor
-// cores, weights stationary.
+// Grouped expert projections on the 5th-generation tensor cores, weights
+// stationary: the prefill, and decode of four or more tokens.
 //
 // Qiita "custom Metal gather_qmm" (sections 4 and 7): the gate and up
 // projections share each token's x, SwiGLU joins them, down maps the
@@ -11,10 +11,9 @@
 // its int8/int4 codes arrive by TMA, are dequantised to fp16 in registers and
 // written to TENSOR MEMORY (tcgen05.st), from where the MMA reads them; the
 // tokens' 16-bit rows are the B operand (N = the tile's token count rounded up
-// to 16), from shared memory by TMA. Keeping A out of shared memory matters:
-// staged through shared memory, every K stage moved ~64-80 KB through it (code
-// tile in and out, A out and in, B in and out) and the shared-memory bandwidth,
-// not the HBM stream or the tensor pipe, set the pace.
+// to 16), from shared memory by TMA. With A in tensor memory a K stage moves
+// only the code tile and the token tile through shared memory (32-48 KB
+// instead of 64-80 KB with A staged there as well).
 // Tensor memory (512 columns): two fp32 accumulators of 128 columns, so that
 // the epilogue of one item overlaps the MMAs of the next, and a ring of 6 A
 // stages of 32 columns (128 rows x 64 fp16). Each tcgen05 instruction costs
