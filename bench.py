@@ -513,18 +513,21 @@ def run_reference(args):
     # independent layers, each with its own token, as in the GPU arm
     xs = W.make_tokens(cfg, L, 0, "cpu").double().numpy().reshape(L, 1, -1)
 
-    def step():
+    def step(threads):
         for l in range(L):
             r = oracle.router(xs[l], host[l][0], host[l][1], cfg.k)
-            oracle.moe(layers[l], xs[l], r["idx"], r["w"], cfg.qbits, nthreads=nth)
+            oracle.moe(layers[l], xs[l], r["idx"], r["w"], cfg.qbits, nthreads=threads)
 
     for _ in range(max(0, min(args.warmup, 1))):
-        step()
+        step(nth)
     steps = max(1, min(args.steps, 8))
     t0 = time.perf_counter()
     for _ in range(steps):
-        step()
+        step(nth)
     el = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    step(1)  # one step on one thread, for scale
+    el1 = time.perf_counter() - t1
     v = steps / el
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tokens/s",
@@ -535,7 +538,9 @@ def run_reference(args):
                                "blk32 fp16 scales, bf16 x, Zipf(1.1) router bias",
                    "inputs": "independent layers: each layer decodes its own token every step"},
         "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
-                         "sample": f"{steps} token(s) x {L} layers"},
+                         "sample": f"{steps} token(s) x {L} layers",
+                         "single_thread": {"value": round(1.0 / el1, 4), "unit": "tokens/s", "cores": 1,
+                                           "sample": f"1 token x {L} layers"}},
         "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
