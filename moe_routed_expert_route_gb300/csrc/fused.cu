@@ -1,4 +1,5 @@
-// One whole MoE layer for one token in ONE persistent launch (decode, T = 1).
+// One whole MoE layer for one token in ONE persistent launch (decode; a batch
+// of up to three tokens is run as one launch per token).
 //
 // lilting.ch "observing the Qwen MoE router" (section "hooking the router"):
 // router logits -> fp32 softmax -> top-k. Qiita "custom Metal gather_qmm"
@@ -13,8 +14,9 @@
 //      router weights (1-4 experts' rows) into registers
 //   1  x -> shared memory; the CTA's logits -> workspace (tagged)
 //   2  warp 0 of every CTA polls all E logits and runs the softmax + top-k
-//      (no second exchange is needed to learn the routing); the other warps
-//      turn x into 16-bit fixed-point planes meanwhile
+//      (no second exchange is needed to learn the routing); the 12 warps that
+//      do not share warp 0's scheduler turn x into 16-bit fixed-point planes
+//      meanwhile
 //   3  one thread starts bulk (TMA) copies of this CTA's rows of the k down
 //      matrices into shared memory while the 16 warps stream this CTA's share
 //      of the k*F gate/up row pairs from HBM (two row pairs in flight per
