@@ -31,12 +31,19 @@
  *    own kernels, so they can be captured into a CUDA graph.
  *  - Synchronous argument checks return MOE_ERR_INVALID_ARG / MOE_ERR_WORKSPACE
  *    / MOE_ERR_UNSUPPORTED before anything is launched. A failed launch returns
- *    MOE_ERR_CUDA. Problems found on the device (an expert id outside [0, E))
- *    are written to the workspace's status word -- the offending access is
- *    skipped, never performed -- and are read back by moe_check_status().
+ *    MOE_ERR_CUDA. Problems found on the device (an expert id outside [0, E),
+ *    a wait that ran out) are written to the workspace's status word -- the
+ *    offending access is skipped, never performed -- and are read back by
+ *    moe_check_status().
  *  - Workspace: `ws_bytes` >= moe_workspace_bytes(op, ...). It must be zeroed
- *    once before its first use (cudaMemset); the library leaves its counters at
- *    zero after every call.
+ *    once before its first use (cudaMemset). Its header holds a launch sequence
+ *    number that keeps growing from call to call; do not clear it afterwards.
+ *  - Single-token calls (T <= 3) run a persistent kernel with one CTA per SM
+ *    whose CTAs wait on one another (bounded waits, about 30 ms by default,
+ *    see moe_set_wait_limit). It needs every SM of the device: a kernel running
+ *    at the same time on another stream can hold SMs until a wait runs out, in
+ *    which case the call records MOE_ERR_DEVICE_TIMEOUT and its outputs are not
+ *    valid. Do not run other kernels concurrently with these calls.
  *  - Alignment: every pointer 16-byte aligned; D and F multiples of 32, so
  *    every int8 row (D or F bytes) and int4 row (D/2 or F/2 bytes) starts on a
  *    16-byte boundary.
@@ -93,7 +100,13 @@ typedef struct {
 } moe_experts_t;
 
 /* Operation ids for moe_workspace_bytes. */
-enum { MOE_OP_ROUTE = 0, MOE_OP_DECODE = 1, MOE_OP_LAYER = 2, MOE_OP_PREFILL = 3 };
+enum {
+    MOE_OP_ROUTE = 0,
+    MOE_OP_DECODE = 1,
+    MOE_OP_LAYER = 2,         /* also moe_layer_stack (with T = 1) */
+    MOE_OP_PREFILL = 3,
+    MOE_OP_LAYER_RESIDENT = 4 /* moe_layer_resident */
+};
 
 /*
  * Bytes of workspace an operation needs for T tokens (T >= 1). Returns 0 for an
@@ -167,6 +180,52 @@ moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts,
                        float* y, void* x_next, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * One whole layer with residency substitution between the router and the
+ * experts (gist.science "Which expert misses are worth waiting for?", method
+ * section; the rule of moe_substitute): the router's top-k, then each missed
+ * expert is kept if it is the token's first choice or its weight is >=
+ * threshold, and otherwise replaced by the best resident expert; the experts
+ * read are the substituted ones.
+ *   resident   [E] uint8 (1 = resident)         threshold as moe_substitute
+ *   idx, w     [T][k] out: the router's top-k and weights (weights are kept by
+ *              a replacement)                   probs [T][E] out or NULL
+ *   idx_used   [T][k] out: the experts read     sub_flag [T][k], sub_mass [T]
+ *              out, as moe_substitute
+ *   y, x_next  as moe_decode
+ * T <= 3 runs the whole layer, substitution included, in one single-token
+ * launch per token; more tokens run moe_layer's kernels with moe_substitute's
+ * kernel between routing and experts. Workspace: MOE_OP_LAYER_RESIDENT.
+ */
+moe_status_t moe_layer_resident(const moe_router_t* router, const moe_experts_t* experts, const void* x,
+                                moe_dtype_t x_dtype, int T, const uint8_t* resident, float threshold,
+                                int32_t* idx, float* w, float* probs, int32_t* idx_used, uint8_t* sub_flag,
+                                float* sub_mass, float* y, void* x_next, void* workspace, size_t ws_bytes,
+                                void* stream);
+
+/*
+ * A stack of nlayers (<= 64) single-token layers in ONE launch of the
+ * single-token layer kernel: layer l+1 starts only when every CTA has written
+ * layer l's y and x_next. All layers share E, D, F, k, the quantisation, the
+ * scale and router dtypes and norm_topk.
+ *   routers, experts   host arrays [nlayers] of descriptors
+ *   x        host array [nlayers] of device pointers, each [D] in x_dtype.
+ *            chain = 1: layer 0 reads x[0] and layer l > 0 reads x_next[l-1]
+ *            (the residual stream; x[l > 0] is ignored). chain = 0: layer l
+ *            reads x[l] (independent tokens), still after layer l-1 is done.
+ *   idx, w   host arrays [nlayers] of device pointers to [k] outputs
+ *   y        host array [nlayers] of device pointers to [D] fp32 outputs
+ *   x_next   host array [nlayers] of device pointers to [D] outputs (x + y in
+ *            x_dtype), entries may be NULL except where chain = 1 needs them
+ *            (l < nlayers - 1); the whole array may be NULL when chain = 0
+ * The host arrays are read during the call only. Workspace: MOE_OP_LAYER with
+ * T = 1. Shapes the single-token kernel cannot run return MOE_ERR_UNSUPPORTED.
+ */
+moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe_experts_t* experts,
+                             const void* const* x, moe_dtype_t x_dtype, int chain, int32_t* const* idx,
+                             float* const* w, float* const* y, void* const* x_next, void* workspace,
+                             size_t ws_bytes, void* stream);
+
+/*
  * Prefill of T tokens: router, then the (token, slot) assignments grouped by
  * expert (histogram, exclusive scan, stable permutation), a grouped matrix
  * product per expert on the tensor cores, and the weighted un-permute.
@@ -187,18 +246,21 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
  * run a layer (a frozen or captured memory pool, a host runtime whose
  * allocator is out of reach, an embedding that hands over only its input and
  * output buffers). Its scratch is a static device array inside the library of
- * 139,520 bytes (header + E tagged logits + k*F activations), held by every GPU
- * that loads the library until the process exits. Limits: E <= 1024,
- * k*F <= 32768, k <= 16, router weights in the dtype of x; larger sizes return
- * MOE_ERR_WORKSPACE, shapes the single-token kernel cannot run return
- * MOE_ERR_UNSUPPORTED. Nothing is allocated: the first call on a device looks
- * up the array's device address (cudaGetSymbolAddress) and caches it, so make
- * that first call before any stream capture. Every call on a device shares the
- * array, which keeps the previous call's contents (the status word is cleared
- * at the start of each call); calls whose execution overlaps on the GPU, e.g.
- * on two streams, race and must be avoided. Device-side conditions (an expert
- * id out of range, a timed-out wait) are not reported by this entry point.
- * Arguments as moe_layer with T = 1.
+ * 147,712 bytes (header + E tagged logits + k*F activations + per-CTA flags),
+ * held by every GPU that loads the library until the process exits. Limits:
+ * E <= 1024 and k*F <= 32768 (beyond them: MOE_ERR_WORKSPACE); router weights
+ * in the dtype of x; shapes the single-token kernel cannot run (k > 32 among
+ * them) return MOE_ERR_UNSUPPORTED. Nothing is allocated: the first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) and caches
+ * it, so make that first call before any stream capture. `stream` must belong
+ * to the current device (MOE_ERR_INVALID_ARG otherwise). Every call on a device
+ * shares the array, which keeps the previous call's contents (the status word
+ * is cleared at the start of each call); calls whose execution overlaps on the
+ * GPU, e.g. on two streams, race and must be avoided. Device-side conditions
+ * (an expert id out of range, a wait that ran out because another kernel held
+ * SMs) are not reported by this entry point, and outputs after such a
+ * condition are not valid: a caller that needs to detect them uses moe_layer
+ * with a workspace and moe_check_status. Arguments as moe_layer with T = 1.
  */
 moe_status_t moe_layer_noalloc(const moe_router_t* router, const moe_experts_t* experts, const void* x,
                                moe_dtype_t x_dtype, int32_t* idx, float* w, float* probs, float* y,
@@ -209,6 +271,16 @@ moe_status_t moe_layer_noalloc(const moe_router_t* router, const moe_experts_t* 
  * zero and returns it (MOE_OK if no device-side problem was recorded).
  */
 moe_status_t moe_check_status(void* workspace, void* stream);
+
+/*
+ * Sets the longest time, in clock64 cycles, that any bounded wait of a kernel
+ * using this workspace spins before it records MOE_ERR_DEVICE_TIMEOUT and lets
+ * the call finish (outputs then not valid); 0 restores the default (2^26
+ * cycles, about 30 ms at 2 GHz). Enqueued on `stream`; it stays set for later
+ * calls on the workspace. A short limit detects a stalled layer sooner; the
+ * library's tests use it to make a wait run out on purpose.
+ */
+moe_status_t moe_set_wait_limit(void* workspace, unsigned long long cycles, void* stream);
 
 /* Static description of a status code. */
 const char* moe_status_string(moe_status_t status);

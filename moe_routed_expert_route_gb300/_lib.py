@@ -25,10 +25,11 @@ MOE_ERR_BAD_INDEX, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_WORKSPACE = 4, 5, 6
 # moe_dtype_t / moe_qfmt_t / op ids
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_Q_INT8_SYM_B32, MOE_Q_INT4_SYM_B32 = 0, 1
-MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_LAYER, MOE_OP_PREFILL = 0, 1, 2, 3
+MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_LAYER, MOE_OP_PREFILL, MOE_OP_LAYER_RESIDENT = 0, 1, 2, 3, 4
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_substitute", "moe_decode", "moe_layer",
-            "moe_prefill", "moe_layer_noalloc", "moe_check_status", "moe_status_string")
+            "moe_layer_resident", "moe_layer_stack", "moe_prefill", "moe_layer_noalloc",
+            "moe_check_status", "moe_set_wait_limit", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -65,11 +66,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer.argtypes = [P, P, P, I, I, P, P, P, P, P, P, S, P]
     lib.moe_prefill.argtypes = [P, P, P, I, I, P, P, P, P, P, P, S, P]
     lib.moe_layer_noalloc.argtypes = [P, P, P, I, P, P, P, P, P, P]
+    lib.moe_layer_resident.argtypes = [P, P, P, I, I, P, ctypes.c_float, P, P, P, P, P, P, P, P, P, S, P]
+    lib.moe_layer_stack.argtypes = [I, P, P, P, I, I, P, P, P, P, P, S, P]
     lib.moe_check_status.argtypes = [P, P]
+    lib.moe_set_wait_limit.argtypes = [P, ctypes.c_ulonglong, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for f in ("moe_route", "moe_substitute", "moe_decode", "moe_layer", "moe_prefill",
-              "moe_layer_noalloc", "moe_check_status"):
+              "moe_layer_noalloc", "moe_layer_resident", "moe_layer_stack", "moe_check_status",
+              "moe_set_wait_limit"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -290,5 +295,73 @@ def moe_layer_noalloc(router: Router, experts: Experts, x, idx, w, probs, y, x_n
                                                        _ptr(y), _ptr(x_next), _stream(stream)))
 
 
+def moe_layer_resident(router: Router, experts: Experts, x, resident, threshold: float, idx, w, probs,
+                       idx_used, sub_flag, sub_mass, y, x_next, ws, stream=None):
+    """One layer with residency substitution between the router and the experts."""
+    r = router.struct()
+    e = experts.struct()
+    T = x.shape[0]
+    _dev(x, "x", (torch.float32, torch.bfloat16), (T, e.D))
+    _dev(resident, "resident", torch.uint8, (r.E,))
+    _dev(idx, "idx", torch.int32, (T, r.k))
+    _dev(w, "w", torch.float32, (T, r.k))
+    if probs is not None:
+        _dev(probs, "probs", torch.float32, (T, r.E))
+    _dev(idx_used, "idx_used", torch.int32, (T, r.k))
+    _dev(sub_flag, "sub_flag", torch.uint8, (T, r.k))
+    _dev(sub_mass, "sub_mass", torch.float32, (T,))
+    _dev(y, "y", torch.float32, (T, e.D))
+    if x_next is not None:
+        _dev(x_next, "x_next", x.dtype, (T, e.D))
+    thr = float(threshold)
+    _check("moe_layer_resident", _lib.moe_layer_resident(
+        ctypes.byref(r), ctypes.byref(e), _ptr(x), _act_dtype(x), T, _ptr(resident), ctypes.c_float(thr),
+        _ptr(idx), _ptr(w), _ptr(probs), _ptr(idx_used), _ptr(sub_flag), _ptr(sub_mass), _ptr(y),
+        _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_layer_stack(routers, experts, x, chain: bool, idx, w, y, x_next, ws, stream=None):
+    """One token through a stack of layers in one launch.
+
+    routers, experts: lists of Router / Experts (one per layer). x, idx, w, y,
+    x_next: lists of per-layer tensors ([1][D], [1][k], [1][k], [1][D], [1][D])
+    or stacked tensors whose first dimension is the layer; x_next may be None
+    when ``chain`` is false."""
+    L = len(routers)
+    if len(experts) != L:
+        raise ValueError("one Experts per Router")
+    rs = (_Router * L)(*[r.struct() for r in routers])
+    es = (_Experts * L)(*[e.struct() for e in experts])
+    D, k = es[0].D, rs[0].k
+
+    def ptrs(ts, name, dtype, shape, optional=False):
+        arr = (ctypes.c_void_p * L)()
+        for l in range(L):
+            t = None if ts is None else ts[l]
+            if t is None:
+                if not optional:
+                    raise ValueError(f"{name}[{l}] is required")
+                arr[l] = None
+                continue
+            _dev(t, f"{name}[{l}]", dtype, shape)
+            arr[l] = t.data_ptr()
+        return arr
+
+    xd = x[0].dtype
+    xs = ptrs(x, "x", xd, (1, D))
+    _act_dtype(x[0])
+    ia = ptrs(idx, "idx", torch.int32, (1, k))
+    wa = ptrs(w, "w", torch.float32, (1, k))
+    ya = ptrs(y, "y", torch.float32, (1, D))
+    xn = None if x_next is None else ptrs(x_next, "x_next", xd, (1, D), optional=True)
+    _check("moe_layer_stack", _lib.moe_layer_stack(L, rs, es, xs, _act_dtype(x[0]), 1 if chain else 0, ia, wa,
+                                                   ya, xn, _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def moe_check_status(ws: torch.Tensor, stream=None) -> int:
     return int(_lib.moe_check_status(_ptr(ws), _stream(stream)))
+
+
+def moe_set_wait_limit(ws: torch.Tensor, cycles: int, stream=None):
+    """Longest spin of any device wait on this workspace (clock64 cycles; 0 = default)."""
+    _check("moe_set_wait_limit", _lib.moe_set_wait_limit(_ptr(ws), int(cycles), _stream(stream)))

@@ -25,6 +25,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Workspace sections, in bytes from the start. 0 = section not used.
 struct Layout {
     size_t logits = 0, xq_hi = 0, xq_lo = 0, xq_s = 0, grp_expert = 0, grp_off = 0, assign = 0, h = 0;
+    size_t flags = 0;
     size_t total = 0;
 };
 
@@ -50,6 +51,8 @@ Layout layout(int op, int T, int k, int E, int D, int F) {
         L.assign = take(sizeof(int32_t) * (size_t)T * k);
         L.h = take(sizeof(uint64_t) * (size_t)T * k * F);
     }
+    // per-CTA completion flags of the single-token layer kernel
+    if (experts) L.flags = take(sizeof(unsigned) * 2 * kFusedMaxGrid);
     L.total = off;
     return L;
 }
@@ -189,13 +192,18 @@ ExpertParams expert_params(const moe_experts_t* X, const void* x, moe_dtype_t x_
     return p;
 }
 
-FusedParams fused_params(const moe_experts_t* X, const void* x, int k, float* y, void* x_next,
-                         void* ws, const Layout& L) {
-    FusedParams f = {};
-    f.E = X->E;
-    f.D = X->D;
-    f.F = X->F;
-    f.k = k;
+FusedCommon fused_common(void* ws, const Layout& L) {
+    FusedCommon f = {};
+    f.nlayers = 1;
+    f.hdr = at<WsHeader>(ws, 0);
+    f.logits = L.logits ? at<uint64_t>(ws, L.logits) : nullptr;
+    f.h = at<float>(ws, L.h);
+    f.flags = at<unsigned>(ws, L.flags);
+    return f;
+}
+
+FusedLayer fused_layer(const moe_experts_t* X, const void* x, float* y, void* x_next) {
+    FusedLayer f = {};
     f.x = x;
     f.gate_q = X->gate_q;
     f.gate_s = X->gate_s;
@@ -205,9 +213,6 @@ FusedParams fused_params(const moe_experts_t* X, const void* x, int k, float* y,
     f.down_s = X->down_s;
     f.y = y;
     f.x_next = x_next;
-    f.hdr = at<WsHeader>(ws, 0);
-    f.logits = L.logits ? at<uint64_t>(ws, L.logits) : nullptr;
-    f.h = at<float>(ws, L.h);
     return f;
 }
 
@@ -305,9 +310,7 @@ moe_status_t grouped_experts(const moe_experts_t* experts, const void* x, moe_dt
     const int cb = qbits == 8 ? 1 : 2;  // codes per byte
     const unsigned rb = 64 / cb;        // code bytes per row per K stage
     const bool sf16 = experts->s_dtype == MOE_F16;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = device_sm_count();
     EgParams g1 = {};
     if (!make_tmap_2d(&g1.tmX, 1, xp, D, n, 2ull * D, 64, nt, 128) ||
         !make_tmap_2d(&g1.tmXh, 1, xp, D, n, 2ull * D, 64, nt / 2, 128) ||
@@ -350,20 +353,135 @@ moe_status_t grouped_experts(const moe_experts_t* experts, const void* x, moe_dt
     return from_cuda(launch_combine(cp, s));
 }
 
+// Offset of the probabilities that substitution reads when the caller passes
+// none (after every other section of a layer workspace).
+size_t layer_bytes(int T, int k, int E, int D, int F) {
+    size_t bytes = layout(MOE_OP_LAYER, T, k, E, D, F).total;
+    // several tokens through the grouped products
+    if (T >= 2 && prefill_shape_ok(E, D, F)) bytes = std::max(bytes, prefill_layout(T, k, E, D, F).total);
+    return align_up(bytes);
+}
+
+// One layer for T tokens, with an optional residency substitution between the
+// routing and the experts.
+moe_status_t layer_impl(const moe_router_t* router, const moe_experts_t* experts, const void* x,
+                        moe_dtype_t x_dtype, int T, const uint8_t* resident, float threshold, int32_t* idx,
+                        float* w, float* probs, int32_t* idx_used, uint8_t* sub_flag, float* sub_mass, float* y,
+                        void* x_next, void* workspace, size_t ws_bytes, cudaStream_t s) {
+    moe_status_t st = check_router(router, x_dtype);
+    if (st != MOE_OK) return st;
+    st = check_experts(experts, x_dtype, router->k);
+    if (st != MOE_OK) return st;
+    if (router->E != experts->E || router->D != experts->D) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > kMaxDecodeT || !al16(x) || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
+    if (x_next && !al16(x_next)) return MOE_ERR_INVALID_ARG;
+    const int k = router->k, E = experts->E, D = experts->D, F = experts->F;
+    Layout L = layout(MOE_OP_LAYER, T, k, E, D, F);
+    if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (T <= kFusedTokens && (router->w_dtype == MOE_BF16) == (x_dtype == MOE_BF16)) {
+        FusedCommon fc = fused_common(workspace, L);
+        size_t smem = 0;
+        int grid = 0;
+        if (fused_plan(E, D, F, k, qbits_of(experts), scale_bytes(experts), x_dtype == MOE_BF16 ? 2 : 4, true,
+                       &fc, &smem, &grid)) {
+            fc.norm_topk = router->norm_topk ? 1 : 0;
+            fc.threshold = threshold;
+            const size_t xb = x_dtype == MOE_BF16 ? 2 : 4;
+            for (int t = 0; t < T; t++) {  // one single-token launch per token
+                FusedLayer ly = fused_layer(experts, static_cast<const char*>(x) + (size_t)t * D * xb,
+                                            y + (size_t)t * D,
+                                            x_next ? static_cast<char*>(x_next) + (size_t)t * D * xb : nullptr);
+                ly.W = router->W;
+                ly.bias = router->bias;
+                ly.idx = idx + (size_t)t * k;
+                ly.w = w + (size_t)t * k;
+                ly.probs = probs ? probs + (size_t)t * E : nullptr;
+                if (resident) {
+                    ly.resident = resident;
+                    ly.idx_used = idx_used + (size_t)t * k;
+                    ly.sub_flag = sub_flag + (size_t)t * k;
+                    ly.sub_mass = sub_mass + t;
+                }
+                cudaError_t e = launch_fused(fc, &ly, qbits_of(experts), experts->s_dtype == MOE_F16,
+                                             x_dtype == MOE_BF16, grid, smem, s);
+                if (e != cudaSuccess) return MOE_ERR_CUDA;
+            }
+            return MOE_OK;
+        }
+    }
+    float* sub_probs = probs;
+    if (resident && !probs) {
+        if (ws_bytes < layer_bytes(T, k, E, D, F) + sizeof(float) * (size_t)T * E) return MOE_ERR_WORKSPACE;
+        sub_probs = at<float>(workspace, layer_bytes(T, k, E, D, F));
+    }
+    // the substituted routing (weights unchanged: a replacement keeps its slot's weight)
+    auto substitute = [&]() {
+        SubstituteParams sp = {T, E, k, sub_probs, idx, w, resident, threshold, idx_used, w, sub_flag, sub_mass};
+        return launch_substitute(sp, s);
+    };
+    if (T >= 2 && prefill_shape_ok(E, D, F)) {
+        PLayout P = prefill_layout(T, k, E, D, F);
+        if (ws_bytes < P.total) return MOE_ERR_WORKSPACE;
+        moe_status_t rs = route_many(router, x, x_dtype, T, idx, w, sub_probs, at<float>(workspace, P.logits),
+                                     at<WsHeader>(workspace, 0), s);
+        if (rs != MOE_OK) return rs;
+        if (resident && substitute() != cudaSuccess) return MOE_ERR_CUDA;
+        return grouped_experts(experts, x, x_dtype, T, k, resident ? idx_used : idx, w, y, x_next, nullptr,
+                               nullptr, workspace, P, s);
+    }
+    RouterParams rp = router_params(router, x, T, idx, w, sub_probs, workspace, L);
+    ExpertParams ep = expert_params(experts, x, x_dtype, T, k, resident ? idx_used : idx, w, y, x_next,
+                                    workspace, L);
+    if (!resident) {
+        // the router's last CTA also builds the expert kernels' inputs
+        rp.xq_hi = const_cast<int8_t*>(ep.xq_hi);
+        rp.xq_lo = const_cast<uint8_t*>(ep.xq_lo);
+        rp.xq_s = const_cast<float*>(ep.xq_s);
+        rp.qbits = ep.qbits;
+        rp.grp_expert = const_cast<int32_t*>(ep.grp_expert);
+        rp.grp_off = const_cast<int32_t*>(ep.grp_off);
+        rp.assign = const_cast<int32_t*>(ep.assign);
+    }
+    cudaError_t e = launch_router(rp, router->w_dtype == MOE_BF16, x_dtype == MOE_BF16, s, true);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (resident) {
+        if (substitute() != cudaSuccess) return MOE_ERR_CUDA;
+        PrepParams pp = {};
+        pp.T = T;
+        pp.E = E;
+        pp.D = D;
+        pp.k = k;
+        pp.qbits = ep.qbits;
+        pp.x = x;
+        pp.x_bf16 = ep.x_bf16;
+        pp.idx = idx_used;
+        pp.hdr = ep.hdr;
+        pp.xq_hi = at<int8_t>(workspace, L.xq_hi);
+        pp.xq_lo = at<uint8_t>(workspace, L.xq_lo);
+        pp.xq_s = at<float>(workspace, L.xq_s);
+        pp.grp_expert = at<int32_t>(workspace, L.grp_expert);
+        pp.grp_off = at<int32_t>(workspace, L.grp_off);
+        pp.assign = at<int32_t>(workspace, L.assign);
+        if (launch_prep(pp, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return from_cuda(launch_experts(ep, s));
+}
+
+__global__ void set_wait_limit_kernel(WsHeader* h, unsigned long long cycles) { h->wait_limit = cycles; }
+
 }  // namespace
 
 extern "C" {
 
 size_t moe_workspace_bytes(int op, int T, int k, int E, int D, int F) {
     if (T < 1 || k < 1 || E < 1 || D < kBlk || D % kBlk) return 0;
-    if ((op == MOE_OP_DECODE || op == MOE_OP_LAYER || op == MOE_OP_PREFILL) && (F < kBlk || F % kBlk)) return 0;
+    if (op != MOE_OP_ROUTE && (F < kBlk || F % kBlk)) return 0;
     if (op == MOE_OP_PREFILL) return prefill_shape_ok(E, D, F) ? prefill_layout(T, k, E, D, F).total : 0;
+    if (op == MOE_OP_LAYER_RESIDENT) return layer_bytes(T, k, E, D, F) + sizeof(float) * (size_t)T * E;
     if (op < MOE_OP_ROUTE || op > MOE_OP_LAYER) return 0;
-    size_t bytes = layout(op, T, k, E, D, F).total;
+    if (op == MOE_OP_ROUTE) return layout(op, T, k, E, D, F).total;
     // several tokens through the grouped products (see moe_decode / moe_layer)
-    if (op != MOE_OP_ROUTE && T >= 2 && prefill_shape_ok(E, D, F))
-        bytes = std::max(bytes, prefill_layout(T, k, E, D, F).total);
-    return bytes;
+    return layer_bytes(T, k, E, D, F);
 }
 
 moe_status_t moe_route(const moe_router_t* router, const void* x, moe_dtype_t x_dtype, int T,
@@ -402,21 +520,20 @@ moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t
     if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T <= kFusedTokens) {
-        FusedParams fp = fused_params(experts, x, k, y, x_next, workspace, L);
+        FusedCommon fc = fused_common(workspace, L);
         size_t smem = 0;
         int grid = 0;
         if (fused_plan(experts->E, experts->D, experts->F, k, qbits_of(experts), scale_bytes(experts),
-                       x_dtype == MOE_BF16 ? 2 : 4, false, &fp, &smem, &grid)) {
-            fp.has_router = 0;
+                       x_dtype == MOE_BF16 ? 2 : 4, false, &fc, &smem, &grid)) {
             const size_t xb = x_dtype == MOE_BF16 ? 2 : 4;
             for (int t = 0; t < T; t++) {  // one single-token launch per token
-                FusedParams ft = fp;
-                ft.x = static_cast<const char*>(x) + (size_t)t * experts->D * xb;
-                ft.y = y + (size_t)t * experts->D;
-                ft.x_next = x_next ? static_cast<char*>(x_next) + (size_t)t * experts->D * xb : nullptr;
-                ft.idx_in = idx + (size_t)t * k;
-                ft.w_in = w + (size_t)t * k;
-                cudaError_t e = launch_fused(ft, qbits_of(experts), experts->s_dtype == MOE_F16,
+                FusedLayer ly = fused_layer(experts, static_cast<const char*>(x) + (size_t)t * experts->D * xb,
+                                            y + (size_t)t * experts->D,
+                                            x_next ? static_cast<char*>(x_next) + (size_t)t * experts->D * xb
+                                                   : nullptr);
+                ly.idx_in = idx + (size_t)t * k;
+                ly.w_in = w + (size_t)t * k;
+                cudaError_t e = launch_fused(fc, &ly, qbits_of(experts), experts->s_dtype == MOE_F16,
                                              x_dtype == MOE_BF16, grid, smem, s);
                 if (e != cudaSuccess) return MOE_ERR_CUDA;
             }
@@ -455,63 +572,67 @@ moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t
 moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts, const void* x,
                        moe_dtype_t x_dtype, int T, int32_t* idx, float* w, float* probs, float* y,
                        void* x_next, void* workspace, size_t ws_bytes, void* stream) {
-    moe_status_t st = check_router(router, x_dtype);
-    if (st != MOE_OK) return st;
-    st = check_experts(experts, x_dtype, router->k);
-    if (st != MOE_OK) return st;
-    if (router->E != experts->E || router->D != experts->D) return MOE_ERR_INVALID_ARG;
-    if (T < 1 || T > kMaxDecodeT || !al16(x) || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
-    if (x_next && !al16(x_next)) return MOE_ERR_INVALID_ARG;
-    const int k = router->k;
-    Layout L = layout(MOE_OP_LAYER, T, k, experts->E, experts->D, experts->F);
+    return layer_impl(router, experts, x, x_dtype, T, nullptr, 0.f, idx, w, probs, nullptr, nullptr, nullptr, y,
+                      x_next, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_layer_resident(const moe_router_t* router, const moe_experts_t* experts, const void* x,
+                                moe_dtype_t x_dtype, int T, const uint8_t* resident, float threshold,
+                                int32_t* idx, float* w, float* probs, int32_t* idx_used, uint8_t* sub_flag,
+                                float* sub_mass, float* y, void* x_next, void* workspace, size_t ws_bytes,
+                                void* stream) {
+    if (!resident || !idx_used || !sub_flag || !sub_mass) return MOE_ERR_INVALID_ARG;
+    if (std::isnan(threshold) || threshold < 0.f) return MOE_ERR_INVALID_ARG;
+    return layer_impl(router, experts, x, x_dtype, T, resident, threshold, idx, w, probs, idx_used, sub_flag,
+                      sub_mass, y, x_next, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe_experts_t* experts,
+                             const void* const* x, moe_dtype_t x_dtype, int chain, int32_t* const* idx,
+                             float* const* w, float* const* y, void* const* x_next, void* workspace,
+                             size_t ws_bytes, void* stream) {
+    if (nlayers < 1 || nlayers > kStackMax || !routers || !experts || !x || !idx || !w || !y)
+        return MOE_ERR_INVALID_ARG;
+    const moe_router_t& R0 = routers[0];
+    const moe_experts_t& X0 = experts[0];
+    for (int l = 0; l < nlayers; l++) {
+        const moe_router_t& R = routers[l];
+        const moe_experts_t& X = experts[l];
+        moe_status_t st = check_router(&R, x_dtype);
+        if (st != MOE_OK) return st;
+        st = check_experts(&X, x_dtype, R.k);
+        if (st != MOE_OK) return st;
+        if (R.E != X.E || R.D != X.D || R.E != R0.E || R.D != R0.D || R.k != R0.k || R.w_dtype != R0.w_dtype ||
+            (R.norm_topk != 0) != (R0.norm_topk != 0) || X.F != X0.F || X.q != X0.q || X.s_dtype != X0.s_dtype)
+            return MOE_ERR_INVALID_ARG;
+        if ((l == 0 || !chain) && !al16(x[l])) return MOE_ERR_INVALID_ARG;
+        if (!idx[l] || !w[l] || !y[l]) return MOE_ERR_INVALID_ARG;
+        void* xn = x_next ? x_next[l] : nullptr;
+        if (xn && !al16(xn)) return MOE_ERR_INVALID_ARG;
+        if (chain && l + 1 < nlayers && !xn) return MOE_ERR_INVALID_ARG;  // the next layer's input
+    }
+    if ((R0.w_dtype == MOE_BF16) != (x_dtype == MOE_BF16)) return MOE_ERR_UNSUPPORTED;
+    Layout L = layout(MOE_OP_LAYER, 1, R0.k, X0.E, X0.D, X0.F);
     if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (T <= kFusedTokens && (router->w_dtype == MOE_BF16) == (x_dtype == MOE_BF16)) {
-        FusedParams fp = fused_params(experts, x, k, y, x_next, workspace, L);
-        size_t smem = 0;
-        int grid = 0;
-        if (fused_plan(experts->E, experts->D, experts->F, k, qbits_of(experts), scale_bytes(experts),
-                       x_dtype == MOE_BF16 ? 2 : 4, true, &fp, &smem, &grid)) {
-            fp.has_router = 1;
-            fp.norm_topk = router->norm_topk ? 1 : 0;
-            fp.W = router->W;
-            fp.bias = router->bias;
-            const size_t xb = x_dtype == MOE_BF16 ? 2 : 4;
-            for (int t = 0; t < T; t++) {  // one single-token launch per token
-                FusedParams ft = fp;
-                ft.x = static_cast<const char*>(x) + (size_t)t * experts->D * xb;
-                ft.y = y + (size_t)t * experts->D;
-                ft.x_next = x_next ? static_cast<char*>(x_next) + (size_t)t * experts->D * xb : nullptr;
-                ft.idx = idx + (size_t)t * k;
-                ft.w = w + (size_t)t * k;
-                ft.probs = probs ? probs + (size_t)t * experts->E : nullptr;
-                cudaError_t e = launch_fused(ft, qbits_of(experts), experts->s_dtype == MOE_F16,
-                                             x_dtype == MOE_BF16, grid, smem, s);
-                if (e != cudaSuccess) return MOE_ERR_CUDA;
-            }
-            return MOE_OK;
-        }
+    FusedCommon fc = fused_common(workspace, L);
+    size_t smem = 0;
+    int grid = 0;
+    if (!fused_plan(X0.E, X0.D, X0.F, R0.k, qbits_of(&X0), scale_bytes(&X0), x_dtype == MOE_BF16 ? 2 : 4, true,
+                    &fc, &smem, &grid))
+        return MOE_ERR_UNSUPPORTED;
+    fc.norm_topk = R0.norm_topk ? 1 : 0;
+    fc.nlayers = nlayers;
+    fc.chain = chain ? 1 : 0;
+    FusedLayer ly[kStackMax];
+    for (int l = 0; l < nlayers; l++) {
+        ly[l] = fused_layer(&experts[l], x[l], y[l], x_next ? x_next[l] : nullptr);
+        ly[l].W = routers[l].W;
+        ly[l].bias = routers[l].bias;
+        ly[l].idx = idx[l];
+        ly[l].w = w[l];
     }
-    if (T >= 2 && prefill_shape_ok(experts->E, experts->D, experts->F)) {
-        PLayout P = prefill_layout(T, k, experts->E, experts->D, experts->F);
-        if (ws_bytes < P.total) return MOE_ERR_WORKSPACE;
-        moe_status_t rs = route_many(router, x, x_dtype, T, idx, w, probs, at<float>(workspace, P.logits),
-                                     at<WsHeader>(workspace, 0), s);
-        if (rs != MOE_OK) return rs;
-        return grouped_experts(experts, x, x_dtype, T, k, idx, w, y, x_next, nullptr, nullptr, workspace, P, s);
-    }
-    RouterParams rp = router_params(router, x, T, idx, w, probs, workspace, L);
-    ExpertParams ep = expert_params(experts, x, x_dtype, T, k, idx, w, y, x_next, workspace, L);
-    rp.xq_hi = const_cast<int8_t*>(ep.xq_hi);
-    rp.xq_lo = const_cast<uint8_t*>(ep.xq_lo);
-    rp.xq_s = const_cast<float*>(ep.xq_s);
-    rp.qbits = ep.qbits;
-    rp.grp_expert = const_cast<int32_t*>(ep.grp_expert);
-    rp.grp_off = const_cast<int32_t*>(ep.grp_off);
-    rp.assign = const_cast<int32_t*>(ep.assign);
-    cudaError_t e = launch_router(rp, router->w_dtype == MOE_BF16, x_dtype == MOE_BF16, s, true);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    return from_cuda(launch_experts(ep, s));
+    return from_cuda(launch_fused(fc, ly, qbits_of(&X0), X0.s_dtype == MOE_F16, x_dtype == MOE_BF16, grid, smem,
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* experts, const void* x,
@@ -534,8 +655,6 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
     int32_t* idx_buf = idx ? idx : at<int32_t>(workspace, P.idx);
     float* w_buf = w ? w : at<float>(workspace, P.w);
     float* logits = at<float>(workspace, P.logits);
-    cudaError_t e;
-
     moe_status_t rs = route_many(router, x, x_dtype, T, idx_buf, w_buf, nullptr, logits, hdr, s);
     if (rs != MOE_OK) return rs;
     return grouped_experts(experts, x, x_dtype, T, k, idx_buf, w_buf, y, nullptr, counts, perm, workspace, P, s);
@@ -547,12 +666,20 @@ moe_status_t moe_check_status(void* workspace, void* stream) {
     int st = 0;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-    // after a device-side problem a launch may have left its counters mid-way:
-    // clear the whole header (status, counters, launch sequence number)
-    size_t clear = st != 0 ? sizeof(WsHeader) : sizeof(int);
-    if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    // only the status word is cleared: the launch sequence number must keep
+    // growing (it tags the values the layer kernel's CTAs exchange), and no
+    // kernel leaves a counter behind, even after a wait ran out
+    if (st != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     return static_cast<moe_status_t>(st);
+}
+
+moe_status_t moe_set_wait_limit(void* workspace, unsigned long long cycles, void* stream) {
+    if (!workspace || ((uintptr_t)workspace & (kAlign - 1))) return MOE_ERR_WORKSPACE;
+    set_wait_limit_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(at<WsHeader>(workspace, 0), cycles);
+    return from_cuda(cudaGetLastError());
 }
 
 const char* moe_status_string(moe_status_t s) {

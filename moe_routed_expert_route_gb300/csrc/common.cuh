@@ -16,17 +16,18 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // ------------------------------------------------------------ workspace header
 // The first 256 bytes of every workspace: device status word, the router's
-// "CTAs finished" counter, the number of distinct routed experts, a grid
-// barrier counter (back at zero when a launch ends) and the launch sequence
-// number that tags values exchanged between CTAs of the persistent kernel.
+// "CTAs finished" counter, the number of distinct routed experts, the launch
+// sequence number that tags values exchanged between the CTAs of the
+// persistent layer kernel, and the limit of every bounded device wait.
 struct WsHeader {
     int status;
     unsigned int done;
     int n_groups;
     unsigned int bar;  // unused, zero
     unsigned int seq;  // launch sequence number of the persistent layer kernel
-    unsigned int hcount[2];  // CTAs done with their activations, by launch parity
-    int pad[57];
+    unsigned int pad0[3];
+    unsigned long long wait_limit;  // clock64 cycles a device wait may spin; 0 = default
+    int pad[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

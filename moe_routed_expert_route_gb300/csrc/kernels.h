@@ -104,22 +104,44 @@ struct SubstituteParams {
     float* mass;
 };
 
-struct FusedParams {
-    int E, D, F, k, norm_topk, has_router, router_nseg, rows;
+// One layer of the persistent single-token layer kernel: its weights, its
+// token and its outputs.
+struct FusedLayer {
     const void* W;            // router [E][D], same dtype as x
-    const float* bias;
-    const void* x;            // [1][D]
+    const float* bias;        // [E] or null
+    const void* x;            // [D] input token
     const void *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
-    const int32_t* idx_in;    // [k] when has_router == 0
+    const int32_t* idx_in;    // [k] routing when there is no router phase
     const float* w_in;
-    int32_t* idx;             // [k] out when has_router
-    float* w;
-    float* probs;             // [E] or null
-    float* y;                 // [D]
-    void* x_next;             // [D] or null
+    const uint8_t* resident;  // [E] residency mask (substitution) or null
+    int32_t* idx;             // [k] out: the router's top-k
+    float* w;                 // [k] out: routing weights
+    float* probs;             // [E] out or null
+    int32_t* idx_used;        // [k] out or null: experts read after substitution
+    uint8_t* sub_flag;        // [k] out or null
+    float* sub_mass;          // [1] out or null
+    float* y;                 // [D] out
+    void* x_next;             // [D] out (x + y in x's dtype) or null
+};
+
+// Shape and workspace of a launch of the single-token layer kernel.
+struct FusedCommon {
+    int E, D, F, k, norm_topk, has_router, router_nseg, rows, nlayers, chain;
+    float threshold;          // substitution threshold (with a residency mask)
+    int pad;
     WsHeader* hdr;
     uint64_t* logits;         // workspace [E], tagged values
-    float* h;                 // workspace [k][F]
+    float* h;                 // workspace [k*F] activations
+    unsigned* flags;          // workspace [2][kFusedMaxGrid] per-CTA completion tags
+};
+
+constexpr int kFusedMaxGrid = 1024;  // CTAs of the layer kernel (<= SMs)
+constexpr int kStackMax = 64;        // layers per launch of the layer kernel
+
+template <int NL>
+struct FusedArgs {
+    FusedCommon c;
+    FusedLayer L[NL];
 };
 
 // Router logits on the tensor cores: tile (mt, nt) = 128 token rows of x times
@@ -214,9 +236,11 @@ cudaError_t launch_perm(const PermParams& p, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
 bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes, bool has_router,
-                FusedParams* fp, size_t* smem, int* grid);
-cudaError_t launch_fused(const FusedParams& p, int qbits, bool s_f16, bool x_bf16, int grid, size_t smem,
-                         cudaStream_t s);
+                FusedCommon* fc, size_t* smem, int* grid);
+// nlayers = fc.nlayers entries of `layers` (<= kStackMax)
+cudaError_t launch_fused(const FusedCommon& fc, const FusedLayer* layers, int qbits, bool s_f16, bool x_bf16,
+                         int grid, size_t smem, cudaStream_t s);
+int device_sm_count();
 cudaError_t launch_router(const RouterParams& p, bool w_bf16, bool x_bf16, cudaStream_t s, bool pdl);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_experts(const ExpertParams& p, cudaStream_t s);

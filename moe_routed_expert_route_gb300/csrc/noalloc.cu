@@ -17,12 +17,15 @@ namespace moe {
 namespace {
 
 // Scratch of the layer kernel: header (status word, launch sequence number,
-// completion counters), the E tagged logits and the k*F activations.
+// wait limit), the E tagged logits, the k*F activations and the per-CTA
+// completion flags.
 constexpr int kNoAllocMaxE = 1024;
 constexpr int kNoAllocMaxKF = 32768;
 constexpr size_t kNoAllocHeader = 256;
 constexpr size_t kNoAllocLogits = sizeof(uint64_t) * kNoAllocMaxE;
-constexpr size_t kNoAllocBytes = kNoAllocHeader + kNoAllocLogits + sizeof(float) * kNoAllocMaxKF;  // 139,520 B
+constexpr size_t kNoAllocH = sizeof(float) * kNoAllocMaxKF;
+constexpr size_t kNoAllocFlags = sizeof(unsigned) * 2 * kFusedMaxGrid;
+constexpr size_t kNoAllocBytes = kNoAllocHeader + kNoAllocLogits + kNoAllocH + kNoAllocFlags;  // 147,712 B
 static_assert(sizeof(WsHeader) == kNoAllocHeader, "header size");
 
 // Zero-initialised at load time; shared by every call on the device.
@@ -62,7 +65,7 @@ extern "C" moe_status_t moe_layer_noalloc(const moe_router_t* router, const moe_
                                           float* probs, float* y, void* x_next, void* stream) {
     if (!router || !experts) return MOE_ERR_INVALID_ARG;
     const int E = experts->E, D = experts->D, F = experts->F, k = router->k;
-    if (router->E != E || router->D != D || k < 1 || k > E || k > 16) return MOE_ERR_INVALID_ARG;
+    if (router->E != E || router->D != D || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
     if (D < kBlk || D % kBlk || F < kBlk || F % kBlk) return MOE_ERR_INVALID_ARG;
     if (E > kNoAllocMaxE || (long)k * F > kNoAllocMaxKF) return MOE_ERR_WORKSPACE;  // beyond the static scratch
     if (router->w_dtype != x_dtype || (x_dtype != MOE_F32 && x_dtype != MOE_BF16)) return MOE_ERR_UNSUPPORTED;
@@ -76,44 +79,51 @@ extern "C" moe_status_t moe_layer_noalloc(const moe_router_t* router, const moe_
     if (router->bias && ((uintptr_t)router->bias & 3u)) return MOE_ERR_INVALID_ARG;
 
     const int qbits = experts->q == MOE_Q_INT8_SYM_B32 ? 8 : 4;
-    FusedParams fp = {};
+    FusedCommon fc = {};
     size_t smem = 0;
     int grid = 0;
     if (!fused_plan(E, D, F, k, qbits, experts->s_dtype == MOE_F16 ? 2 : 4, x_dtype == MOE_BF16 ? 2 : 4,
-                    true, &fp, &smem, &grid))
+                    true, &fc, &smem, &grid))
         return MOE_ERR_UNSUPPORTED;
 
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the scratch address below is the current device's: a stream of another
+    // device would run the kernel against the wrong device's array
+    if (s) {
+        int cur = 0, sdev = 0;
+        if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (sdev != cur) return MOE_ERR_INVALID_ARG;
+    }
     void* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the status word must start at zero; the kernel's counters are kept
-    // consistent from one call to the next by the kernel itself
+    // the status word must start at zero; the rest of the scratch is kept
+    // consistent from one call to the next by the kernel itself (values are
+    // tagged with the launch sequence number in the header)
     if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
 
     unsigned char* base = static_cast<unsigned char*>(scratch);
-    fp.E = E;
-    fp.D = D;
-    fp.F = F;
-    fp.k = k;
-    fp.has_router = 1;
-    fp.norm_topk = router->norm_topk ? 1 : 0;
-    fp.W = router->W;
-    fp.bias = router->bias;
-    fp.x = x;
-    fp.gate_q = experts->gate_q;
-    fp.gate_s = experts->gate_s;
-    fp.up_q = experts->up_q;
-    fp.up_s = experts->up_s;
-    fp.down_q = experts->down_q;
-    fp.down_s = experts->down_s;
-    fp.idx = idx;
-    fp.w = w;
-    fp.probs = probs;
-    fp.y = y;
-    fp.x_next = x_next;
-    fp.hdr = reinterpret_cast<WsHeader*>(base);
-    fp.logits = reinterpret_cast<uint64_t*>(base + kNoAllocHeader);
-    fp.h = reinterpret_cast<float*>(base + kNoAllocHeader + kNoAllocLogits);
-    cudaError_t e = launch_fused(fp, qbits, experts->s_dtype == MOE_F16, x_dtype == MOE_BF16, grid, smem, s);
+    fc.nlayers = 1;
+    fc.norm_topk = router->norm_topk ? 1 : 0;
+    fc.hdr = reinterpret_cast<WsHeader*>(base);
+    fc.logits = reinterpret_cast<uint64_t*>(base + kNoAllocHeader);
+    fc.h = reinterpret_cast<float*>(base + kNoAllocHeader + kNoAllocLogits);
+    fc.flags = reinterpret_cast<unsigned*>(base + kNoAllocHeader + kNoAllocLogits + kNoAllocH);
+    FusedLayer ly = {};
+    ly.W = router->W;
+    ly.bias = router->bias;
+    ly.x = x;
+    ly.gate_q = experts->gate_q;
+    ly.gate_s = experts->gate_s;
+    ly.up_q = experts->up_q;
+    ly.up_s = experts->up_s;
+    ly.down_q = experts->down_q;
+    ly.down_s = experts->down_s;
+    ly.idx = idx;
+    ly.w = w;
+    ly.probs = probs;
+    ly.y = y;
+    ly.x_next = x_next;
+    cudaError_t e = launch_fused(fc, &ly, qbits, experts->s_dtype == MOE_F16, x_dtype == MOE_BF16, grid, smem, s);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

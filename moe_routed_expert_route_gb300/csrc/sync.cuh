@@ -48,11 +48,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned phase) {
 }
 
 // Bounded wait on an mbarrier phase. Returns false (and records a timeout)
-// if the phase did not complete within kSpinLimitCycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned phase, int* status) {
+// if the phase did not complete within `limit` cycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned phase, int* status,
+                                          long long limit = kSpinLimitCycles) {
     long long t0 = clock64();
     while (!mbar_try_wait(bar, phase)) {
-        if (clock64() - t0 > kSpinLimitCycles) {
+        if (clock64() - t0 > limit) {
             record_error(status, MOE_ERR_DEVICE_TIMEOUT);
             return false;
         }
@@ -69,36 +70,27 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Arrive on a completion counter and wait until `target` CTAs have arrived:
-// one thread per CTA polls one word. Bounded: on timeout records
-// MOE_ERR_DEVICE_TIMEOUT, sets *abort and returns (results are then invalid),
-// so a broken launch ends instead of hanging the GPU.
-__device__ __forceinline__ void arrive_and_wait(unsigned* counter, unsigned target, int* status, int* abort) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        red_release_add(counter, 1u);
-        if (!*abort) {
-            long long t0 = clock64();
-            while (ld_acquire_u32(counter) < target) {
-                if (clock64() - t0 > kSpinLimitCycles) {
-                    record_error(status, MOE_ERR_DEVICE_TIMEOUT);
-                    *abort = 1;
-                    break;
-                }
-            }
-        }
-    }
-    __syncthreads();
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // Values exchanged between the CTAs of one launch carry a tag derived from the
-// launch's sequence number in the upper 32 bits of one 64-bit word, so a reader
-// can tell a value of this launch from a stale one without a separate barrier:
-// it polls the data itself. 64-bit aligned accesses are single-copy atomic.
-// The tag is a negative quiet-NaN bit pattern holding 22 bits of the sequence
-// number: zeroed memory and ordinary float data never look like a current tag.
-__device__ __forceinline__ unsigned seq_tag(unsigned seq) { return 0xFFC00000u | (seq & 0x3FFFFFu); }
+// launch's sequence number (the upper 32 bits of one 64-bit word, or a whole
+// 32-bit flag word), so a reader can tell a value of this launch from a stale
+// one by polling the data itself. 64-bit aligned accesses are single-copy
+// atomic. A tag is never 0, so zeroed memory never carries a current tag, and
+// for the first 2^22 sequence numbers it is a negative quiet-NaN bit pattern,
+// which finite float data never is; tags repeat only after 2^32 launches.
+__device__ __forceinline__ unsigned seq_tag(unsigned seq) {
+    unsigned t = (seq + 1u) ^ 0xFFC00000u;
+    return t ? t : 0xFFC00000u;
+}
 __device__ __forceinline__ void st_tagged(uint64_t* p, float v, unsigned tag) {
     uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
@@ -111,45 +103,25 @@ __device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
 __device__ __forceinline__ bool tag_ok(uint64_t w, unsigned tag) { return (unsigned)(w >> 32) == tag; }
 __device__ __forceinline__ float tag_val(uint64_t w) { return __uint_as_float((unsigned)w); }
 
-// Reads n tagged values [i0, i0 + n*stride) of this launch into out[] (n is a
-// compile-time bound, entries with i >= limit read as 0), polling until every
-// value carries `tag`. Bounded: on timeout records MOE_ERR_DEVICE_TIMEOUT,
-// sets *abort and returns what it has.
-template <int N>
-__device__ __forceinline__ void ld_tagged_all(const uint64_t* base, int i0, int stride, int limit,
-                                              unsigned tag, float* out, int* status, int* abort) {
-    bool ready[N];
-#pragma unroll
-    for (int q = 0; q < N; q++) {
-        int i = i0 + q * stride;
-        ready[q] = i >= limit;
-        out[q] = 0.f;
-    }
-    long long t0 = clock64();
+// Called by one whole warp: polls the n flag words flags[0..n) until every one
+// holds `tag` (all loads of a round in flight before any is examined), then
+// fences so that what the flags' writers stored before their release is
+// visible. Bounded: on timeout records MOE_ERR_DEVICE_TIMEOUT and returns false.
+__device__ __forceinline__ bool poll_flags(const unsigned* flags, int n, unsigned tag, long long limit,
+                                           int* status) {
+    const int lane = threadIdx.x & 31;
+    const long long t0 = clock64();
     while (true) {
-        uint64_t w[N];
-#pragma unroll
-        for (int q = 0; q < N; q++)  // all loads in flight before the first is examined
-            if (!ready[q]) w[q] = ld_tagged(base + i0 + q * stride);
         bool all = true;
-#pragma unroll
-        for (int q = 0; q < N; q++) {
-            if (!ready[q]) {
-                if (tag_ok(w[q], tag)) {
-                    ready[q] = true;
-                    out[q] = tag_val(w[q]);
-                } else {
-                    all = false;
-                }
-            }
-        }
-        if (all || *abort) break;
-        if (clock64() - t0 > kSpinLimitCycles) {
-            record_error(status, MOE_ERR_DEVICE_TIMEOUT);
-            *abort = 1;
-            break;
+        for (int i = lane; i < n; i += 32) all &= ld_relaxed_u32(flags + i) == tag;
+        if (__all_sync(0xffffffffu, all)) break;
+        if (clock64() - t0 > limit) {
+            if (lane == 0) record_error(status, MOE_ERR_DEVICE_TIMEOUT);
+            return false;
         }
     }
+    fence_acq_rel_gpu();
+    return true;
 }
 
 }  // namespace moe

@@ -194,3 +194,44 @@ def near_tie_tokens(probs32: np.ndarray, k: int, eps: float = 1e-6) -> np.ndarra
     kk = min(k + 1, p.shape[1])
     gaps = p[:, : kk - 1] - p[:, 1:kk]
     return np.nonzero((gaps <= eps).any(axis=1))[0]
+
+
+def substitution_near_ties(probs32, idx, w, resident, threshold: float, eps: float = 1e-6) -> np.ndarray:
+    """Tokens whose residency substitution (gist.science, method section: keep
+    a missed expert that is the first choice or has weight >= threshold, else
+    replace it by the best resident expert outside the token's k) could
+    legitimately come out differently under another summation order of the
+    same arithmetic:
+
+      * a missed slot r >= 1 whose weight lies within ``eps`` of a positive
+        threshold (the keep-or-replace decision could flip), or
+      * m >= 1 slots are replaced and two neighbours among the first m+1
+        replacement candidates (resident experts outside the token's k, sorted
+        by fp32 probability) lie within ``eps`` (which candidate goes to which
+        slot could change).
+    """
+    p = np.asarray(probs32, dtype=np.float64)
+    idx = np.asarray(idx, dtype=np.int64)
+    w = np.asarray(w, dtype=np.float64)
+    res = np.asarray(resident).astype(bool)
+    T, k = idx.shape
+    out = []
+    for t in range(T):
+        own = set(idx[t].tolist())
+        ambiguous = False
+        m = 0
+        for r in range(1, k):
+            if res[idx[t, r]]:
+                continue
+            if threshold > 0 and abs(w[t, r] - threshold) <= eps:
+                ambiguous = True
+            elif w[t, r] < threshold:
+                m += 1
+        if not ambiguous and m >= 1:
+            cand = np.array([p[t, e] for e in range(p.shape[1]) if res[e] and e not in own])
+            cand = np.sort(cand)[::-1][: m + 1]
+            if cand.size >= 2 and ((cand[:-1] - cand[1:]) <= eps).any():
+                ambiguous = True
+        if ambiguous:
+            out.append(t)
+    return np.asarray(out, dtype=np.int64)

@@ -28,3 +28,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Near ties and ambiguous substitutions excluded from the bit-exact
+    comparisons, per test case (the parity rule asks for the count)."""
+    try:
+        from parity import TIES
+    except Exception:  # pragma: no cover
+        return
+    if not TIES:
+        return
+    tr = terminalreporter
+    tr.section("excluded from bit-exact comparison (near ties within 1e-6)")
+    for key, (n, total) in TIES.items():
+        tr.write_line(f"{key}: {n} of {total}")

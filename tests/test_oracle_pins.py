@@ -468,3 +468,58 @@ def test_pins_pass_on_the_real_oracle():
 def test_planted_mistake_is_caught(tmp_path, name):
     lib = _build_mutant(tmp_path, name)
     assert not _pins_pass(lib), f"planted mistake {name} passed every pin"
+
+
+# ------------------------------------------------- near-tie exclusion rules
+
+def _exact(expr: str) -> float:
+    """Value of a golden's arithmetic expression (numbers, + - * **), computed
+    exactly with fractions and then rounded once to fp32."""
+    import ast
+
+    def ev(n):
+        if isinstance(n, ast.Expression):
+            return ev(n.body)
+        if isinstance(n, ast.Constant) and isinstance(n.value, (int, float)):
+            return Fraction(str(n.value))
+        if isinstance(n, ast.UnaryOp) and isinstance(n.op, ast.USub):
+            return -ev(n.operand)
+        if isinstance(n, ast.BinOp):
+            a, b = ev(n.left), ev(n.right)
+            if isinstance(n.op, ast.Add):
+                return a + b
+            if isinstance(n.op, ast.Sub):
+                return a - b
+            if isinstance(n.op, ast.Mult):
+                return a * b
+            if isinstance(n.op, ast.Pow) and b.denominator == 1:
+                return a ** int(b)
+        raise ValueError(f"unsupported expression {expr!r}")
+
+    v = ev(ast.parse(expr, mode="eval"))
+    f32 = np.float32(float(v))
+    assert Fraction(float(f32)) == v, f"{expr} is not exactly representable in fp32"
+    return float(f32)
+
+
+def test_near_tie_tokens_golden():
+    g = json.load(open(os.path.join(GOLDEN, "near_ties.json")))
+    for case in g["cases"]:
+        p = np.array([[_exact(v) for v in row] for row in case["rows"]], dtype=np.float32)
+        got = oracle.near_tie_tokens(p, case["k"]).tolist()
+        assert got == case["excluded"], (case["why"], got)
+
+
+def test_substitution_near_ties_golden():
+    g = json.load(open(os.path.join(GOLDEN, "substitution_ties.json")))
+    toks = g["tokens"]
+    p = np.array([[_exact(v) for v in t["probs"]] for t in toks], dtype=np.float32)
+    idx = np.array([t["idx"] for t in toks], dtype=np.int32)
+    w = np.array([t["w"] for t in toks], dtype=np.float64)
+    res = np.array(g["resident"], dtype=np.uint8)
+    got = oracle.substitution_near_ties(p, idx, w, res, g["threshold"]).tolist()
+    assert got == g["ambiguous"], got
+    # the rule never fires for fetch-all (threshold 0) through the weight test,
+    # nor for the first-choice rule (threshold +inf)
+    assert 0 not in oracle.substitution_near_ties(p[:1], idx[:1], w[:1], res, float("inf")).tolist()
+    assert oracle.substitution_near_ties(p[:2], idx[:2], w[:2], res, 0.0).tolist() == []

@@ -1,27 +1,31 @@
 """GPU path vs the CPU oracle, element by element, through the C ABI.
 
-Criteria (kept identical everywhere):
+Criteria (shared with the prefill tests, see tests/parity.py):
   * routing ids: bit-exact, except tokens whose sorted oracle probabilities have
     two neighbours among the first k+1 within 1e-6 (a near tie: another
-    summation order may rank them differently); the number skipped is asserted
-    to be small and printed;
+    summation order may rank them differently); such a token must still get a
+    valid top-k under the oracle's probabilities; the number excluded is
+    asserted to be small and printed in the pytest summary;
   * routing weights: |gpu - oracle| <= 1e-5; probabilities: |gpu - oracle| <=
     1e-6 + 1e-5 * p (the 2048-term router dot is accumulated in fp32 in
     another order by the tensor-core router of the multi-token paths);
   * layer output y (fp32): max |y_gpu - y_oracle| <= 2e-3 * max |y_oracle| per
     tensor, where the oracle is evaluated on the routing the GPU chose (the
     routing itself is checked separately above), so near-tie tokens are checked
-    too.
+    too;
+  * substitution: ids, flags bit-exact and mass within 1e-6 against the
+    oracle's routing followed by the oracle's substitution, excluding routing
+    near ties and ambiguous substitutions (a weight within 1e-6 of the
+    threshold, near-tied replacement candidates), counted and printed.
 """
 from __future__ import annotations
-
-import os
 
 import numpy as np
 import pytest
 import torch
 
 import oracle
+import parity
 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -31,8 +35,8 @@ if torch.cuda.is_available():
     import moe_routed_expert_route_gb300 as M  # noqa: F811
 
 DEV = "cuda"
-REL_TOL = 2e-3
-NTH = os.cpu_count() or 1
+REL_TOL = parity.REL_TOL
+NTH = parity.NTH
 
 
 def small_cfg(E, k, D, F, qbits=8, scale=torch.float16, x_dtype=torch.bfloat16,
@@ -57,26 +61,14 @@ def gpu_layer(cfg, layer, x, probs=True, x_next=False):
     return {k_: (v.cpu() if v is not None else None) for k_, v in out.items()}
 
 
-def check_routing(ref, got, k, max_skip_frac=0.1):
-    T = ref["idx"].shape[0]
-    skip = set(oracle.near_tie_tokens(ref["probs32"], k).tolist())
-    keep = np.array([t for t in range(T) if t not in skip], dtype=np.int64)
-    assert len(skip) <= max(1, int(max_skip_frac * T)), f"{len(skip)} near-tie tokens of {T}"
-    gi = got["idx"].numpy()
-    assert np.array_equal(gi[keep], ref["idx"][keep]), "routing ids differ from the oracle"
-    np.testing.assert_allclose(got["w"].numpy()[keep], ref["w"][keep], rtol=0, atol=1e-5)
-    if got.get("probs") is not None:
-        np.testing.assert_allclose(got["probs"].numpy(), ref["probs"], rtol=1e-5, atol=1e-6)
-    return len(skip)
+def check_routing(ref, got, k, max_skip_frac=0.1, label=""):
+    g = {n: (got[n].numpy() if got.get(n) is not None else None) for n in ("idx", "w", "probs")}
+    return parity.check_routing(ref, g, k, max_skip_frac, label=label)
 
 
 def check_y(layer, x, got, qbits, T=None):
-    y_ref = oracle.moe(layer, x, got["idx"], got["w"].double(), qbits, nthreads=NTH)
-    y = got["y"].double().numpy()
-    err = np.abs(y - y_ref).max()
-    bound = REL_TOL * np.abs(y_ref).max()
-    assert err <= bound, f"max|y - oracle| = {err:.3e} > {bound:.3e}"
-    return err / np.abs(y_ref).max()
+    return parity.check_y(layer, x, got["idx"].numpy(), got["w"].double().numpy(), got["y"].double().numpy(),
+                          qbits)
 
 
 # ------------------------------------------------------------------ tiny
@@ -87,7 +79,7 @@ def test_tiny_layer_matches_oracle():
     x = W.make_tokens(cfg, cfg.T, 0, DEV)
     got = gpu_layer(cfg, layer, x)
     ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
-    check_routing(ref, got, cfg.k)
+    check_routing(ref, got, cfg.k, label="tiny E8 k2 T4")
     check_y(layer, x, got, cfg.qbits)
     # and against the oracle's own routing, token by token where routing agrees
     np.testing.assert_allclose(got["y"].double().numpy(), ref["y"], rtol=0,
@@ -131,7 +123,7 @@ def test_ragged_shapes(qbits, scale, x_dtype, rdt, shape):
     x = W.make_tokens(cfg, T, 3, DEV)
     got = gpu_layer(cfg, layer, x)
     ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
-    check_routing(ref, got, cfg.k, max_skip_frac=0.5)
+    check_routing(ref, got, cfg.k, max_skip_frac=0.5, label=f"ragged {shape} q{qbits}")
     check_y(layer, x, got, cfg.qbits)
 
 
@@ -153,7 +145,7 @@ def test_single_token_layer(qbits, scale, x_dtype, rdt, shape):
         x = W.make_tokens(cfg, 1, stream, DEV)
         got = gpu_layer(cfg, layer, x, x_next=True)
         ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
-        check_routing(ref, got, cfg.k, max_skip_frac=1.0)
+        check_routing(ref, got, cfg.k, max_skip_frac=1.0, label=f"single token {shape} q{qbits}")
         check_y(layer, x, got, cfg.qbits)
         assert torch.equal(got["x_next"], (x.cpu().float() + got["y"]).to(x.dtype))
         # the same routing through moe_decode (no router phase)
@@ -166,8 +158,8 @@ def test_single_token_layer(qbits, scale, x_dtype, rdt, shape):
 
 
 def test_single_token_repeated_launches_reuse_workspace():
-    """Back-to-back persistent launches on one workspace: the grid-barrier
-    counter must be back at zero after every launch."""
+    """Back-to-back persistent launches on one workspace: every launch tags
+    its exchanges with a new sequence number and leaves no counter behind."""
     cfg = small_cfg(64, 4, 512, 256, cfg_id=90)
     layer = W.make_layer(cfg, 0, DEV)
     router = M.Router(layer["Wr"], layer["bias"], cfg.k)
@@ -194,7 +186,7 @@ def test_k_equals_e_and_one_hot():
     x = W.make_tokens(cfg, 6, 0, DEV)
     got = gpu_layer(cfg, layer, x)
     ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
-    check_routing(ref, got, cfg.k)
+    check_routing(ref, got, cfg.k, label="k = E = 8")
     check_y(layer, x, got, cfg.qbits)
     np.testing.assert_allclose(got["w"].numpy().sum(1), 1.0, atol=1e-6)
     # one-hot router: bias +30 on expert 5, k = 1 -> y = that expert's MLP
@@ -225,7 +217,7 @@ def test_decode_e256_chain_matches_oracle(cfg1_layers):
     for l, layer in enumerate(layers):
         got = gpu_layer(cfg, layer, x, x_next=True)
         ref = oracle.layer_forward(layer, x, cfg.k, cfg.qbits)
-        skipped += check_routing(ref, got, cfg.k, max_skip_frac=1.0)
+        skipped += check_routing(ref, got, cfg.k, max_skip_frac=1.0, label="decode E256 chain")
         check_y(layer, x, got, cfg.qbits)
         # x_{l+1} = bf16(x_l + y_l), built from the oracle's y
         x = (x.cpu().double() + torch.from_numpy(ref["y"])).to(torch.bfloat16).to(DEV)
@@ -239,7 +231,7 @@ def test_batched_decode_sweep(cfg1_layers, T):
     x = W.make_tokens(cfg, T, 7, DEV)
     got = gpu_layer(cfg, layer, x)
     ref = oracle.router(x, layer["Wr"], layer["bias"], cfg.k)
-    check_routing(ref, got, cfg.k)
+    check_routing(ref, got, cfg.k, label=f"batched decode E256 T={T}")
     check_y(layer, x, got, cfg.qbits)
 
 
@@ -308,16 +300,138 @@ def test_substitution_and_int4_decode(cfg3_layer, T, threshold):
     assert M.moe_check_status(ws) == M.MOE_OK
     got = dict(idx=idx.cpu(), w=w.cpu(), probs=probs.cpu())
     ref = oracle.router(x, layer["Wr"], layer["bias"], k)
-    check_routing(ref, got, k, max_skip_frac=0.2)
-    # substitution on the GPU's own routing and probabilities (decisions in fp32)
+    check_routing(ref, got, k, max_skip_frac=0.2, label=f"substitution E512 T={T} thr={threshold}")
+    # the kernel alone: the oracle's rule on the GPU's own probabilities (decisions in fp32)
     sref = oracle.substitute(probs.cpu().numpy(), idx.cpu(), w.cpu().double(), mask.cpu(), threshold)
     assert np.array_equal(flag.cpu().numpy(), sref["flag"])
     assert np.array_equal(idx2.cpu().numpy(), sref["idx"])
     np.testing.assert_allclose(mass.cpu().numpy(), sref["mass"], rtol=0, atol=1e-6)
     assert torch.equal(w2.cpu(), w.cpu())
+    # end to end: the oracle's own routing followed by its substitution rule
+    parity.check_substitution(ref, mask.cpu().numpy(), threshold,
+                              dict(idx_used=idx2.cpu().numpy(), flag=flag.cpu().numpy(), mass=mass.cpu().numpy()),
+                              label=f"substitution E512 T={T} thr={threshold}")
     check_y(layer, x, dict(idx=idx2.cpu(), w=w2.cpu(), y=y.cpu()), cfg.qbits)
     n_sub = int((flag == 2).sum())
     print(f"T={T} thr={threshold}: substituted {n_sub}/{T * k}, mass mean {mass.mean().item():.4f}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 16])
+@pytest.mark.parametrize("threshold", [0.15, 0.0, float("inf")])
+def test_layer_resident_matches_oracle(cfg3_layer, T, threshold):
+    """moe_layer_resident: routing, substitution and int4 experts in one call
+    (one launch per token for T <= 3)."""
+    cfg, layer, mask = cfg3_layer
+    k = cfg.k
+    x = W.make_tokens(cfg, T, 12, DEV)
+    router = M.Router(layer["Wr"], layer["bias"], k)
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    out = dict(idx=torch.empty(T, k, dtype=torch.int32, device=DEV), w=torch.empty(T, k, device=DEV),
+               probs=torch.empty(T, cfg.E, device=DEV), idx_used=torch.full((T, k), -9, dtype=torch.int32,
+                                                                            device=DEV),
+               flag=torch.full((T, k), 9, dtype=torch.uint8, device=DEV), mass=torch.empty(T, device=DEV),
+               y=torch.empty(T, cfg.D, device=DEV), xn=torch.empty_like(x))
+    ws = M.workspace(M.MOE_OP_LAYER_RESIDENT, T, k, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_layer_resident(router, experts, x, mask, threshold, out["idx"], out["w"], out["probs"], out["idx_used"],
+                         out["flag"], out["mass"], out["y"], out["xn"], ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    got = {n: v.cpu() for n, v in out.items()}
+    ref = oracle.router(x, layer["Wr"], layer["bias"], k)
+    label = f"layer_resident E512 T={T} thr={threshold}"
+    check_routing(ref, got, k, max_skip_frac=0.2, label=label)
+    # the rule on the GPU's own probabilities and routing: exact
+    sref = oracle.substitute(got["probs"].numpy(), got["idx"], got["w"].double(), mask.cpu(), threshold)
+    assert np.array_equal(got["flag"].numpy(), sref["flag"])
+    assert np.array_equal(got["idx_used"].numpy(), sref["idx"])
+    np.testing.assert_allclose(got["mass"].numpy(), sref["mass"], rtol=0, atol=1e-6)
+    # and end to end against the oracle's routing
+    parity.check_substitution(ref, mask.cpu().numpy(), threshold,
+                              dict(idx_used=got["idx_used"].numpy(), flag=got["flag"].numpy(),
+                                   mass=got["mass"].numpy()), label=label)
+    check_y(layer, x, dict(idx=got["idx_used"], w=got["w"], y=got["y"]), cfg.qbits)
+    assert torch.equal(got["xn"], (x.cpu().float() + got["y"]).to(x.dtype))
+
+
+# ------------------------------------------------------- stacked layers
+
+@pytest.mark.parametrize("cfg_id", [1, 3])
+def test_layer_stack_chain_matches_oracle(cfg_id):
+    """Three layers in one launch, chained through x_next: each layer is
+    checked against the oracle evaluated on the input that layer actually
+    received (the previous layer's x_next), and y against the oracle on the
+    GPU's routing."""
+    cfg = W.CONFIGS[cfg_id]
+    L = 3
+    layers = [W.make_layer(cfg, l, DEV, chunk=64) for l in range(L)]
+    routers = [M.Router(lw["Wr"], lw["bias"], cfg.k) for lw in layers]
+    experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
+    x0 = W.make_tokens(cfg, 1, 31, DEV)
+    idx = [torch.empty(1, cfg.k, dtype=torch.int32, device=DEV) for _ in range(L)]
+    w = [torch.empty(1, cfg.k, device=DEV) for _ in range(L)]
+    y = [torch.empty(1, cfg.D, device=DEV) for _ in range(L)]
+    xn = [torch.empty_like(x0) for _ in range(L)]
+    ws = M.workspace(M.MOE_OP_LAYER, 1, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
+    xs = [x0] + [None] * (L - 1)
+    M.moe_layer_stack(routers, experts, [x0] * L, True, idx, w, y, xn, ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    x_in = x0
+    for l in range(L):
+        ref = oracle.router(x_in, layers[l]["Wr"], layers[l]["bias"], cfg.k)
+        got = dict(idx=idx[l].cpu(), w=w[l].cpu(), y=y[l].cpu())
+        check_routing(ref, got, cfg.k, max_skip_frac=1.0, label=f"stack chain cfg{cfg_id} layer {l}")
+        check_y(layers[l], x_in, got, cfg.qbits)
+        assert torch.equal(xn[l].cpu(), (x_in.cpu().float() + got["y"]).to(x0.dtype))
+        x_in = xn[l]
+    del xs
+
+
+def test_layer_stack_independent_equals_single_layers(cfg1_layers):
+    """Independent inputs: a stack launch gives bit-identical results to one
+    moe_layer call per layer."""
+    cfg, layers = cfg1_layers
+    L = len(layers)
+    routers = [M.Router(lw["Wr"], lw["bias"], cfg.k) for lw in layers]
+    experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
+    xs = [W.make_tokens(cfg, 1, 40 + l, DEV) for l in range(L)]
+    idx = [torch.empty(1, cfg.k, dtype=torch.int32, device=DEV) for _ in range(L)]
+    w = [torch.empty(1, cfg.k, device=DEV) for _ in range(L)]
+    y = [torch.empty(1, cfg.D, device=DEV) for _ in range(L)]
+    ws = M.workspace(M.MOE_OP_LAYER, 1, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_layer_stack(routers, experts, xs, False, idx, w, y, None, ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    for l in range(L):
+        one = gpu_layer(cfg, layers[l], xs[l], probs=False)
+        assert torch.equal(one["idx"], idx[l].cpu()) and torch.equal(one["w"], w[l].cpu())
+        assert torch.equal(one["y"], y[l].cpu())
+
+
+# ------------------------------------------------------ bounded waits
+
+def test_wait_limit_runs_out_and_the_workspace_recovers():
+    """A wait limit of a few cycles makes the layer kernel's cross-CTA waits
+    run out: the call must finish, record MOE_ERR_DEVICE_TIMEOUT, and the same
+    workspace must give correct results once the limit is restored."""
+    cfg = small_cfg(256, 8, 2048, 768, cfg_id=95)
+    layer = W.make_layer(cfg, 0, DEV, chunk=64)
+    router = M.Router(layer["Wr"], layer["bias"], cfg.k)
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    ws = M.workspace(M.MOE_OP_LAYER, 1, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
+    x = W.make_tokens(cfg, 1, 5, DEV)
+    idx = torch.empty(1, cfg.k, dtype=torch.int32, device=DEV)
+    w = torch.empty(1, cfg.k, device=DEV)
+    y = torch.empty(1, cfg.D, device=DEV)
+    M.moe_set_wait_limit(ws, 16)
+    M.moe_layer(router, experts, x, idx, w, None, y, None, ws)
+    assert M.moe_check_status(ws) == M.MOE_ERR_DEVICE_TIMEOUT
+    assert M.moe_check_status(ws) == M.MOE_OK  # cleared by the read
+    M.moe_set_wait_limit(ws, 0)
+    got = gpu_layer(cfg, layer, x)
+    M.moe_layer(router, experts, x, idx, w, None, y, None, ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    assert torch.equal(idx.cpu(), got["idx"]) and torch.equal(y.cpu(), got["y"])
+    ref = oracle.router(x, layer["Wr"], layer["bias"], cfg.k)
+    check_routing(ref, dict(idx=idx.cpu(), w=w.cpu()), cfg.k, max_skip_frac=1.0, label="after a timeout")
+    check_y(layer, x, dict(idx=idx.cpu(), w=w.cpu(), y=y.cpu()), cfg.qbits)
 
 
 # ------------------------------------------------------------- edge cases

@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -39,6 +40,10 @@ def _run_pair(cfg, layer, stream_ids):
         err = np.abs(got["y"].double().cpu().numpy() - y_ref).max()
         assert err <= REL_TOL * np.abs(y_ref).max(), f"max |y_noalloc - y| = {err:.3e}"
         assert torch.equal(got["xn"], (x.float() + got["y"]).to(x.dtype))
+        # and directly against the oracle, on the routing this entry point chose
+        y_or = oracle.moe(layer, x, got["idx"].cpu(), got["w"].cpu().double(), cfg.qbits)
+        err_or = np.abs(got["y"].double().cpu().numpy() - y_or).max()
+        assert err_or <= REL_TOL * np.abs(y_or).max(), f"max |y_noalloc - oracle| = {err_or:.3e}"
 
 
 def test_noalloc_matches_workspace_layer_e256():
@@ -52,6 +57,7 @@ def test_noalloc_matches_workspace_layer_int4_e512():
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
+    """k*F beyond the static scratch is refused before anything is launched."""
     import moe_routed_expert_route_gb300 as M
     cfg = W.LayerConfig("big", E=8, k=8, D=64, F=8192, T=1, qbits=8, scale_dtype=torch.float16,
                         x_dtype=torch.bfloat16, router_dtype=torch.bfloat16, router_sigma=0.1,
