@@ -1,19 +1,28 @@
 """Benchmark of the routed-expert MoE layer on one GB300 (sm_103a).
 
-Default workload: decode of one token through 40 stacked independent MoE layers
-of 256 experts, top-8, d_model 2048, d_ff 768 (Qwen3.6-35B-A3B-shaped), int8
-symmetric per-block-32 weights with fp16 scales, bf16 activations, Zipf(1.1)
-router bias. One step = router GEMV + fp32 softmax + top-k + gathered gate/up +
-SwiGLU + per-slot down + weighted combine + residual, for all 40 layers. The
-layers are independent: in each step every layer takes its own token, drawn
-from a device-resident bank of distinct seeded tokens (data="synthetic").
+Headline workload: decode of one token through 40 stacked independent MoE
+layers of 256 experts, top-8, d_model 2048, d_ff 768 (Qwen3.6-35B-A3B-shaped),
+int8 symmetric per-block-32 weights with fp16 scales, bf16 activations,
+Zipf(1.1) router bias. One step = router GEMV + fp32 softmax + top-k +
+gathered gate/up + SwiGLU + per-slot down + weighted combine + residual, for
+all 40 layers, in one launch of the stacked single-token layer kernel: layer
+l+1 starts only after every CTA has finished layer l. Every layer takes its own
+token, drawn from a device-resident bank of distinct seeded tokens
+(data="synthetic").
+
+The same run also measures, under "workloads", the other configurations on
+the same resident weights: the batched decode sweep (T = 1..64), residency
+substitution with int4 experts (T = 1, 16) and prefill (T = 2048, 16384), each
+with its roofline, the CPU oracle's rate on a bounded sample, and the clocks
+seen while it ran.
 
 Prints ONE JSON line (rank 0). With --impl reference the CPU oracle is timed on
-a bounded sample of the same workload instead.
+a bounded sample of the headline workload instead.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -28,24 +37,32 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-# DRAM bytes (read + write) of one launch of the single-token layer kernel on
-# the default workload: dram__bytes_read.sum + dram__bytes_write.sum from one
-# ncu capture of that launch
-LAYER_KERNEL_DRAM_BYTES = 41_244_928 + 5_120
-
 import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer decode tokens/s and routed-expert HBM GB/s (% of GB300 peak), 1 GPU"
 L2_BYTES = 129 * 1024 * 1024
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# single-token layer kernel on one layer of the headline workload, from the ncu
+# capture summarised in the named file. Reported only while the kernel source
+# is the one that capture measured (same sha256 prefix of csrc/fused.cu).
+LAYER_KERNEL_TRAFFIC = {"fused_sha16": None, "bytes_per_layer": None,
+                        "source": "profiles/fused_layer_kernel_decode_E256_k8.md"}
+
+
+def fused_sha16() -> str:
+    p = os.path.join(ROOT, "moe_routed_expert_route_gb300", "csrc", "fused.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained") or 0) or None,
+                "measured")
     except Exception:
-        return 6800.0, 1900.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 class ClockSampler:
@@ -64,7 +81,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "500", "-i", str(self.index)],
+                 "-lms", "200", "-i", str(self.index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -104,19 +121,28 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def roofline(bound, achieved, peak, unit, kernel, extra=None):
+    d = {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+         "frac": round(achieved / peak, 4)}
+    if extra:
+        d.update(extra)
+    return d
+
+
 # ------------------------------------------------------------------ decode
 
 class DecodeStack:
-    """40 layers resident in HBM; per step every layer decodes its own token."""
+    """`layers` layers resident in HBM; per step every layer decodes its own
+    token batch. T = 1 runs the whole stack in one launch of the stacked
+    single-token layer kernel; T > 1 runs one moe_layer call per layer."""
 
-    def __init__(self, cfg: W.LayerConfig, dev, T: int = 1, layers: int = None):
+    def __init__(self, cfg: W.LayerConfig, dev, T: int = 1, layers: int = None, layer_weights=None):
         import moe_routed_expert_route_gb300 as M
         self.M = M
         self.cfg = cfg
-        self.T = T
         self.L = layers or cfg.layers
         self.dev = dev
-        self.layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(self.L)]
+        self.layers = layer_weights or [W.make_layer(cfg, l, dev, chunk=64) for l in range(self.L)]
         self.routers = [M.Router(lw["Wr"], lw["bias"], cfg.k) for lw in self.layers]
         self.experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in self.layers]
         self._buffers(T)
@@ -149,6 +175,10 @@ class DecodeStack:
         if from_bank:
             torch.index_select(self.bank, 0, self.ctr, out=self.XIN.view(1, self.L, self.T, -1))
             self.ctr.add_(1).remainder_(self.NB)
+        if self.T == 1:
+            M.moe_layer_stack(self.routers, self.experts, [self.XIN[l] for l in range(self.L)], False, self.idx,
+                              self.w, self.y, [self.XN[l] for l in range(self.L)], self.ws)
+            return
         for l in range(self.L):
             M.moe_layer(self.routers[l], self.experts[l], self.XIN[l], self.idx[l], self.w[l], None,
                         self.y[l], self.XN[l], self.ws)
@@ -168,21 +198,24 @@ class DecodeStack:
         return g
 
     def kernels_per_step(self):
-        return self.L  # one persistent layer launch per layer at T = 1
+        if self.T == 1:
+            return 1  # one launch of the stacked layer kernel
+        if self.T <= 3:
+            return self.L * self.T
+        return self.L * 8  # router GEMM, top-k, grouping (3), gather, two grouped products, combine
+
+    def unions(self):
+        return [int(torch.unique(self.idx[l]).numel()) for l in range(self.L)]
 
     def routed_bytes_per_step(self):
         """Algorithmic bytes: codes + scales of the distinct routed experts."""
-        per_expert = W.routed_bytes_per_expert(self.cfg)
-        total = 0
-        for l in range(self.L):
-            total += int(torch.unique(self.idx[l]).numel()) * per_expert
-        return total
+        return sum(self.unions()) * W.routed_bytes_per_expert(self.cfg)
 
 
-def time_graph(stack, stream, steps, warmup, world):
+def time_graph(graph, stream, steps, warmup, world=1, dev=None):
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            stack.graph.replay()
+            graph.replay()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -192,12 +225,12 @@ def time_graph(stack, stream, steps, warmup, world):
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps):
-            stack.graph.replay()
+            graph.replay()
         end.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
     if world > 1:
-        ms = max_over_ranks(ms, stack.dev)
+        ms = max_over_ranks(ms, dev)
     return ms
 
 
@@ -243,25 +276,307 @@ def time_e2e(stack, stream, steps, warmup):
     return (t1 - t0) * 1e3, h2d, d2h
 
 
-def cpu_baseline_decode(stack, budget_s=15.0):
-    """The oracle, as it stands, on the GB300 host's cores: tokens through all
-    layers, as many as fit in about `budget_s` seconds (at least one)."""
+# ---------------------------------------------------- CPU oracle baselines
+# The oracle as it stands, on this host's cores, on a bounded sample of each
+# workload (the same seeded inputs as the GPU measurement).
+
+def _host_layer(lw):
+    return (lw["Wr"].cpu(), lw["bias"].cpu() if lw["bias"] is not None else None)
+
+
+def oracle_decode_rate(cfg, layers, ntok: int, threads: int, warmup: int = 1):
+    """Tokens/s of the oracle (router + routed experts) for ntok tokens, each
+    through every layer, after `warmup` tokens."""
     import oracle
-    cfg = stack.cfg
-    nth = os.cpu_count() or 1
-    host = [(lw["Wr"].cpu(), lw["bias"].cpu() if lw["bias"] is not None else None) for lw in stack.layers]
-    xs = W.make_tokens(cfg, stack.T * stack.L, 9, "cpu").double().numpy().reshape(stack.L, stack.T, -1)
-    tokens = 0
+    host = [_host_layer(lw) for lw in layers]
+    L = len(layers)
+    xs = W.make_tokens(cfg, (ntok + warmup) * L, 9, "cpu").double().numpy().reshape(ntok + warmup, L, 1, -1)
+
+    def token(i):
+        for l in range(L):
+            r = oracle.router(xs[i, l], host[l][0], host[l][1], cfg.k)
+            oracle.moe(layers[l], xs[i, l], r["idx"], r["w"], cfg.qbits, nthreads=threads)
+
+    for i in range(warmup):
+        token(i)
     t0 = time.perf_counter()
-    while True:
-        for l in range(stack.L):  # independent layers, each with its own token batch
-            r = oracle.router(xs[l], host[l][0], host[l][1], cfg.k)
-            oracle.moe(stack.layers[l], xs[l], r["idx"], r["w"], cfg.qbits, nthreads=nth)
-        tokens += stack.T
-        el = time.perf_counter() - t0
-        if el >= budget_s or tokens >= 64:
-            break
-    return tokens / el, nth, f"{tokens} token(s) x {stack.L} layers (router + routed experts), {el:.1f} s"
+    for i in range(warmup, warmup + ntok):
+        token(i)
+    el = time.perf_counter() - t0
+    return ntok / el, el
+
+
+def cpu_baseline_decode(cfg, layers, ntok=8, single=True):
+    nth = os.cpu_count() or 1
+    v, el = oracle_decode_rate(cfg, layers, ntok, nth)
+    out = {"value": round(v, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
+           "sample": f"{ntok} tokens x {len(layers)} layers (router + routed experts, fp64) after 1 warm-up "
+                     f"token, {el:.1f} s"}
+    if single:
+        v1, el1 = oracle_decode_rate(cfg, layers, 1, 1, warmup=0)
+        out["single_thread"] = {"value": round(v1, 4), "unit": "tokens/s", "cores": 1,
+                                "sample": f"1 token x {len(layers)} layers, {el1:.1f} s"}
+    return out
+
+
+# ------------------------------------------------------------ workloads
+
+def run_headline(args, dev, world, rank):
+    cfg = W.CONFIGS[1]
+    stack = DecodeStack(cfg, dev, T=1, layers=args.layers)
+    stream = torch.cuda.Stream(dev)
+    stack.capture(stream)
+    steps, warmup = args.steps, max(3, args.warmup)
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        ms = time_graph(stack.graph, stream, steps, warmup, world, dev)
+    status = stack.M.moe_check_status(stack.ws)
+    assert status == 0, f"device status {status}"
+    ms_step = ms / steps
+    tok_s = job_throughput(stack.T * steps, world, ms)
+    routed = stack.routed_bytes_per_step()
+    hbm_peak, tf_peak, tf_sus, peak_kind = peaks()
+    layer_us = ms_step * 1e3 / stack.L
+    per_layer_bytes = routed / stack.L
+    achieved = per_layer_bytes / (layer_us * 1e-6) / 1e9
+    e2e_ms, h2d, d2h = time_e2e(stack, stream, min(steps, 2000), warmup)
+    e2e = world * stack.T * min(steps, 2000) / (e2e_ms / 1e3)
+    same = LAYER_KERNEL_TRAFFIC["fused_sha16"] == fused_sha16()
+    traffic = LAYER_KERNEL_TRAFFIC["bytes_per_layer"] if same else None
+    line = {
+        "metric": METRIC,
+        "value": round(tok_s, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8/fp16-scale weights x bf16 activations; dots on 16-bit block fixed-point activations "
+                 "(int32 exact), fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": f"decode: 1 token x {stack.L} layers, E=256 top-8 D=2048 F=768, int8 sym "
+                               "blk32 fp16 scales, bf16 x, Zipf(1.1) router bias",
+                   "T": stack.T, "layers": stack.L, "E": cfg.E, "k": cfg.k, "D": cfg.D, "F": cfg.F,
+                   "routed_bytes_per_token": routed // stack.T,
+                   "routed_gbs": round(routed / (ms_step * 1e-3) / 1e9, 1),
+                   "l2": f"no flush: {routed / 1e9:.2f} GB of distinct weights per step > "
+                         f"{L2_BYTES / 2**20:.0f} MiB L2",
+                   "inputs": "independent layers: each layer decodes its own bank token every step; layer l+1 "
+                             "starts after every CTA finished layer l",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "graph": "one CUDA graph per step: token gather + one launch of the stacked layer kernel"},
+        "roofline": roofline("hbm", achieved, hbm_peak, "GB/s",
+                             "fused_layer_kernel (one launch = the whole 40-layer stack)",
+                             {"peak_kind": peak_kind, "per_layer_bytes": int(per_layer_bytes),
+                              "per_layer_us": round(layer_us, 3), "per_launch_bytes": int(routed),
+                              "per_launch_us": round(ms_step * 1e3, 2),
+                              "traffic": None if traffic is None else traffic * stack.L,
+                              "traffic_unit": "DRAM bytes per launch",
+                              "traffic_source": LAYER_KERNEL_TRAFFIC["source"] if same else
+                              "no ncu capture of this kernel version"}),
+        "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": stack.kernels_per_step() * steps,
+        "clocks": clk.summary(),
+    }
+    return line, stack, stream
+
+
+def run_batched(args, dev, stack):
+    """Batched decode over the same 40-layer stack, T in {1,...,64}."""
+    cfg = W.CONFIGS[2]
+    per_expert = W.routed_bytes_per_expert(cfg)
+    hbm, _, _, kind = peaks()
+    pts = []
+    with ClockSampler(0) as clk:
+        for T in (1, 2, 4, 8, 16, 32, 64):
+            st = DecodeStack(cfg, dev, T=T, layers=stack.L, layer_weights=stack.layers)
+            stream = torch.cuda.Stream(dev)
+            st.capture(stream)
+            steps = max(10, args.steps // 4)
+            ms = time_graph(st.graph, stream, steps, max(3, args.warmup)) / steps
+            U = st.unions()
+            routed = sum(U) * per_expert
+            gbs = routed / (ms * 1e-3) / 1e9
+            pts.append({"T": T, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+                        "union_experts_mean": round(sum(U) / len(U), 2), "union_min": min(U), "union_max": max(U),
+                        "routed_gbs": round(gbs, 1),
+                        "roofline": roofline("hbm", gbs, hbm, "GB/s",
+                                             "stacked layer kernel" if T == 1 else
+                                             ("single-token layer kernel per token" if T <= 3 else
+                                              "grouped tensor-core products"), {"peak_kind": kind})})
+            s = st.M.moe_check_status(st.ws)
+            assert s == 0, f"T={T}: device status {s}"
+            del st
+    torch.cuda.synchronize()
+    nth = os.cpu_count() or 1
+    v, el = oracle_decode_rate(cfg, stack.layers, 8, nth)
+    return {"workload": f"batched decode sweep, {stack.L} layers E=256 top-8 D=2048 F=768 int8, T = 1..64",
+            "unit": "tokens/s", "points": pts,
+            "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                             "sample": f"8 tokens x {stack.L} layers ({el:.1f} s); the oracle's cost per token "
+                                       "does not depend on the batch"},
+            "clocks": clk.summary()}
+
+
+def run_substitution(args, dev):
+    """Residency substitution (0.15 rule) + int4 experts, 512 experts top-10, 16 layers."""
+    import moe_routed_expert_route_gb300 as M
+    import oracle
+    cfg = W.CONFIGS[3]
+    L = cfg.layers if args.layers is None else min(args.layers, cfg.layers)
+    layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(L)]
+    masks = [W.make_resident_mask(cfg, l, dev) for l in range(L)]
+    per_expert = W.routed_bytes_per_expert(cfg)
+    hbm, _, _, kind = peaks()
+    k = cfg.k
+    routers = [M.Router(lw["Wr"], lw["bias"], k) for lw in layers]
+    experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
+    res = []
+    with ClockSampler(0) as clk:
+        for T in (1, 16):
+            XIN = torch.empty(L, T, cfg.D, dtype=cfg.x_dtype, device=dev)
+            XN = torch.empty(L, T, cfg.D, dtype=cfg.x_dtype, device=dev)
+            bufs = [dict(idx=torch.empty(T, k, dtype=torch.int32, device=dev), w=torch.empty(T, k, device=dev),
+                         used=torch.empty(T, k, dtype=torch.int32, device=dev),
+                         flag=torch.empty(T, k, dtype=torch.uint8, device=dev),
+                         mass=torch.empty(T, device=dev), y=torch.empty(T, cfg.D, device=dev)) for _ in range(L)]
+            ws = M.workspace(M.MOE_OP_LAYER_RESIDENT, T, k, cfg.E, cfg.D, cfg.F, dev)
+            NB = 16 if T > 8 else 64
+            bank = W.make_tokens(cfg, NB * L * T, 1, dev).reshape(NB, L, T, cfg.D)
+            ctr = torch.zeros(1, dtype=torch.long, device=dev)
+            torch.cuda.synchronize()
+
+            def step():
+                torch.index_select(bank, 0, ctr, out=XIN.view(1, L, T, -1))
+                ctr.add_(1).remainder_(NB)
+                for l in range(L):
+                    b = bufs[l]
+                    M.moe_layer_resident(routers[l], experts[l], XIN[l], masks[l], cfg.threshold, b["idx"], b["w"],
+                                         None, b["used"], b["flag"], b["mass"], b["y"], XN[l], ws)
+
+            stream = torch.cuda.Stream(dev)
+            with torch.cuda.stream(stream):
+                step()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            steps = max(10, args.steps // 4)
+            ms = time_graph(g, stream, steps, max(3, args.warmup)) / steps
+            U = [int(torch.unique(bufs[l]["used"]).numel()) for l in range(L)]
+            flags = torch.stack([b["flag"] for b in bufs]).cpu()
+            mass = torch.stack([b["mass"] for b in bufs]).cpu()
+            gbs = sum(U) * per_expert / (ms * 1e-3) / 1e9
+            res.append({"T": T, "layers": L, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+                        "us_per_layer": round(ms * 1e3 / L, 2), "distinct_experts_mean": round(sum(U) / L, 2),
+                        "routed_gbs": round(gbs, 1),
+                        "roofline": roofline("hbm", gbs, hbm, "GB/s",
+                                             "single-token layer kernel with substitution" if T == 1 else
+                                             "router GEMM + substitution + grouped tensor-core products",
+                                             {"peak_kind": kind}),
+                        "substituted_frac": round(float((flags == 2).float().mean()), 4),
+                        "fetched_miss_frac": round(float((flags == 1).float().mean()), 4),
+                        "mass_mean": round(float(mass.mean()), 4), "mass_max": round(float(mass.max()), 4)})
+            assert M.moe_check_status(ws) == 0
+            del g, bufs, bank
+    # oracle: router + substitution + routed experts, a sample of tokens through all layers
+    nth = os.cpu_count() or 1
+    host = [_host_layer(lw) for lw in layers]
+    hmask = [m.cpu() for m in masks]
+    ntok = 4
+    xs = W.make_tokens(cfg, (ntok + 1) * L, 9, "cpu").double().numpy().reshape(ntok + 1, L, 1, -1)
+
+    def token(i):
+        for l in range(L):
+            r = oracle.router(xs[i, l], host[l][0], host[l][1], k)
+            s = oracle.substitute(r["probs32"], r["idx"], r["w"], hmask[l], cfg.threshold)
+            oracle.moe(layers[l], xs[i, l], s["idx"], s["w"], cfg.qbits, nthreads=nth)
+
+    token(0)
+    t0 = time.perf_counter()
+    for i in range(1, ntok + 1):
+        token(i)
+    el = time.perf_counter() - t0
+    del layers
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {"workload": f"substitution 0.15 rule + int4 experts, E=512 top-10 D=2048 F=512, 25% resident, "
+                        f"{L} layers", "unit": "tokens/s", "points": res,
+            "cpu_baseline": {"value": round(ntok / el, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                             "sample": f"{ntok} tokens x {L} layers (router + substitution + routed experts) after "
+                                       f"1 warm-up token, {el:.1f} s"},
+            "clocks": clk.summary()}
+
+
+def run_prefill(args, dev, stack, T):
+    """Prefill of T tokens on the decode layer shape, rotating over 4 layers
+    of the resident stack (5 GB of weights)."""
+    import moe_routed_expert_route_gb300 as M
+    import oracle
+    cfg = W.CONFIGS[4]
+    L = min(4, stack.L)
+    layers = stack.layers[:L]
+    routers = stack.routers[:L]
+    experts = stack.experts[:L]
+    x = W.make_tokens(cfg, T, 0, dev)
+    y = torch.empty(T, cfg.D, device=dev)
+    idx = torch.empty(T, cfg.k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, cfg.k, device=dev)
+    counts = torch.empty(L, cfg.E, dtype=torch.int32, device=dev)
+    ws = M.workspace(M.MOE_OP_PREFILL, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(dev)
+
+    def step(l):
+        M.moe_prefill(routers[l], experts[l], x, y, idx, w, counts[l], None, ws)
+
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            step(l)
+    torch.cuda.synchronize()
+    U = [int((counts[l] > 0).sum()) for l in range(L)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for l in range(L):
+            step(l)
+    hbm, tf, tf_sus, kind = peaks()
+    with ClockSampler(0) as clk:
+        steps = max(5, args.steps // 40)
+        ms = time_graph(g, stream, steps, max(3, args.warmup)) / steps / L
+    flops = 2.0 * T * cfg.k * 3 * cfg.D * cfg.F
+    wbytes = (sum(U) / L) * W.routed_bytes_per_expert(cfg)
+    assert M.moe_check_status(ws) == 0
+    tfs = flops / (ms * 1e-3) / 1e12
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    tensor_frac, hbm_frac = tfs / tf, gbs / hbm
+    # oracle on a sample of the same tokens (one layer)
+    nth = os.cpu_count() or 1
+    ns = 32
+    xs = x[:ns].cpu()
+    t0 = time.perf_counter()
+    r = oracle.router(xs, layers[0]["Wr"].cpu(), layers[0]["bias"].cpu(), cfg.k)
+    oracle.moe(layers[0], xs, r["idx"], r["w"], cfg.qbits, nthreads=nth)
+    el = time.perf_counter() - t0
+    del ws
+    torch.cuda.empty_cache()
+    return {"workload": f"prefill T={T} E=256 top-8 D=2048 F=768 int8 (fp16 tensor-core operands)",
+            "T": T, "unit": "tokens/s", "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_layer": round(ms, 4),
+            "distinct_experts_mean": round(sum(U) / L, 1), "expert_weight_gb": round(wbytes / 1e9, 3),
+            "expert_tflops": round(tfs, 1), "weight_gbs": round(gbs, 1),
+            "roofline": roofline("tensor" if tensor_frac >= hbm_frac else "hbm",
+                                 tfs if tensor_frac >= hbm_frac else gbs,
+                                 tf if tensor_frac >= hbm_frac else hbm,
+                                 "TFLOP/s" if tensor_frac >= hbm_frac else "GB/s",
+                                 "router GEMM + grouping + two grouped tensor-core products + combine",
+                                 {"peak_kind": kind, "tensor_frac_of_bf16_peak": round(tensor_frac, 4),
+                                  "hbm_frac_of_weights": round(hbm_frac, 4),
+                                  "note": "fp16 operands: the bf16 peak applies (same nominal rate)"}),
+            "cpu_baseline": {"value": round(ns / el, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                             "sample": f"{ns} of the {T} tokens through one layer, {el:.1f} s"},
+            "clocks": clk.summary()}
 
 
 def run_ours(args):
@@ -274,230 +589,28 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     import __graft_entry__
     __graft_entry__.build()
-    cfg = W.CONFIGS[1]
-    stack = DecodeStack(cfg, dev, T=1, layers=args.layers)
-    stream = torch.cuda.Stream(dev)
-    stack.capture(stream)
-    steps, warmup = args.steps, max(3, args.warmup)
-    with ClockSampler(local) as clk:
-        ms = time_graph(stack, stream, steps, warmup, world)
-    status = stack.M.moe_check_status(stack.ws)
-    assert status == 0, f"device status {status}"
-    ms_step = ms / steps
-    tok_s = job_throughput(stack.T * steps, world, ms)
-    routed = stack.routed_bytes_per_step()
-    hbm_peak, tf_peak, peak_kind = peaks()
-    layer_us = ms_step * 1e3 / stack.L
-    per_layer_bytes = routed / stack.L
-    achieved = per_layer_bytes / (layer_us * 1e-6) / 1e9
-    e2e_ms, h2d, d2h = time_e2e(stack, stream, min(steps, 2000), warmup)
-    e2e = world * stack.T * min(steps, 2000) / (e2e_ms / 1e3)
-    line = {
-        "metric": METRIC,
-        "value": round(tok_s, 2),
-        "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": steps,
-        "warmup": warmup,
-        "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "int8 weights x bf16 activations, int32/fp32 accumulate",
-        "data": "synthetic",
-        "config": {"workload": f"decode: 1 token x {stack.L} layers, E=256 top-8 D=2048 F=768, int8 sym "
-                               "blk32 fp16 scales, bf16 x, Zipf(1.1) router bias",
-                   "T": stack.T, "layers": stack.L, "E": cfg.E, "k": cfg.k, "D": cfg.D, "F": cfg.F,
-                   "routed_bytes_per_token": routed // stack.T,
-                   "routed_gbs": round(routed / (ms_step * 1e-3) / 1e9, 1),
-                   "l2": f"no flush: {routed / 1e9:.2f} GB of distinct weights per step > "
-                         f"{L2_BYTES / 2**20:.0f} MiB L2",
-                   "inputs": "independent layers: each layer decodes its own bank token every step",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "graph": "one CUDA graph per step, programmatic dependent launch between kernels"},
-        "roofline": {"bound": "hbm", "kernel": "fused_layer_kernel (one launch = one whole layer)",
-                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
-                     "per_launch_bytes": int(per_layer_bytes), "per_launch_us": round(layer_us, 3),
-                     # measured DRAM bytes of one launch of this kernel, per launch like achieved
-                     "traffic": LAYER_KERNEL_DRAM_BYTES, "traffic_unit": "bytes per launch"},
-        "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": stack.kernels_per_step() * steps,
-        "clocks": clk.summary(),
-    }
+    line, stack, stream = run_headline(args, dev, world, rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, sample = cpu_baseline_decode(stack, args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": "tokens/s", "cores": cores,
-                                "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = cpu_baseline_decode(W.CONFIGS[1], stack.layers, ntok=8)
+    if world == 1 and not args.headline_only:
+        extra = {}
+        extra["batched_decode"] = run_batched(args, dev, stack)
+        extra["prefill_T2048"] = run_prefill(args, dev, stack, 2048)
+        extra["prefill_T16384"] = run_prefill(args, dev, stack, 16384)
+        del stack
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        extra["substitution"] = run_substitution(args, dev)
+        line["workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-# ------------------------------------------------- secondary workloads
-# (measured on request with --workload; the default line is the decode step)
-
-def _time_graph_simple(g, stream, steps, warmup):
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps
-
-
-def run_batched(args, dev):
-    """Batched decode over the 40-layer stack, T in {1,...,64}."""
-    cfg = W.CONFIGS[2]
-    per_expert = W.routed_bytes_per_expert(cfg)
-    out = []
-    stack = None
-    for T in (1, 2, 4, 8, 16, 32, 64):
-        if stack is None:
-            stack = DecodeStack(cfg, dev, T=T, layers=args.layers)
-        else:  # same weights, new token batch
-            stack._buffers(T)
-            torch.cuda.synchronize()
-        stream = torch.cuda.Stream(dev)
-        stack.capture(stream)
-        ms = _time_graph_simple(stack.graph, stream, max(10, args.steps // 4), max(3, args.warmup))
-        U = [int(torch.unique(stack.idx[l]).numel()) for l in range(stack.L)]
-        routed = sum(U) * per_expert
-        out.append({"T": T, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
-                    "union_experts_mean": round(sum(U) / len(U), 2), "union_min": min(U), "union_max": max(U),
-                    "routed_gbs": round(routed / (ms * 1e-3) / 1e9, 1)})
-        st = stack.M.moe_check_status(stack.ws)
-        assert st == 0, f"T={T}: device status {st} ({stack.M.status_string(st)})"
-    return {"workload": "batched decode sweep, 40 layers E=256 top-8 D=2048 F=768 int8", "points": out}
-
-
-def run_substitution(args, dev):
-    """Residency substitution (0.15 rule) + int4 decode, 512 experts top-10, 16 layers."""
-    import moe_routed_expert_route_gb300 as M
-    cfg = W.CONFIGS[3]
-    L = args.layers or cfg.layers
-    layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(L)]
-    masks = [W.make_resident_mask(cfg, l, dev) for l in range(L)]
-    per_expert = W.routed_bytes_per_expert(cfg)
-    res = []
-    for T in (1, 16):
-        k = cfg.k
-        # independent layers: each takes its own token batch from a device bank
-        XIN = torch.empty(L, T, cfg.D, dtype=cfg.x_dtype, device=dev)
-        XN = torch.empty(L, T, cfg.D, dtype=cfg.x_dtype, device=dev)
-        bufs = [dict(idx=torch.empty(T, k, dtype=torch.int32, device=dev), w=torch.empty(T, k, device=dev),
-                     probs=torch.empty(T, cfg.E, device=dev), idx2=torch.empty(T, k, dtype=torch.int32, device=dev),
-                     w2=torch.empty(T, k, device=dev), flag=torch.empty(T, k, dtype=torch.uint8, device=dev),
-                     mass=torch.empty(T, device=dev), y=torch.empty(T, cfg.D, device=dev)) for _ in range(L)]
-        ws_r = M.workspace(M.MOE_OP_ROUTE, T, k, cfg.E, cfg.D, cfg.F, dev)
-        ws_d = M.workspace(M.MOE_OP_DECODE, T, k, cfg.E, cfg.D, cfg.F, dev)
-        routers = [M.Router(lw["Wr"], lw["bias"], k) for lw in layers]
-        experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
-        NB = 16 if T > 8 else 64
-        bank = W.make_tokens(cfg, NB * L * T, 1, dev).reshape(NB, L, T, cfg.D)
-        ctr = torch.zeros(1, dtype=torch.long, device=dev)
-        torch.cuda.synchronize()  # setup ran on the default stream; the steps run on another
-
-        def step():
-            torch.index_select(bank, 0, ctr, out=XIN.view(1, L, T, -1))
-            ctr.add_(1).remainder_(NB)
-            for l in range(L):
-                b = bufs[l]
-                M.moe_route(routers[l], XIN[l], b["idx"], b["w"], b["probs"], ws_r)
-                M.moe_substitute(b["probs"], b["idx"], b["w"], masks[l], cfg.threshold, b["idx2"], b["w2"],
-                                 b["flag"], b["mass"])
-                M.moe_decode(experts[l], XIN[l], b["idx2"], b["w2"], b["y"], XN[l], ws_d)
-
-        stream = torch.cuda.Stream(dev)
-        with torch.cuda.stream(stream):
-            step()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step()
-        ms = _time_graph_simple(g, stream, max(10, args.steps // 4), max(3, args.warmup))
-        U = [int(torch.unique(bufs[l]["idx2"]).numel()) for l in range(L)]
-        flags = torch.stack([b["flag"] for b in bufs]).cpu()
-        mass = torch.stack([b["mass"] for b in bufs]).cpu()
-        res.append({"T": T, "layers": L, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
-                    "us_per_layer": round(ms * 1e3 / L, 2), "distinct_experts_mean": round(sum(U) / L, 2),
-                    "routed_gbs": round(sum(U) * per_expert / (ms * 1e-3) / 1e9, 1),
-                    "substituted_frac": round(float((flags == 2).float().mean()), 4),
-                    "fetched_miss_frac": round(float((flags == 1).float().mean()), 4),
-                    "mass_mean": round(float(mass.mean()), 4), "mass_max": round(float(mass.max()), 4)})
-        assert M.moe_check_status(ws_d) == 0
-    return {"workload": "substitution 0.15 rule + int4 decode, E=512 top-10 D=2048 F=512, 25% resident",
-            "points": res}
-
-
-def run_prefill(args, dev, T=None):
-    """Prefill of T tokens (default 2048), rotating over 4 layers (5 GB of weights)."""
-    import moe_routed_expert_route_gb300 as M
-    cfg = W.CONFIGS[4]
-    T = T or cfg.T
-    L = args.layers or 4
-    layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(L)]
-    routers = [M.Router(lw["Wr"], lw["bias"], cfg.k) for lw in layers]
-    experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
-    x = W.make_tokens(cfg, T, 0, dev)
-    y = torch.empty(T, cfg.D, device=dev)
-    idx = torch.empty(T, cfg.k, dtype=torch.int32, device=dev)
-    w = torch.empty(T, cfg.k, device=dev)
-    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
-    ws = M.workspace(M.MOE_OP_PREFILL, T, cfg.k, cfg.E, cfg.D, cfg.F, dev)
-    torch.cuda.synchronize()  # setup ran on the default stream; the steps run on another
-    stream = torch.cuda.Stream(dev)
-
-    def step(l):
-        M.moe_prefill(routers[l], experts[l], x, y, idx, w, counts, None, ws)
-
-    with torch.cuda.stream(stream):
-        for l in range(L):
-            step(l)
-    torch.cuda.synchronize()
-    U = int((counts > 0).sum())
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for l in range(L):
-            step(l)
-    ms = _time_graph_simple(g, stream, max(5, args.steps // 40), max(3, args.warmup)) / L
-    flops = 2.0 * T * cfg.k * 3 * cfg.D * cfg.F
-    wbytes = U * W.routed_bytes_per_expert(cfg)
-    hbm, tf, kind = peaks()
-    assert M.moe_check_status(ws) == 0
-    return {"workload": f"prefill T={T} E=256 top-8 D=2048 F=768 int8 (fp16 tensor-core operands)",
-            "T": T, "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_layer": round(ms, 4),
-            "distinct_experts": U, "expert_weight_gb": round(wbytes / 1e9, 3),
-            "expert_tflops": round(flops / (ms * 1e-3) / 1e12, 1), "tensor_frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / tf, 4),
-            "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1), "weight_frac_of_hbm_peak": round(wbytes / (ms * 1e-3) / 1e9 / hbm, 4)}
-
-
-def run_workload(args):
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    import __graft_entry__
-    __graft_entry__.build()
-    if args.workload == "batched":
-        r = run_batched(args, dev)
-    elif args.workload == "substitution":
-        r = run_substitution(args, dev)
-    else:
-        r = run_prefill(args, dev)
-        if args.prefill_extra:
-            r["extra"] = run_prefill(args, dev, T=16384)
-    print(json.dumps(r), flush=True)
-
-
 def run_reference(args):
-    """The CPU oracle on a bounded sample of the same workload."""
+    """The CPU oracle on a bounded sample of the headline workload (the same
+    sample as the GPU arm's cpu_baseline)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -506,43 +619,21 @@ def run_reference(args):
     oracle.build()
     cfg = W.CONFIGS[1]
     L = args.layers or cfg.layers
-    nth = os.cpu_count() or 1
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     layers = [W.make_layer(cfg, l, dev, chunk=64) for l in range(L)]
-    host = [(lw["Wr"].cpu(), lw["bias"].cpu()) for lw in layers]
-    # independent layers, each with its own token, as in the GPU arm
-    xs = W.make_tokens(cfg, L, 0, "cpu").double().numpy().reshape(L, 1, -1)
-
-    def step(threads):
-        for l in range(L):
-            r = oracle.router(xs[l], host[l][0], host[l][1], cfg.k)
-            oracle.moe(layers[l], xs[l], r["idx"], r["w"], cfg.qbits, nthreads=threads)
-
-    for _ in range(max(0, min(args.warmup, 1))):
-        step(nth)
     steps = max(1, min(args.steps, 8))
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        step(nth)
-    el = time.perf_counter() - t0
-    t1 = time.perf_counter()
-    step(1)  # one step on one thread, for scale
-    el1 = time.perf_counter() - t1
-    v = steps / el
+    cb = cpu_baseline_decode(cfg, layers, ntok=steps)
+    v = cb["value"]
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tokens/s",
-        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3),
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": world, "steps": steps, "warmup": 1, "ms_per_step": round(1e3 / v, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"decode: 1 token x {L} layers, E=256 top-8 D=2048 F=768, int8 sym "
                                "blk32 fp16 scales, bf16 x, Zipf(1.1) router bias",
                    "inputs": "independent layers: each layer decodes its own token every step"},
-        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
-                         "sample": f"{steps} token(s) x {L} layers",
-                         "single_thread": {"value": round(1.0 / el1, 4), "unit": "tokens/s", "cores": 1,
-                                           "sample": f"1 token x {L} layers"}},
-        "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
@@ -553,17 +644,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--workload", default="decode", choices=["decode", "batched", "substitution", "prefill"],
-                    help="decode (default, the headline line) or a secondary workload")
-    ap.add_argument("--prefill-extra", action="store_true", help="also time a 16384-token prefill")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="only the 40-layer decode line (no batched / substitution / prefill workloads)")
     ap.add_argument("--layers", type=int, default=None,
                     help="stacked layers (default: the workload's 40); fewer only for profiling captures")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload != "decode":
-        run_workload(args)
     else:
         run_ours(args)
 

@@ -209,14 +209,14 @@ moe_status_t moe_layer_resident(const moe_router_t* router, const moe_experts_t*
  * scale and router dtypes and norm_topk.
  *   routers, experts   host arrays [nlayers] of descriptors
  *   x        host array [nlayers] of device pointers, each [D] in x_dtype.
- *            chain = 1: layer 0 reads x[0] and layer l > 0 reads x_next[l-1]
- *            (the residual stream; x[l > 0] is ignored). chain = 0: layer l
+ *            chain = 1: layer 0 reads x[0] and layer l > 0 reads layer l-1's
+ *            x + y (the residual stream; x[l > 0] is ignored). chain = 0: layer l
  *            reads x[l] (independent tokens), still after layer l-1 is done.
  *   idx, w   host arrays [nlayers] of device pointers to [k] outputs
  *   y        host array [nlayers] of device pointers to [D] fp32 outputs
  *   x_next   host array [nlayers] of device pointers to [D] outputs (x + y in
- *            x_dtype), entries may be NULL except where chain = 1 needs them
- *            (l < nlayers - 1); the whole array may be NULL when chain = 0
+ *            x_dtype) or NULL entries; the whole array may be NULL (chained
+ *            layers hand their output to the next layer through the workspace)
  * The host arrays are read during the call only. Workspace: MOE_OP_LAYER with
  * T = 1. Shapes the single-token kernel cannot run return MOE_ERR_UNSUPPORTED.
  */
@@ -246,7 +246,7 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
  * run a layer (a frozen or captured memory pool, a host runtime whose
  * allocator is out of reach, an embedding that hands over only its input and
  * output buffers). Its scratch is a static device array inside the library of
- * 147,712 bytes (header + E tagged logits + k*F activations + per-CTA flags),
+ * 270,592 bytes (header + E tagged logits + k*F tagged activations),
  * held by every GPU that loads the library until the process exits. Limits:
  * E <= 1024 and k*F <= 32768 (beyond them: MOE_ERR_WORKSPACE); router weights
  * in the dtype of x; shapes the single-token kernel cannot run (k > 32 among

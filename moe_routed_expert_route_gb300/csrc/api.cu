@@ -25,7 +25,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Workspace sections, in bytes from the start. 0 = section not used.
 struct Layout {
     size_t logits = 0, xq_hi = 0, xq_lo = 0, xq_s = 0, grp_expert = 0, grp_off = 0, assign = 0, h = 0;
-    size_t flags = 0;
+    size_t xex = 0;
     size_t total = 0;
 };
 
@@ -51,8 +51,8 @@ Layout layout(int op, int T, int k, int E, int D, int F) {
         L.assign = take(sizeof(int32_t) * (size_t)T * k);
         L.h = take(sizeof(uint64_t) * (size_t)T * k * F);
     }
-    // per-CTA completion flags of the single-token layer kernel
-    if (experts) L.flags = take(sizeof(unsigned) * 2 * kFusedMaxGrid);
+    // a layer's x_next as tagged words (stacked single-token layers)
+    if (experts) L.xex = take(sizeof(uint64_t) * (size_t)D);
     L.total = off;
     return L;
 }
@@ -197,8 +197,8 @@ FusedCommon fused_common(void* ws, const Layout& L) {
     f.nlayers = 1;
     f.hdr = at<WsHeader>(ws, 0);
     f.logits = L.logits ? at<uint64_t>(ws, L.logits) : nullptr;
-    f.h = at<float>(ws, L.h);
-    f.flags = at<unsigned>(ws, L.flags);
+    f.h = at<uint64_t>(ws, L.h);
+    f.xex = at<uint64_t>(ws, L.xex);
     return f;
 }
 
@@ -373,7 +373,7 @@ moe_status_t layer_impl(const moe_router_t* router, const moe_experts_t* experts
     st = check_experts(experts, x_dtype, router->k);
     if (st != MOE_OK) return st;
     if (router->E != experts->E || router->D != experts->D) return MOE_ERR_INVALID_ARG;
-    if (T < 1 || T > kMaxDecodeT || !al16(x) || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > kMaxDecodeT || !al16(x) || !idx || !w || !al16(y)) return MOE_ERR_INVALID_ARG;
     if (x_next && !al16(x_next)) return MOE_ERR_INVALID_ARG;
     const int k = router->k, E = experts->E, D = experts->D, F = experts->F;
     Layout L = layout(MOE_OP_LAYER, T, k, E, D, F);
@@ -514,7 +514,7 @@ moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t
                         void* workspace, size_t ws_bytes, void* stream) {
     moe_status_t st = check_experts(experts, x_dtype, k);
     if (st != MOE_OK) return st;
-    if (T < 1 || T > kMaxDecodeT || !al16(x) || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > kMaxDecodeT || !al16(x) || !idx || !w || !al16(y)) return MOE_ERR_INVALID_ARG;
     if (x_next && !al16(x_next)) return MOE_ERR_INVALID_ARG;
     Layout L = layout(MOE_OP_DECODE, T, k, experts->E, experts->D, experts->F);
     if (!workspace || ((uintptr_t)workspace & (kAlign - 1)) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
@@ -606,10 +606,9 @@ moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe
             (R.norm_topk != 0) != (R0.norm_topk != 0) || X.F != X0.F || X.q != X0.q || X.s_dtype != X0.s_dtype)
             return MOE_ERR_INVALID_ARG;
         if ((l == 0 || !chain) && !al16(x[l])) return MOE_ERR_INVALID_ARG;
-        if (!idx[l] || !w[l] || !y[l]) return MOE_ERR_INVALID_ARG;
+        if (!idx[l] || !w[l] || !al16(y[l])) return MOE_ERR_INVALID_ARG;
         void* xn = x_next ? x_next[l] : nullptr;
         if (xn && !al16(xn)) return MOE_ERR_INVALID_ARG;
-        if (chain && l + 1 < nlayers && !xn) return MOE_ERR_INVALID_ARG;  // the next layer's input
     }
     if ((R0.w_dtype == MOE_BF16) != (x_dtype == MOE_BF16)) return MOE_ERR_UNSUPPORTED;
     Layout L = layout(MOE_OP_LAYER, 1, R0.k, X0.E, X0.D, X0.F);

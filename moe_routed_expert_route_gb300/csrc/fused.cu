@@ -10,9 +10,11 @@
 // it is the first choice or its weight is >= the threshold, and is otherwise
 // replaced by the best resident expert.
 //
-// Grid = one CTA of 16 warps per SM, all resident; the CTAs exchange small
-// vectors through L2, each value or completion flag tagged with the launch's
-// sequence number, so readers poll the data itself and no counter is shared:
+// Grid = one CTA of 16 warps per SM, all resident. The CTAs exchange three
+// small vectors through L2 -- the logits, the activations and (in a stack) a
+// layer's output -- as 64-bit words that carry a tag derived from the launch's
+// sequence number next to the value. A reader polls the words themselves until
+// each carries the current tag: no counter, flag or memory fence is involved.
 //   0  before waiting on the previous launch: a bulk copy brings this CTA's
 //      rows of the router weights (1-7 experts) into shared memory
 //   1  x -> shared memory; the CTA's logits -> workspace (tagged); x -> 16-bit
@@ -27,17 +29,17 @@
 //   3  one thread starts bulk copies of this CTA's rows of the k down
 //      matrices into shared memory while the 16 warps stream this CTA's share
 //      of the k*F gate/up row pairs from HBM (two row pairs in flight per warp)
-//      and write h = silu(g)*u to the workspace; the CTA then raises its
-//      completion flag
-//   4  after every CTA's flag, the CTA reads all k*F activations once and
-//      turns them into 16-bit fixed point (one power-of-two scale per block of
-//      32 units); each warp dots its share of the (row, slot) pairs against the
-//      staged down rows (integer dp4a); the CTA combines the k slots in slot
-//      order, y[d] = sum_r w[r] * o_r[d], and writes x_next = x + y
-// In a stack, layer l+1 starts when every CTA has raised its flag for layer l
-// (its y and x_next are written): in chained mode its token is x_next of layer
-// l, otherwise its own input, read only after that wait either way. The next
-// layer's router rows are copied in while the current layer streams.
+//      and publish h = silu(g)*u (tagged)
+//   4  the CTA reads all k*F activations once (eight 16-byte loads in flight
+//      per thread) and turns them into 16-bit fixed point (one power-of-two
+//      scale per block of 32 units); each warp takes a (slot, share of the
+//      CTA's rows) task, holds the slot's activations in registers and dots
+//      them with the staged down rows (integer dp4a); the CTA combines the k
+//      slots in slot order, y[d] = sum_r w[r] * o_r[d], and writes x_next = x + y
+// In a stack, layer l+1 starts when every word of layer l's x_next has
+// arrived: in chained mode those words are its token, otherwise its own
+// input, read only after that wait either way. The next layer's router rows
+// are copied in while the current layer streams.
 // Without a router (moe_decode) phases 0-2 are replaced by reading idx/w.
 #include <mutex>
 
@@ -49,12 +51,16 @@ namespace moe {
 
 constexpr int kFThreads = 512;
 constexpr int kFWarps = 16;
-constexpr int kNRC = 4;  // router 16-byte chunks per lane
-constexpr int kNCH = 4;  // gate/up 16-byte chunks per lane
-constexpr int kDP = 4;   // (row, slot) down dots reduced together
+constexpr int kNRC = 4;      // router 16-byte chunks per lane
+constexpr int kNCH = 4;      // gate/up 16-byte chunks per lane
+constexpr int kDP = 8;       // down rows per warp task pass (computed together)
+constexpr int kNPL = 4;      // 8-byte down pieces per lane (F <= 1024 int8, 2048 int4)
+constexpr int kChunk = 128;  // tagged words per staged chunk (1 KB)
 
+// Shared-memory plan of one CTA.
 struct FusedLayout {
-    size_t x, xhi, xlo, xs, hhi, hlo, hs, wr, dq, ds, part, cand, rcand, total;
+    size_t x, xhi, xlo, xs, hhi, hlo, hs, wr, dq, ds, part, cand, rcand, sel, stage;
+    size_t total;
 };
 
 __host__ __device__ inline size_t fl_align(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -62,6 +68,8 @@ __host__ __device__ inline size_t fl_align(size_t v, size_t a) { return (v + a -
 // experts handled per CTA by the router phase
 __host__ __device__ inline int fused_nexp(int E, int G) { return (E + G - 1) / G; }
 
+// The staging region receives the tagged activations and (in a stack) the
+// previous layer's output.
 __host__ __device__ inline FusedLayout fused_layout(int E, int D, int F, int k, int qbits, int s_bytes,
                                                     int x_bytes, int rows, int G) {
     FusedLayout L;
@@ -81,7 +89,10 @@ __host__ __device__ inline FusedLayout fused_layout(int E, int D, int F, int k, 
     L.part = o;  o = fl_align(o + sizeof(float) * (size_t)k * rows, 16);
     L.cand = o;  o = fl_align(o + sizeof(uint2) * (size_t)nvw * k, 16);
     L.rcand = o; o = fl_align(o + sizeof(uint2) * (size_t)nvw * (2 * k - 1), 16);
-    L.total = o;
+    L.sel = o;   o = fl_align(o + sizeof(uint2) * 64, 16);
+    L.stage = fl_align(o, 128);
+    o = L.stage + sizeof(uint64_t) * (size_t)(k * F > D ? k * F : D);
+    L.total = fl_align(o, 16);
     return L;
 }
 
@@ -91,73 +102,95 @@ struct RowPair {
     ST gs[kNCH], us[kNCH];  // widened where used, so no load is waited for early
 };
 
-// Fixed-point conversion of NB blocks of 32 values held one per lane, the
-// NB max-reductions interleaved so their shuffles overlap.
-template <int NB>
-__device__ __forceinline__ void fx_store_blocks(const float (&v)[NB], const int (&blk)[NB], int nblk, int lane,
-                                                int qbits, int8_t* hi, uint8_t* lo, float* scale) {
-    float m[NB];
-#pragma unroll
-    for (int i = 0; i < NB; i++) m[i] = fabsf(v[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int i = 0; i < NB; i++) m[i] = fmaxf(m[i], __shfl_xor_sync(kFull, m[i], o));
-#pragma unroll
-    for (int i = 0; i < NB; i++) {
-        if (blk[i] < nblk) {
-            Fx f = fx_of_blockmax(m[i]);
-            int X = fx_code(v[i], f.mul);
-            int pos = blk[i] * kBlk + fx_pos(lane, qbits);
-            hi[pos] = (int8_t)(X >> 8);
-            lo[pos] = (uint8_t)(X & 0xff);
-            if (lane == 0) scale[blk[i]] = f.scale;
-        }
-    }
+// Fixed-point conversion of one block of 32 values held one per lane.
+__device__ __forceinline__ void fx_store_block1(float v, int blk, int lane, int qbits, int8_t* hi, uint8_t* lo,
+                                                float* scale) {
+    const float m = warp_max(fabsf(v));
+    const Fx f = fx_of_blockmax(m);
+    const int X = fx_code(v, f.mul);
+    const int pos = blk * kBlk + fx_pos(lane, qbits);
+    hi[pos] = (int8_t)(X >> 8);
+    lo[pos] = (uint8_t)(X & 0xff);
+    if (lane == 0) scale[blk] = f.scale;
 }
 
-// Called by a whole warp whose lane l holds expert `e` (consecutive ids in
-// lane order) with order key `key` (fp32 bits of its probability + 1, 0 for
-// no expert): writes the n largest keys, largest first and the lower id first
-// among equal keys, as {key, id} to out[0..n); missing entries are {0, 0}.
-__device__ __forceinline__ void extract_top(unsigned key, int n, uint2* out, int e, int lane) {
-    for (int it = 0; it < n; it++) {
-        const unsigned m = __reduce_max_sync(kFull, key);
-        if (m == 0u) {
-            for (int i = it + lane; i < n; i += 32) out[i] = make_uint2(0u, 0u);
-            return;
-        }
-        const unsigned tied = __ballot_sync(kFull, key == m);
-        if (lane == __ffs(tied) - 1) {
-            out[it] = make_uint2(m, (unsigned)e);
-            key = 0u;
-        }
-    }
+// Candidate order: {fp32 bits of p + 1, id} (x = 0: no expert); a ranks
+// before b when its probability is larger, or equal with a lower id.
+__device__ __forceinline__ int cand_before(uint2 a, uint2 b) {
+    return (a.x > b.x || (a.x == b.x && a.y < b.y)) ? 1 : 0;
 }
 
-// Called by one warp: removes and returns the largest {key, id} of list[0..n)
-// (lower id on equal keys); key 0 if the list is exhausted.
-__device__ __forceinline__ uint2 take_best(uint2* list, int n, int lane) {
-    unsigned bk = 0u, be = 0xffffffffu;
-    int bi = -1;
-    for (int i = lane; i < n; i += 32) {
-        const uint2 cd = list[i];
-        if (cd.x != 0u && (cd.x > bk || (cd.x == bk && cd.y < be))) {
-            bk = cd.x;
-            be = cd.y;
-            bi = i;
+// Called by a whole warp: brings the n tagged words src[0..n) of the chunks
+// c = warp, warp + 16, ... (kChunk words each) into dst (same offsets) by bulk
+// copies, re-copying any chunk that still holds a word without `tag`, until
+// every word of the warp's chunks carries it. Bounded by `lim`; on timeout
+// records MOE_ERR_DEVICE_TIMEOUT and returns false (the copies in flight have
+// landed by then).
+__device__ __noinline__ bool warp_stage_tagged(uint64_t* dst, const uint64_t* src, int n, unsigned tag, uint64_t* bar,
+                                  unsigned& phase, long long lim, int* status) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nch = (n + kChunk - 1) / kChunk;
+    int mine = 0;
+    for (int c = warp; c < nch; c += kFWarps) mine++;
+    unsigned pending = mine >= 32 ? 0xffffffffu : ((1u << mine) - 1u);
+    const long long t0 = clock64();
+    bool ok = true;
+#pragma unroll 1
+    while (pending) {
+        if (lane == 0) {
+            unsigned bytes = 0;
+            for (int i = 0; i < mine; i++)
+                if (pending >> i & 1u) bytes += 8u * (unsigned)min(kChunk, n - (warp + kFWarps * i) * kChunk);
+            mbar_arrive_expect_tx(bar, bytes);
+            for (int i = 0; i < mine; i++) {
+                if (!(pending >> i & 1u)) continue;
+                const int c = warp + kFWarps * i;
+                bulk_g2s(dst + (size_t)c * kChunk, src + (size_t)c * kChunk,
+                         8u * (unsigned)min(kChunk, n - c * kChunk), bar);
+            }
+        }
+        // the lanes agree on the outcome: the loop and the return are warp-uniform
+        if (!__all_sync(kFull, mbar_wait(bar, phase, status, lim))) {
+            mbar_wait(bar, phase, status);  // the copies must land before the memory is reused
+            ok = false;
+        }
+        phase ^= 1u;
+        unsigned still = 0;
+#pragma unroll 1
+        for (int i = 0; i < mine; i++) {
+            if (!(pending >> i & 1u)) continue;
+            const int c = warp + kFWarps * i;
+            bool good = true;
+#pragma unroll
+            for (int q = 0; q < kChunk / 32; q++) {
+                const int wi = c * kChunk + q * 32 + lane;
+                if (wi < n) good &= tag_ok(dst[wi], tag);
+            }
+            if (!__all_sync(kFull, good)) still |= 1u << i;
+        }
+        pending = still;
+        const bool late = __shfl_sync(kFull, clock64() - t0 > lim, 0);
+        if (!ok || (pending && late)) {
+            if (lane == 0 && ok) record_error(status, MOE_ERR_DEVICE_TIMEOUT);
+            return false;
         }
     }
-    const unsigned m = __reduce_max_sync(kFull, bk);
-    const unsigned me = __reduce_min_sync(kFull, bk == m ? be : 0xffffffffu);
-    if (m != 0u && bi >= 0 && bk == m && be == me) list[bi].x = 0u;
-    __syncwarp();
-    return make_uint2(m, me);
+    return ok;
 }
 
-template <int QB, typename ST, typename XT, int NL>
+// Layer shape known at compile time (0 = read from the parameters): the
+// kernel is instantiated for the decode shapes it serves most, so that every
+// loop bound and shared-memory offset is a constant there.
+template <int E_, int K_, int D_, int F_>
+struct FShape {
+    static constexpr int E = E_, k = K_, D = D_, F = F_;
+};
+using FRuntime = FShape<0, 0, 0, 0>;
+
+template <int QB, typename ST, typename XT, int NL, class SH>
 __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_constant__ FusedArgs<NL> a) {
     extern __shared__ __align__(128) unsigned char sm[];
+    __shared__ FusedLayer s_ly[2];  // this layer's and the next layer's pointers
     __shared__ float s_rpart[kFWarps];
     __shared__ float s_rmax[kFWarps];
     __shared__ float s_rsum[kFWarps];
@@ -165,13 +198,15 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     __shared__ float s_w[32];
     __shared__ unsigned s_seq;
     __shared__ long long s_lim;
-    __shared__ __align__(8) uint64_t s_bar;   // down rows of the current layer
-    __shared__ __align__(8) uint64_t s_rbar;  // router rows of the next layer
+    __shared__ __align__(8) uint64_t s_bar;              // down rows of the current layer
+    __shared__ __align__(8) uint64_t s_rbar;             // router rows
+    __shared__ __align__(8) uint64_t s_wbar[kFWarps];    // per-warp staging
 
     const FusedCommon& P = a.c;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x, G = gridDim.x;
-    const int E = P.E, D = P.D, F = P.F, k = P.k;
+    const int E = SH::E ? SH::E : P.E, D = SH::D ? SH::D : P.D;
+    const int F = SH::F ? SH::F : P.F, k = SH::k ? SH::k : P.k;
     const int nb = D / kBlk, nbF = F / kBlk;
     const int rowD = QB == 8 ? D : D / 2;  // bytes of a gate/up row
     const int rowF = QB == 8 ? F : F / 2;  // bytes of a down row
@@ -189,9 +224,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     float* s_part = reinterpret_cast<float*>(sm + Lo.part);
     uint2* s_cand = reinterpret_cast<uint2*>(sm + Lo.cand);
     uint2* s_rcand = reinterpret_cast<uint2*>(sm + Lo.rcand);
+    uint2* s_sel = reinterpret_cast<uint2*>(sm + Lo.sel);
+    uint64_t* s_stage = reinterpret_cast<uint64_t*>(sm + Lo.stage);
     int* status = &P.hdr->status;
-    unsigned* flag_h = P.flags;                  // activations of a layer written
-    unsigned* flag_x = P.flags + kFusedMaxGrid;  // y / x_next of a layer written
 
     // this CTA's share: output rows (whole pairs), gate/up units, router experts
     const int d_begin = 2 * (int)((long)c * (D / 2) / G), d_end = 2 * (int)((long)(c + 1) * (D / 2) / G);
@@ -205,22 +240,32 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     const bool rvalid = P.has_router && e_begin + rj < e_end;
     constexpr int EPC = 16 / sizeof(XT);
     const int nvw = (E + 31) / 32;
+    const int nxw = sizeof(XT) == 2 ? D / 2 : D;  // tagged words of a layer's x_next
 
+    // one layer's pointers, from the kernel parameters into s_ly[b]
+    auto load_layer = [&](int l, int b) {
+        constexpr int NWD = sizeof(FusedLayer) / 4;
+        const int t = tid - (kFThreads - 64);  // the last two warps
+        if (t >= 0 && t < NWD)
+            reinterpret_cast<uint32_t*>(&s_ly[b])[t] = reinterpret_cast<const uint32_t*>(&a.L[l])[t];
+    };
     // bulk copy of this CTA's router rows (contiguous) of layer l
-    auto request_router = [&](int l) {
+    auto request_router = [&](const FusedLayer& Y) {
         const unsigned bytes = (unsigned)((e_end - e_begin) * D * (int)sizeof(XT));
         mbar_arrive_expect_tx(&s_rbar, bytes);
-        if (bytes) bulk_g2s(sm + Lo.wr, static_cast<const XT*>(a.L[l].W) + (size_t)e_begin * D, bytes, &s_rbar);
+        if (bytes) bulk_g2s(sm + Lo.wr, static_cast<const XT*>(Y.W) + (size_t)e_begin * D, bytes, &s_rbar);
     };
 
     // ---------------------------------------------------------- phase 0
+    load_layer(0, 0);
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         mbar_init(&s_rbar, 1);
+        for (int i = 0; i < kFWarps; i++) mbar_init(&s_wbar[i], 1);
         fence_barrier_init();
-        if (P.has_router) request_router(0);
     }
     __syncthreads();
+    if (tid == 0 && P.has_router) request_router(s_ly[0]);
     pdl_wait();
     pdl_trigger();
     // the previous launch on this workspace has completed: its sequence
@@ -234,26 +279,53 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     const unsigned seq0 = s_seq;
     const long long lim = s_lim;
     int router_next = P.has_router ? 0 : -1;  // layer whose router copy is requested and not waited for
+    unsigned wph = 0;                         // this warp's staging-barrier phase
     // this thread saw a wait run out; decisions on it are taken with
     // __syncthreads_or so that every thread of the CTA takes the same branch
     bool ab = false;
 
+#pragma unroll 1
     for (int l = 0; l < P.nlayers; l++) {
-        const FusedLayer& Y = a.L[l];
+        const FusedLayer& Y = s_ly[l & 1];
         const unsigned tag = seq_tag(seq0 + (unsigned)l);
-
-        // ------------------------------------------------------ phase 1
-        if (l > 0) {
-            // every CTA has written layer l-1's y and x_next
-            if (warp == 0 && !poll_flags(flag_x, G, seq_tag(seq0 + (unsigned)l - 1u), lim, status)) ab = true;
-            if (__syncthreads_or(ab)) break;
-        }
-        const XT* X = reinterpret_cast<const XT*>((l > 0 && P.chain) ? a.L[l - 1].x_next : Y.x);
-        for (int i = tid; i < D; i += kFThreads) s_x[i] = ldcg_f32(X + i);
-        // residency of the experts this thread selects among
+        // requested now, used after the logits: bias of this CTA's experts and
+        // the residency of the experts this thread selects among
+        const float bias_r = (P.has_router && Y.bias && tid < e_end - e_begin) ? Y.bias[e_begin + tid] : 0.f;
         const int e0 = tid, e1 = tid + kFThreads;
         const bool res0 = Y.resident && e0 < E && Y.resident[e0];
         const bool res1 = Y.resident && e1 < E && Y.resident[e1];
+
+        // ------------------------------------------------------ phase 1
+        if (l > 0) {
+            // layer l-1's x_next, tagged word by word by the CTAs that wrote it,
+            // staged into shared memory: this layer starts when all of it has
+            // arrived; chained, it is this layer's token
+            const unsigned ptag = seq_tag(seq0 + (unsigned)l - 1u);
+            if (!warp_stage_tagged(s_stage, P.xex, nxw, ptag, &s_wbar[warp], wph, lim, status)) ab = true;
+            if (P.chain) {
+#pragma unroll 1
+                for (int i = warp * kChunk + lane; i < nxw; i += kFWarps * kChunk)
+#pragma unroll
+                    for (int q = 0; q < kChunk; q += 32) {
+                        const int wi = i + q;
+                        if (wi < nxw) {
+                            const uint32_t v = (uint32_t)s_stage[wi];
+                            if constexpr (sizeof(XT) == 2) {
+                                s_x[2 * wi] = bf16lo(v);
+                                s_x[2 * wi + 1] = bf16hi(v);
+                            } else {
+                                s_x[wi] = __uint_as_float(v);
+                            }
+                        }
+                    }
+            }
+            if (__syncthreads_or(ab)) break;
+        }
+        if (l == 0 || !P.chain) {
+            const XT* X = reinterpret_cast<const XT*>(Y.x);
+#pragma unroll 4
+            for (int i = tid; i < D; i += kFThreads) s_x[i] = ldcg_f32(X + i);
+        }
         __syncthreads();
 
         if (P.has_router) {
@@ -284,13 +356,11 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             __syncthreads();
             if (tid < e_end - e_begin) {
                 float lg = 0.f;
+#pragma unroll 4
                 for (int s2 = 0; s2 < nseg; s2++) lg += s_rpart[tid * nseg + s2];
-                if (Y.bias) lg += Y.bias[e_begin + tid];
+                if (Y.bias) lg += bias_r;
                 st_tagged(P.logits + e_begin + tid, lg, tag);
             }
-            // the next layer's router rows stream in while this layer runs
-            if (tid == 0 && l + 1 < P.nlayers) request_router(l + 1);
-            if (l + 1 < P.nlayers) router_next = l + 1;
         } else if (tid < k) {
             int e = ld_cg_i32(Y.idx_in + tid);
             if (e < 0 || e >= E) {
@@ -300,18 +370,12 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             s_idx[tid] = e;
             s_w[tid] = ld_cg_f32(Y.w_in + tid);
         }
+        // the next layer's pointers (its router rows are requested once they are in)
+        if (l + 1 < P.nlayers) load_layer(l + 1, (l + 1) & 1);
 
         // x -> fixed-point planes (while the other CTAs' logits arrive)
-        for (int b0 = warp; b0 < nb; b0 += kFWarps * 4) {
-            float v[4];
-            int blk[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                blk[i] = b0 + kFWarps * i;
-                v[i] = blk[i] < nb ? s_x[blk[i] * kBlk + lane] : 0.f;
-            }
-            fx_store_blocks<4>(v, blk, nb, lane, QB, s_xhi, s_xlo, s_xs);
-        }
+#pragma unroll 1
+        for (int b = warp; b < nb; b += kFWarps) fx_store_block1(s_x[b * kBlk + lane], b, lane, QB, s_xhi, s_xlo, s_xs);
 
         // ------------------------------------------------------ phase 2
         if (P.has_router) {
@@ -319,6 +383,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             {
                 bool r0 = e0 >= E, r1 = e1 >= E;
                 const long long t0 = clock64();
+#pragma unroll 1
                 while (!(r0 && r1)) {
                     const uint64_t w0 = r0 ? 0ull : ld_tagged(P.logits + e0);
                     const uint64_t w1 = r1 ? 0ull : ld_tagged(P.logits + e1);
@@ -336,15 +401,21 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             float mx = warp_max(fmaxf(lg0, lg1));
             if (lane == 0) s_rmax[warp] = mx;
             __syncthreads();
-            mx = s_rmax[0];
-            for (int i = 1; i < kFWarps; i++) mx = fmaxf(mx, s_rmax[i]);
+            {
+                float m2[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) m2[q] = fmaxf(fmaxf(s_rmax[4 * q], s_rmax[4 * q + 1]),
+                                                          fmaxf(s_rmax[4 * q + 2], s_rmax[4 * q + 3]));
+                mx = fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3]));
+            }
             float p0 = e0 < E ? expf(lg0 - mx) : 0.f;
             float p1 = e1 < E ? expf(lg1 - mx) : 0.f;
             const float ws = warp_sum(p0 + p1);
             if (lane == 0) s_rsum[warp] = ws;
             __syncthreads();
             float sum = 0.f;
-            for (int i = 0; i < kFWarps; i++) sum += s_rsum[i];
+#pragma unroll
+            for (int i = 0; i < kFWarps; i++) sum += s_rsum[i];  // fixed order
             const float inv_s = 1.0f / sum;
             p0 *= inv_s;
             p1 *= inv_s;
@@ -352,48 +423,102 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 if (e0 < E) Y.probs[e0] = p0;
                 if (e1 < E) Y.probs[e1] = p1;
             }
-            // per-warp candidates: the k largest of each warp's 32 experts (and
-            // the 2k-1 largest resident ones)
-#pragma unroll
+            // per-warp candidates: every lane counts the lanes of its warp whose
+            // key is larger (key = fp32 bits of p + 1 over ~id: larger p first,
+            // lower id on equal p; keys are unique); ranks below k are kept (and
+            // below 2k-1 among resident experts, for the replacements)
+#pragma unroll 1
             for (int j = 0; j < 2; j++) {
                 const int vw = j * kFWarps + warp;
                 if (vw < nvw) {
                     const int e = vw * 32 + lane;
                     const float pe = j ? p1 : p0;
+                    // 32-bit key: fp32 bits of p + 1 (0 = no expert); among equal
+                    // keys the lower lane (lower id) ranks first
                     const unsigned key = e < E ? __float_as_uint(pe) + 1u : 0u;
-                    extract_top(key, k, s_cand + (size_t)vw * k, e, lane);
+                    const bool re = Y.resident && (j ? res1 : res0);
+                    const unsigned rkey = re ? key : 0u;
+                    int rank = 0, rrank = 0;
                     if (Y.resident) {
-                        const bool re = j ? res1 : res0;
-                        extract_top(re ? key : 0u, 2 * k - 1, s_rcand + (size_t)vw * (2 * k - 1), e, lane);
+#pragma unroll 8
+                        for (int o = 0; o < 32; o++) {
+                            // every lane executes both shuffles
+                            const unsigned ko = __shfl_sync(kFull, key, o);
+                            const int ro = __shfl_sync(kFull, (int)re, o);
+                            const bool before = ko > key || (ko == key && o < lane);
+                            rank += before;
+                            rrank += (ro != 0 && (ko > rkey || (ko == rkey && o < lane))) ? 1 : 0;
+                        }
+                    } else {
+#pragma unroll 8
+                        for (int o = 0; o < 32; o++) {
+                            const unsigned ko = __shfl_sync(kFull, key, o);
+                            rank += (ko > key || (ko == key && o < lane)) ? 1 : 0;
+                        }
+                    }
+                    uint2* cw = s_cand + (size_t)vw * k;
+                    const int nvalid = __popc(__ballot_sync(kFull, key != 0u));
+                    if (key != 0u && rank < k) cw[rank] = make_uint2(key, (unsigned)e);
+                    for (int i = nvalid + lane; i < k; i += 32) cw[i] = make_uint2(0u, 0u);
+                    if (Y.resident) {
+                        uint2* rw = s_rcand + (size_t)vw * (2 * k - 1);
+                        const int nres = __popc(__ballot_sync(kFull, rkey != 0u));
+                        if (rkey != 0u && rrank < 2 * k - 1) rw[rrank] = make_uint2(key, (unsigned)e);
+                        for (int i = nres + lane; i < 2 * k - 1; i += 32) rw[i] = make_uint2(0u, 0u);
                     }
                 }
             }
             __syncthreads();
-            if (warp == 0) {
-                int sel_e = -1;
-                float sel_p = 0.f;
-                for (int r = 0; r < k; r++) {
-                    const uint2 b = take_best(s_cand, nvw * k, lane);
-                    if (lane == r && b.x != 0u) {
-                        sel_e = (int)b.y;
-                        sel_p = __uint_as_float(b.x - 1u);
-                    }
+            // the k best candidates, by each candidate's rank among all of them
+            const int C = nvw * k;
+#pragma unroll 1
+            for (int i = tid; i < C; i += kFThreads) {
+                const uint2 me = s_cand[i];
+                if (me.x == 0u) continue;
+                int rank = 0;
+#pragma unroll 8
+                for (int j2 = 0; j2 < C; j2++) rank += cand_before(s_cand[j2], me);
+                if (rank < k) s_sel[rank] = me;
+            }
+            __syncthreads();
+            if (Y.resident) {
+                // replacement candidates: resident experts outside the chosen k,
+                // ranked the same way; the best ones go to the replaced slots in
+                // rank order
+                const int RC = nvw * (2 * k - 1);
+                if (tid < k) s_sel[32 + tid] = make_uint2(0u, 0u);
+#pragma unroll 1
+                for (int i = tid; i < RC; i += kFThreads) {
+                    const unsigned e = s_rcand[i].y;
+#pragma unroll 1
+                    for (int r = 0; r < k; r++)
+                        if (s_rcand[i].x != 0u && s_sel[r].y == e) s_rcand[i].x = 0u;
                 }
+                __syncthreads();
+#pragma unroll 1
+                for (int i = tid; i < RC; i += kFThreads) {
+                    const uint2 me = s_rcand[i];
+                    if (me.x == 0u) continue;
+                    int rank = 0;
+#pragma unroll 8
+                    for (int j2 = 0; j2 < RC; j2++) rank += cand_before(s_rcand[j2], me);
+                    if (rank < k) s_sel[32 + rank] = me;
+                }
+                __syncthreads();
+            }
+            if (warp == 0) {
+                const uint2 sel = lane < k ? s_sel[lane] : make_uint2(0u, 0u);
+                const int sel_e = sel.x ? (int)sel.y : -1;
+                const float sel_p = sel.x ? __uint_as_float(sel.x - 1u) : 0.f;
                 const float norm = warp_sum(lane < k ? sel_p : 0.f);
                 const float wv = P.norm_topk ? sel_p / norm : sel_p;
                 int use_e = sel_e;
                 unsigned flg = 0;
                 if (Y.resident) {
-                    // replacement candidates: resident experts outside the chosen k
-                    if (lane < k) s_idx[lane] = sel_e;
-                    __syncwarp();
-                    const int nrc = nvw * (2 * k - 1);
-                    for (int i = lane; i < nrc; i += 32)
-                        for (int r = 0; r < k; r++)
-                            if (s_rcand[i].x != 0u && (int)s_rcand[i].y == s_idx[r]) s_rcand[i].x = 0u;
-                    __syncwarp();
                     const bool my_res = lane < k && sel_e >= 0 && Y.resident[sel_e];
                     float mass = 0.f;
+                    int nrep = 0;  // replacements used so far
+#pragma unroll 1
                     for (int r = 0; r < k; r++) {
                         const int er = __shfl_sync(kFull, sel_e, r);
                         const float wr = __shfl_sync(kFull, wv, r);
@@ -407,13 +532,14 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                         } else if (r == 0 || wr >= P.threshold) {
                             f = 1;
                         } else {
-                            const uint2 b = take_best(s_rcand, nrc, lane);
-                            if (b.x == 0u) {
+                            const uint2 b2 = nrep < k ? s_sel[32 + nrep] : make_uint2(0u, 0u);
+                            if (b2.x == 0u) {
                                 f = 3;
                             } else {
-                                out = (int)b.y;
+                                out = (int)b2.y;
                                 f = 2;
                                 mass += wr;
+                                nrep++;
                             }
                         }
                         if (lane == r) {
@@ -423,7 +549,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                     }
                     if (c == 0 && lane == 0 && Y.sub_mass) Y.sub_mass[0] = mass;
                 }
-                __syncwarp();
                 if (lane < k) {
                     s_idx[lane] = use_e;
                     s_w[lane] = wv;
@@ -439,76 +564,106 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
         __syncthreads();
 
         // ------------------------------------------------------ phase 3
-        // bulk copies of this CTA's down rows and their scales
-        auto issue_down = [&]() {
+        // one thread starts bulk copies of this CTA's rows of the k down
+        // matrices (and, in a stack, the next layer's router rows); the warps
+        // stream their share of the gate/up row pairs with 16-byte loads, two
+        // pairs in flight per warp, and publish h = silu(g)*u (tagged)
+        if (tid == 0) {
+            // the whole of this CTA's gate/up rows (consecutive units are
+            // consecutive rows of one expert) are requested into L2 at once, so
+            // that HBM streams them at full rate while the warps' loads find them
+            const uint8_t* GQp = reinterpret_cast<const uint8_t*>(Y.gate_q);
+            const uint8_t* UQp = reinterpret_cast<const uint8_t*>(Y.up_q);
+            const ST* GSp = reinterpret_cast<const ST*>(Y.gate_s);
+            const ST* USp = reinterpret_cast<const ST*>(Y.up_s);
+#pragma unroll 1
+            for (int g0 = g_begin; g0 < g_end;) {
+                const int r = g0 / F, n0 = g0 - r * F;
+                const int n1 = min(F, n0 + (g_end - g0));
+                const int e = s_idx[r];
+                if (e >= 0) {
+                    const size_t row = (size_t)e * F + n0;
+                    const unsigned cb = (unsigned)((n1 - n0) * rowD), sbb = (unsigned)((n1 - n0) * nb * sizeof(ST));
+                    prefetch_l2(GQp + row * rowD, cb);
+                    prefetch_l2(UQp + row * rowD, cb);
+                    if (sbb % 16 == 0) {
+                        prefetch_l2(GSp + row * nb, sbb);
+                        prefetch_l2(USp + row * nb, sbb);
+                    }
+                }
+                g0 += n1 - n0;
+            }
+        }
+        if (tid == 32) {
             unsigned bytes = 0;
+#pragma unroll 1
             for (int r = 0; r < k; r++)
                 if (s_idx[r] >= 0) bytes += nrows * (rowF + nbF * (int)sizeof(ST));
             mbar_arrive_expect_tx(&s_bar, bytes);
             const uint8_t* DQ = reinterpret_cast<const uint8_t*>(Y.down_q);
             const ST* DS = reinterpret_cast<const ST*>(Y.down_s);
-            if (nrows > 0) {
-                for (int r = 0; r < k; r++) {
-                    const int e = s_idx[r];
-                    if (e < 0) continue;
-                    const size_t row0 = (size_t)e * D + d_begin;
-                    bulk_g2s(s_dq + (size_t)r * P.rows * rowF, DQ + row0 * rowF, nrows * rowF, &s_bar);
-                    bulk_g2s(s_ds + (size_t)r * P.rows * nbF, DS + row0 * nbF, nrows * nbF * (int)sizeof(ST),
-                             &s_bar);
-                }
+#pragma unroll 1
+            for (int r = 0; r < k; r++) {
+                const int e = s_idx[r];
+                if (e < 0 || nrows == 0) continue;
+                const size_t row0 = (size_t)e * D + d_begin;
+                bulk_g2s(s_dq + (size_t)r * P.rows * rowF, DQ + row0 * rowF, nrows * rowF, &s_bar);
+                bulk_g2s(s_ds + (size_t)r * P.rows * nbF, DS + row0 * nbF, nrows * nbF * (int)sizeof(ST), &s_bar);
             }
-        };
+            // the next layer's router rows (its pointers were loaded before the last barrier)
+            if (l + 1 < P.nlayers && P.has_router) request_router(s_ly[(l + 1) & 1]);
+        }
+        if (l + 1 < P.nlayers && P.has_router) router_next = l + 1;
 
         const uint8_t* GQ = reinterpret_cast<const uint8_t*>(Y.gate_q);
         const uint8_t* UQ = reinterpret_cast<const uint8_t*>(Y.up_q);
         const ST* GS = reinterpret_cast<const ST*>(Y.gate_s);
         const ST* US = reinterpret_cast<const ST*>(Y.up_s);
         const int nchunk = rowD / 16;
-
         auto load_pair = [&](int g, RowPair<QB, ST>& rp) {
             const int r = g / F, n = g - r * F;
             const int e = g < g_end ? s_idx[r] : -1;
             const bool ok = e >= 0;
             const size_t row = (size_t)(ok ? e : 0) * F + n;
 #pragma unroll
-            for (int j = 0; j < kNCH; j++) {
-                const int ci = j * 32 + lane;
+            for (int q = 0; q < kNCH; q++) {
+                const int ci = q * 32 + lane;
                 if (ok && ci < nchunk) {
-                    rp.g[j] = ld_stream16(GQ + row * rowD + 16 * ci);
-                    rp.u[j] = ld_stream16(UQ + row * rowD + 16 * ci);
+                    rp.g[q] = ld_stream16(GQ + row * rowD + 16 * ci);
+                    rp.u[q] = ld_stream16(UQ + row * rowD + 16 * ci);
                     const int blk = QB == 8 ? (ci >> 1) : ci;
-                    rp.gs[j] = ldg_nc(GS + row * nb + blk);
-                    rp.us[j] = ldg_nc(US + row * nb + blk);
+                    rp.gs[q] = ldg_nc(GS + row * nb + blk);
+                    rp.us[q] = ldg_nc(US + row * nb + blk);
                 } else {
-                    rp.g[j] = rp.u[j] = make_uint4(0, 0, 0, 0);
-                    rp.gs[j] = rp.us[j] = ST(0.f);
+                    rp.g[q] = rp.u[q] = make_uint4(0, 0, 0, 0);
+                    rp.gs[q] = rp.us[q] = ST(0.f);
                 }
             }
         };
         auto finish_pair = [&](int g, const RowPair<QB, ST>& rp) {
             float ga = 0.f, ua = 0.f;
 #pragma unroll
-            for (int j = 0; j < kNCH; j++) {
-                const int ci = j * 32 + lane;
+            for (int q = 0; q < kNCH; q++) {
+                const int ci = q * 32 + lane;
                 if (ci < nchunk) {
                     int ig, iu;
                     float xs;
                     if constexpr (QB == 8) {
                         const uint4 hi = *reinterpret_cast<const uint4*>(s_xhi + 16 * ci);
                         const uint4 lo = *reinterpret_cast<const uint4*>(s_xlo + 16 * ci);
-                        ig = dot_i8_chunk(rp.g[j], hi, lo);
-                        iu = dot_i8_chunk(rp.u[j], hi, lo);
+                        ig = dot_i8_chunk(rp.g[q], hi, lo);
+                        iu = dot_i8_chunk(rp.u[q], hi, lo);
                         xs = s_xs[ci >> 1];
                     } else {
                         const uint4* H = reinterpret_cast<const uint4*>(s_xhi + 32 * ci);
                         const uint4* Lw = reinterpret_cast<const uint4*>(s_xlo + 32 * ci);
                         const uint4 h0 = H[0], h1 = H[1], l0 = Lw[0], l1 = Lw[1];
-                        ig = dot_i4_chunk(rp.g[j], h0, h1, l0, l1);
-                        iu = dot_i4_chunk(rp.u[j], h0, h1, l0, l1);
+                        ig = dot_i4_chunk(rp.g[q], h0, h1, l0, l1);
+                        iu = dot_i4_chunk(rp.u[q], h0, h1, l0, l1);
                         xs = s_xs[ci] * (1.0f / 16.0f);
                     }
-                    ga = fmaf((float)ig, to_f32(rp.gs[j]) * xs, ga);
-                    ua = fmaf((float)iu, to_f32(rp.us[j]) * xs, ua);
+                    ga = fmaf((float)ig, to_f32(rp.gs[q]) * xs, ga);
+                    ua = fmaf((float)iu, to_f32(rp.us[q]) * xs, ua);
                 }
             }
 #pragma unroll
@@ -516,15 +671,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 ga += __shfl_xor_sync(kFull, ga, o);
                 ua += __shfl_xor_sync(kFull, ua, o);
             }
-            if (lane == 0 && g < g_end) P.h[g] = silu_mul(ga, ua);
+            if (lane == 0 && g < g_end) st_tagged(P.h + g, silu_mul(ga, ua), tag);
         };
-
         {
             RowPair<QB, ST> A, B;
             int g = g_begin + warp;
             load_pair(g, A);
-            // the down rows are requested together with the first gate/up rows
-            if (tid == 32) issue_down();
+#pragma unroll 1
             while (g < g_end) {
                 const int g2 = g + kFWarps;
                 load_pair(g2, B);
@@ -536,32 +689,29 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 g = g3;
             }
         }
-        __syncthreads();
-        if (tid == 0) {
-            __threadfence();
-            st_release_u32(flag_h + c, tag);
-        }
 
         // ------------------------------------------------------ phase 4
-        if (warp == 0 && !poll_flags(flag_h, G, tag, lim, status)) ab = true;
-        __syncthreads();
-        // every slot's activations -> 16-bit fixed-point planes, one power-of-two
-        // scale per block of 32 units (8 lanes of 4 units each)
+        // every slot's activations: each warp stages its chunks of the tagged
+        // words (re-copying chunks that are not all there yet) and turns them
+        // into 16-bit fixed point, one power-of-two scale per block of 32 units
+        // (4 units per lane, 8 lanes per block)
         {
-            const int n4 = (k * F) / 4;
-            for (int i0 = warp * 32; i0 < n4; i0 += kFThreads) {
-                const int i = i0 + lane;
-                const bool ok = i < n4;
-                const uint4 t = ok ? ld_cg16(P.h + 4 * i) : make_uint4(0, 0, 0, 0);
-                const float v[4] = {__uint_as_float(t.x), __uint_as_float(t.y), __uint_as_float(t.z),
-                                    __uint_as_float(t.w)};
+            const int nw_ = k * F;
+            if (!warp_stage_tagged(s_stage, P.h, nw_, tag, &s_wbar[warp], wph, lim, status)) ab = true;
+            const int nch = (nw_ + kChunk - 1) / kChunk;
+#pragma unroll 1
+            for (int ch = warp; ch < nch; ch += kFWarps) {
+                const int u = ch * kChunk + 4 * lane;
+                const bool ok = u < nw_;
+                float v[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) v[q] = ok ? tag_val(s_stage[u + q]) : 0.f;
                 float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
                 m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
                 m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
                 m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
                 if (ok) {
                     const Fx f = fx_of_blockmax(m);
-                    const int u = 4 * i;
                     if constexpr (QB == 8) {
                         uint32_t hw = 0, lw = 0;
 #pragma unroll
@@ -576,9 +726,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
                             const int Xq = fx_code(v[q], f.mul);
-                            const int pos = fx_pos(u + q, 4);
-                            s_hhi[pos] = (int8_t)(Xq >> 8);
-                            s_hlo[pos] = (uint8_t)(Xq & 0xff);
+                            s_hhi[fx_pos(u + q, 4)] = (int8_t)(Xq >> 8);
+                            s_hlo[fx_pos(u + q, 4)] = (uint8_t)(Xq & 0xff);
                         }
                     }
                     if ((lane & 7) == 0) s_hs[u / kBlk] = QB == 8 ? f.scale : f.scale * (1.0f / 16.0f);
@@ -591,83 +740,123 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
         }
         __syncthreads();
 
-        // down: (row, slot) pairs q = i*k + r spread over the warps, 8-byte
-        // pieces of a row per lane (int8: 8 units, int4: 16 units)
+        // down: task = (slot, share of the CTA's rows); the warp keeps the
+        // slot's activation planes in registers and dots them with each row
+        // (8-byte pieces per lane: int8 8 units, int4 16 units)
         {
             constexpr int EPP = QB == 8 ? 8 : 16;
+            constexpr int NW = EPP / 4;  // plane words per piece and plane
             const int npieces = rowF / 8;
-            const int npairs = nrows * k;
-            for (int q0 = warp; q0 < npairs; q0 += kFWarps * kDP) {
-                float acc[kDP];
+            const int nsplit = k >= kFWarps ? 1 : kFWarps / k;
+            const int ntask = k * nsplit;
+#pragma unroll 1
+            for (int task = warp; task < ntask; task += kFWarps) {
+                const int r = task / nsplit, part = task - r * nsplit;
+                const int i0 = nrows * part / nsplit, i1 = nrows * (part + 1) / nsplit;
+                if (s_idx[r] < 0 || i0 >= i1) continue;
+                uint32_t hp[kNPL][NW], lp[kNPL][NW];
+                float hsc[kNPL];
 #pragma unroll
-                for (int u = 0; u < kDP; u++) {
-                    acc[u] = 0.f;
-                    const int q = q0 + u * kFWarps;
-                    if (q < npairs) {
-                        const int i = q / k, r = q - (q / k) * k;
-                        if (s_idx[r] >= 0) {
-                            const uint8_t* dq = s_dq + ((size_t)r * P.rows + i) * rowF;
-                            const ST* ds = s_ds + ((size_t)r * P.rows + i) * nbF;
-                            const int8_t* hh = s_hhi + (size_t)r * F;
-                            const uint8_t* hl = s_hlo + (size_t)r * F;
-                            const float* hs = s_hs + (size_t)r * nbF;
-                            for (int pc = lane; pc < npieces; pc += 32) {
-                                const uint2 wv = *reinterpret_cast<const uint2*>(dq + 8 * pc);
-                                const int blk = (EPP * pc) / kBlk;
+                for (int j = 0; j < kNPL; j++) {
+                    const int pc = j * 32 + lane;
+                    hsc[j] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < NW; q++) hp[j][q] = lp[j][q] = 0u;
+                    if (pc < npieces) {
+                        const size_t o = (size_t)r * F + EPP * pc;
+                        if constexpr (QB == 8) {
+                            const uint2 h2 = *reinterpret_cast<const uint2*>(s_hhi + o);
+                            const uint2 l2 = *reinterpret_cast<const uint2*>(s_hlo + o);
+                            hp[j][0] = h2.x;
+                            hp[j][1] = h2.y;
+                            lp[j][0] = l2.x;
+                            lp[j][1] = l2.y;
+                        } else {
+                            const uint4 h4 = *reinterpret_cast<const uint4*>(s_hhi + o);
+                            const uint4 l4 = *reinterpret_cast<const uint4*>(s_hlo + o);
+                            hp[j][0] = h4.x;
+                            hp[j][1] = h4.y;
+                            hp[j][2] = h4.z;
+                            hp[j][3] = h4.w;
+                            lp[j][0] = l4.x;
+                            lp[j][1] = l4.y;
+                            lp[j][2] = l4.z;
+                            lp[j][3] = l4.w;
+                        }
+                        hsc[j] = s_hs[(size_t)r * nbF + (EPP * pc) / kBlk];
+                    }
+                }
+                const uint8_t* dq0 = s_dq + (size_t)r * P.rows * rowF;
+                const ST* ds0 = s_ds + (size_t)r * P.rows * nbF;
+#pragma unroll 1
+                for (int row0 = i0; row0 < i1; row0 += kDP) {
+                    float acc[kDP];
+#pragma unroll
+                    for (int u = 0; u < kDP; u++) {
+                        const int row = min(row0 + u, i1 - 1);  // past the end: a duplicate row, not stored
+                        acc[u] = 0.f;
+#pragma unroll
+                        for (int j = 0; j < kNPL; j++) {
+                            const int pc = j * 32 + lane;
+                            if (pc < npieces) {
+                                const uint2 wv = *reinterpret_cast<const uint2*>(dq0 + (size_t)row * rowF + 8 * pc);
+                                const float sc = to_f32(ds0[row * nbF + (EPP * pc) / kBlk]);
                                 int hd = 0, ld = 0;
                                 if constexpr (QB == 8) {
-                                    const uint2 hp = *reinterpret_cast<const uint2*>(hh + 8 * pc);
-                                    const uint2 lp = *reinterpret_cast<const uint2*>(hl + 8 * pc);
-                                    hd = dp4a_ss(wv.x, hp.x, hd);
-                                    hd = dp4a_ss(wv.y, hp.y, hd);
-                                    ld = dp4a_su(wv.x, lp.x, ld);
-                                    ld = dp4a_su(wv.y, lp.y, ld);
+                                    hd = dp4a_ss(wv.x, hp[j][0], hd);
+                                    hd = dp4a_ss(wv.y, hp[j][1], hd);
+                                    ld = dp4a_su(wv.x, lp[j][0], ld);
+                                    ld = dp4a_su(wv.y, lp[j][1], ld);
                                 } else {
-                                    const uint4 hp = *reinterpret_cast<const uint4*>(hh + 16 * pc);
-                                    const uint4 lp = *reinterpret_cast<const uint4*>(hl + 16 * pc);
-                                    dot_i4_word(wv.x, hp.x, hp.y, lp.x, lp.y, hd, ld);
-                                    dot_i4_word(wv.y, hp.z, hp.w, lp.z, lp.w, hd, ld);
+                                    dot_i4_word(wv.x, hp[j][0], hp[j][1], lp[j][0], lp[j][1], hd, ld);
+                                    dot_i4_word(wv.y, hp[j][2], hp[j][3], lp[j][2], lp[j][3], hd, ld);
                                 }
-                                acc[u] = fmaf(to_f32(ds[blk]) * hs[blk], (float)(hd * 256 + ld), acc[u]);
+                                acc[u] = fmaf(sc * hsc[j], (float)(hd * 256 + ld), acc[u]);
                             }
                         }
                     }
-                }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
+                    for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-                    for (int u = 0; u < kDP; u++) acc[u] += __shfl_xor_sync(kFull, acc[u], o);
-                if (lane == 0) {
+                        for (int u = 0; u < kDP; u++) acc[u] += __shfl_xor_sync(kFull, acc[u], o);
+                    if (lane == 0) {
 #pragma unroll
-                    for (int u = 0; u < kDP; u++) {
-                        const int q = q0 + u * kFWarps;
-                        if (q < npairs) s_part[q] = acc[u];
+                        for (int u = 0; u < kDP; u++)
+                            if (row0 + u < i1) s_part[(row0 + u) * k + r] = acc[u];
                     }
                 }
             }
         }
         __syncthreads();
-        if (tid < nrows) {
-            float y = 0.f;
-            for (int r = 0; r < k; r++)
-                if (s_idx[r] >= 0) y = fmaf(s_w[r], s_part[tid * k + r], y);
-            const int d = d_begin + tid;
-            Y.y[d] = y;
-            if (Y.x_next) {
-                if constexpr (sizeof(XT) == 2)
-                    reinterpret_cast<__nv_bfloat16*>(Y.x_next)[d] = __float2bfloat16_rn(s_x[d] + y);
-                else
-                    reinterpret_cast<float*>(Y.x_next)[d] = s_x[d] + y;
+        // combine, two rows per thread (a CTA's rows come in pairs):
+        // y[d] = sum_r w[r] * o_r[d] in slot order, x_next = x + y; in a stack
+        // the x_next pair is also published as one tagged word
+        if (2 * tid < nrows) {
+            const int d = d_begin + 2 * tid;
+            float y0 = 0.f, y1 = 0.f;
+#pragma unroll 4
+            for (int r = 0; r < k; r++) {
+                if (s_idx[r] >= 0) {
+                    y0 = fmaf(s_w[r], s_part[(2 * tid) * k + r], y0);
+                    y1 = fmaf(s_w[r], s_part[(2 * tid + 1) * k + r], y1);
+                }
+            }
+            *reinterpret_cast<float2*>(Y.y + d) = make_float2(y0, y1);
+            const bool publish = l + 1 < P.nlayers;
+            if constexpr (sizeof(XT) == 2) {
+                const __nv_bfloat162 xn = __floats2bfloat162_rn(s_x[d] + y0, s_x[d + 1] + y1);
+                if (Y.x_next) *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(Y.x_next) + d) = xn;
+                if (publish) st_tagged_u32(P.xex + d / 2, *reinterpret_cast<const uint32_t*>(&xn), tag);
+            } else {
+                const float x0 = s_x[d] + y0, x1 = s_x[d + 1] + y1;
+                if (Y.x_next) *reinterpret_cast<float2*>(static_cast<float*>(Y.x_next) + d) = make_float2(x0, x1);
+                if (publish) {
+                    st_tagged(P.xex + d, x0, tag);
+                    st_tagged(P.xex + d + 1, x1, tag);
+                }
             }
         }
-        if (l + 1 < P.nlayers) {
-            const bool any_ab = __syncthreads_or(ab);
-            if (tid == 0) {
-                __threadfence();
-                st_release_u32(flag_x + c, tag);
-            }
-            if (any_ab) break;
-        }
+        if (l + 1 < P.nlayers && __syncthreads_or(ab)) break;
     }
     // a router copy requested for a layer that did not run must land before
     // this CTA's shared memory is released
@@ -706,11 +895,13 @@ bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes,
                 FusedCommon* fc, size_t* smem, int* grid) {
     const int G = std::min(std::min(device_sm_count(), D / 2), kFusedMaxGrid);
     if (G < 1 || k < 1 || k > 32 || E < k || E > 2 * kFThreads) return false;
+    if (F % kBlk || D % kBlk || (long)k * F > 32 * kFWarps * kChunk) return false;
     const int rows = 2 * ((D / 2 + G - 1) / G);
     const int rowD = qbits == 8 ? D : D / 2;
     if (rowD / 16 > 32 * kNCH) return false;
-    if (F % kBlk || D % kBlk) return false;
-    if (((F / kBlk) * s_bytes) % 16) return false;  // bulk copies of whole scale rows
+    if ((qbits == 8 ? F : F / 2) / 8 > 32 * kNPL) return false;
+    // bulk copies of whole scale rows of the down matrices
+    if (((F / kBlk) * s_bytes) % 16) return false;
     if (has_router) {
         const int nexp = fused_nexp(E, G);
         const int nseg = kFWarps / pow2ceil(nexp);
@@ -735,7 +926,7 @@ bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes,
     return true;
 }
 
-template <int QB, typename ST, typename XT>
+template <int QB, typename ST, typename XT, class SH>
 static cudaError_t launch_fused_t(const FusedCommon& fc, const FusedLayer* layers, int grid, size_t smem,
                                   cudaStream_t s) {
     const dim3 g(grid), b(kFThreads);
@@ -744,27 +935,45 @@ static cudaError_t launch_fused_t(const FusedCommon& fc, const FusedLayer* layer
         a.c = fc;
         a.c.nlayers = 1;
         a.L[0] = layers[0];
-        return launch(fused_layer_kernel<QB, ST, XT, 1>, g, b, smem, s, true, a);
+        return launch(fused_layer_kernel<QB, ST, XT, 1, SH>, g, b, smem, s, true, a);
     }
     if (fc.nlayers > kStackMax) return cudaErrorInvalidValue;
     FusedArgs<kStackMax> a = {};
     a.c = fc;
     for (int l = 0; l < fc.nlayers; l++) a.L[l] = layers[l];
-    return launch(fused_layer_kernel<QB, ST, XT, kStackMax>, g, b, smem, s, true, a);
+    return launch(fused_layer_kernel<QB, ST, XT, kStackMax, SH>, g, b, smem, s, true, a);
+}
+
+// The shapes with a compile-time instantiation: 256 experts top-8, d_model
+// 2048, d_ff 768 (int8, fp16 scales, bf16 x) and 512 experts top-10, d_model
+// 2048, d_ff 512 (int4, fp16 scales, bf16 x); everything else runs the
+// runtime-shape instantiation.
+template <int QB, typename ST, typename XT>
+static cudaError_t launch_fused_shape(const FusedCommon& fc, const FusedLayer* layers, int grid, size_t smem,
+                                      cudaStream_t s) {
+    if constexpr (QB == 8 && sizeof(ST) == 2 && sizeof(XT) == 2) {
+        if (fc.E == 256 && fc.k == 8 && fc.D == 2048 && fc.F == 768)
+            return launch_fused_t<QB, ST, XT, FShape<256, 8, 2048, 768>>(fc, layers, grid, smem, s);
+    }
+    if constexpr (QB == 4 && sizeof(ST) == 2 && sizeof(XT) == 2) {
+        if (fc.E == 512 && fc.k == 10 && fc.D == 2048 && fc.F == 512)
+            return launch_fused_t<QB, ST, XT, FShape<512, 10, 2048, 512>>(fc, layers, grid, smem, s);
+    }
+    return launch_fused_t<QB, ST, XT, FRuntime>(fc, layers, grid, smem, s);
 }
 
 cudaError_t launch_fused(const FusedCommon& fc, const FusedLayer* layers, int qbits, bool s_f16, bool x_bf16,
                          int grid, size_t smem, cudaStream_t s) {
     if (qbits == 8) {
-        if (s_f16) return x_bf16 ? launch_fused_t<8, __half, __nv_bfloat16>(fc, layers, grid, smem, s)
-                                  : launch_fused_t<8, __half, float>(fc, layers, grid, smem, s);
-        return x_bf16 ? launch_fused_t<8, float, __nv_bfloat16>(fc, layers, grid, smem, s)
-                      : launch_fused_t<8, float, float>(fc, layers, grid, smem, s);
+        if (s_f16) return x_bf16 ? launch_fused_shape<8, __half, __nv_bfloat16>(fc, layers, grid, smem, s)
+                                  : launch_fused_shape<8, __half, float>(fc, layers, grid, smem, s);
+        return x_bf16 ? launch_fused_shape<8, float, __nv_bfloat16>(fc, layers, grid, smem, s)
+                      : launch_fused_shape<8, float, float>(fc, layers, grid, smem, s);
     }
-    if (s_f16) return x_bf16 ? launch_fused_t<4, __half, __nv_bfloat16>(fc, layers, grid, smem, s)
-                              : launch_fused_t<4, __half, float>(fc, layers, grid, smem, s);
-    return x_bf16 ? launch_fused_t<4, float, __nv_bfloat16>(fc, layers, grid, smem, s)
-                  : launch_fused_t<4, float, float>(fc, layers, grid, smem, s);
+    if (s_f16) return x_bf16 ? launch_fused_shape<4, __half, __nv_bfloat16>(fc, layers, grid, smem, s)
+                              : launch_fused_shape<4, __half, float>(fc, layers, grid, smem, s);
+    return x_bf16 ? launch_fused_shape<4, float, __nv_bfloat16>(fc, layers, grid, smem, s)
+                  : launch_fused_shape<4, float, float>(fc, layers, grid, smem, s);
 }
 
 }  // namespace moe

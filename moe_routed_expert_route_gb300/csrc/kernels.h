@@ -131,8 +131,8 @@ struct FusedCommon {
     int pad;
     WsHeader* hdr;
     uint64_t* logits;         // workspace [E], tagged values
-    float* h;                 // workspace [k*F] activations
-    unsigned* flags;          // workspace [2][kFusedMaxGrid] per-CTA completion tags
+    uint64_t* h;              // workspace [k*F], tagged activations
+    uint64_t* xex;            // workspace [D] (stacks only): a layer's x_next, tagged
 };
 
 constexpr int kFusedMaxGrid = 1024;  // CTAs of the layer kernel (<= SMs)

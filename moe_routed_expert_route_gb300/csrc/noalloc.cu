@@ -17,15 +17,13 @@ namespace moe {
 namespace {
 
 // Scratch of the layer kernel: header (status word, launch sequence number,
-// wait limit), the E tagged logits, the k*F activations and the per-CTA
-// completion flags.
+// wait limit), the E tagged logits and the k*F tagged activations.
 constexpr int kNoAllocMaxE = 1024;
 constexpr int kNoAllocMaxKF = 32768;
 constexpr size_t kNoAllocHeader = 256;
 constexpr size_t kNoAllocLogits = sizeof(uint64_t) * kNoAllocMaxE;
-constexpr size_t kNoAllocH = sizeof(float) * kNoAllocMaxKF;
-constexpr size_t kNoAllocFlags = sizeof(unsigned) * 2 * kFusedMaxGrid;
-constexpr size_t kNoAllocBytes = kNoAllocHeader + kNoAllocLogits + kNoAllocH + kNoAllocFlags;  // 147,712 B
+constexpr size_t kNoAllocH = sizeof(uint64_t) * kNoAllocMaxKF;
+constexpr size_t kNoAllocBytes = kNoAllocHeader + kNoAllocLogits + kNoAllocH;  // 270,592 B
 static_assert(sizeof(WsHeader) == kNoAllocHeader, "header size");
 
 // Zero-initialised at load time; shared by every call on the device.
@@ -75,7 +73,7 @@ extern "C" moe_status_t moe_layer_noalloc(const moe_router_t* router, const moe_
                            experts->up_s, experts->down_q, experts->down_s};
     for (const void* p : ptrs)
         if (!al16(p)) return MOE_ERR_INVALID_ARG;
-    if (!idx || !w || !y || (x_next && !al16(x_next))) return MOE_ERR_INVALID_ARG;
+    if (!idx || !w || !al16(y) || (x_next && !al16(x_next))) return MOE_ERR_INVALID_ARG;
     if (router->bias && ((uintptr_t)router->bias & 3u)) return MOE_ERR_INVALID_ARG;
 
     const int qbits = experts->q == MOE_Q_INT8_SYM_B32 ? 8 : 4;
@@ -107,8 +105,8 @@ extern "C" moe_status_t moe_layer_noalloc(const moe_router_t* router, const moe_
     fc.norm_topk = router->norm_topk ? 1 : 0;
     fc.hdr = reinterpret_cast<WsHeader*>(base);
     fc.logits = reinterpret_cast<uint64_t*>(base + kNoAllocHeader);
-    fc.h = reinterpret_cast<float*>(base + kNoAllocHeader + kNoAllocLogits);
-    fc.flags = reinterpret_cast<unsigned*>(base + kNoAllocHeader + kNoAllocLogits + kNoAllocH);
+    fc.h = reinterpret_cast<uint64_t*>(base + kNoAllocHeader + kNoAllocLogits);
+    fc.xex = nullptr;  // one layer: no layer output is exchanged
     FusedLayer ly = {};
     ly.W = router->W;
     ly.bias = router->bias;

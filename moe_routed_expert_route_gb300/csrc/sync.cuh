@@ -37,6 +37,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         : "memory");
 }
 
+// Prefetch of `bytes` (multiple of 16, 16-byte aligned) of global memory into
+// L2, without waiting and without a destination.
+__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned phase) {
     unsigned done;
     asm volatile(
@@ -99,6 +105,15 @@ __device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
     uint64_t w;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
     return w;
+}
+// A 32-bit payload (a float, or two 16-bit values) under a tag.
+__device__ __forceinline__ void st_tagged_u32(uint64_t* p, uint32_t v, unsigned tag) {
+    uint64_t w = ((uint64_t)tag << 32) | v;
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+// Two consecutive tagged words (16-byte aligned); each is read single-copy atomically.
+__device__ __forceinline__ void ld_tagged2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 __device__ __forceinline__ bool tag_ok(uint64_t w, unsigned tag) { return (unsigned)(w >> 32) == tag; }
 __device__ __forceinline__ float tag_val(uint64_t w) { return __uint_as_float((unsigned)w); }
