@@ -120,6 +120,27 @@ __device__ __forceinline__ int cand_before(uint2 a, uint2 b) {
     return (a.x > b.x || (a.x == b.x && a.y < b.y)) ? 1 : 0;
 }
 
+// Called by the whole CTA: writes the candidates of list[0..n) whose rank
+// (number of entries ordered before them) is below k to out[rank]. Eight
+// threads share a candidate, each comparing it with every eighth entry.
+__device__ __forceinline__ void rank_candidates(const uint2* list, int n, int k, uint2* out, int tid) {
+    const int q = tid & 7;
+#pragma unroll 1
+    for (int base = 0; base < n; base += kFThreads / 8) {
+        const int i = base + (tid >> 3);
+        const uint2 me = i < n ? list[i] : make_uint2(0u, 0u);
+        int part = 0;
+        if (me.x != 0u) {
+#pragma unroll 4
+            for (int j = q; j < n; j += 8) part += cand_before(list[j], me);
+        }
+        part += __shfl_xor_sync(kFull, part, 1);
+        part += __shfl_xor_sync(kFull, part, 2);
+        part += __shfl_xor_sync(kFull, part, 4);
+        if (me.x != 0u && q == 0 && part < k) out[part] = me;
+    }
+}
+
 // Called by a whole warp: brings the n tagged words src[0..n) of the chunks
 // c = warp, warp + 16, ... (kChunk words each) into dst (same offsets) by bulk
 // copies, re-copying any chunk that still holds a word without `tag`, until
@@ -470,16 +491,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             }
             __syncthreads();
             // the k best candidates, by each candidate's rank among all of them
-            const int C = nvw * k;
-#pragma unroll 1
-            for (int i = tid; i < C; i += kFThreads) {
-                const uint2 me = s_cand[i];
-                if (me.x == 0u) continue;
-                int rank = 0;
-#pragma unroll 8
-                for (int j2 = 0; j2 < C; j2++) rank += cand_before(s_cand[j2], me);
-                if (rank < k) s_sel[rank] = me;
-            }
+            // (eight threads per candidate, each comparing with every eighth entry)
+            rank_candidates(s_cand, nvw * k, k, s_sel, tid);
             __syncthreads();
             if (Y.resident) {
                 // replacement candidates: resident experts outside the chosen k,
@@ -495,15 +508,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                         if (s_rcand[i].x != 0u && s_sel[r].y == e) s_rcand[i].x = 0u;
                 }
                 __syncthreads();
-#pragma unroll 1
-                for (int i = tid; i < RC; i += kFThreads) {
-                    const uint2 me = s_rcand[i];
-                    if (me.x == 0u) continue;
-                    int rank = 0;
-#pragma unroll 8
-                    for (int j2 = 0; j2 < RC; j2++) rank += cand_before(s_rcand[j2], me);
-                    if (rank < k) s_sel[32 + rank] = me;
-                }
+                rank_candidates(s_rcand, RC, k, s_sel + 32, tid);
                 __syncthreads();
             }
             if (warp == 0) {
@@ -564,37 +569,11 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
         __syncthreads();
 
         // ------------------------------------------------------ phase 3
-        // one thread starts bulk copies of this CTA's rows of the k down
-        // matrices (and, in a stack, the next layer's router rows); the warps
-        // stream their share of the gate/up row pairs with 16-byte loads, two
-        // pairs in flight per warp, and publish h = silu(g)*u (tagged)
-        if (tid == 0) {
-            // the whole of this CTA's gate/up rows (consecutive units are
-            // consecutive rows of one expert) are requested into L2 at once, so
-            // that HBM streams them at full rate while the warps' loads find them
-            const uint8_t* GQp = reinterpret_cast<const uint8_t*>(Y.gate_q);
-            const uint8_t* UQp = reinterpret_cast<const uint8_t*>(Y.up_q);
-            const ST* GSp = reinterpret_cast<const ST*>(Y.gate_s);
-            const ST* USp = reinterpret_cast<const ST*>(Y.up_s);
-#pragma unroll 1
-            for (int g0 = g_begin; g0 < g_end;) {
-                const int r = g0 / F, n0 = g0 - r * F;
-                const int n1 = min(F, n0 + (g_end - g0));
-                const int e = s_idx[r];
-                if (e >= 0) {
-                    const size_t row = (size_t)e * F + n0;
-                    const unsigned cb = (unsigned)((n1 - n0) * rowD), sbb = (unsigned)((n1 - n0) * nb * sizeof(ST));
-                    prefetch_l2(GQp + row * rowD, cb);
-                    prefetch_l2(UQp + row * rowD, cb);
-                    if (sbb % 16 == 0) {
-                        prefetch_l2(GSp + row * nb, sbb);
-                        prefetch_l2(USp + row * nb, sbb);
-                    }
-                }
-                g0 += n1 - n0;
-            }
-        }
-        if (tid == 32) {
+        // the warps stream their share of the gate/up row pairs with 16-byte
+        // loads, two pairs in flight per warp, and publish h = silu(g)*u
+        // (tagged); then one thread starts bulk copies of this CTA's rows of the
+        // k down matrices (and, in a stack, the next layer's router rows)
+        auto issue_down = [&]() {
             unsigned bytes = 0;
 #pragma unroll 1
             for (int r = 0; r < k; r++)
@@ -612,7 +591,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             }
             // the next layer's router rows (its pointers were loaded before the last barrier)
             if (l + 1 < P.nlayers && P.has_router) request_router(s_ly[(l + 1) & 1]);
-        }
+        };
         if (l + 1 < P.nlayers && P.has_router) router_next = l + 1;
 
         const uint8_t* GQ = reinterpret_cast<const uint8_t*>(Y.gate_q);
@@ -690,6 +669,10 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             }
         }
 
+        // the down rows are requested once this warp's share of gate/up is
+        // in: the gate/up bytes, which the activation exchange waits for, go
+        // first, and the down rows stream in during that exchange
+        if (tid == 32) issue_down();
         // ------------------------------------------------------ phase 4
         // every slot's activations: each warp stages its chunks of the tagged
         // words (re-copying chunks that are not all there yet) and turns them
