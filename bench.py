@@ -46,7 +46,7 @@ L2_BYTES = 129 * 1024 * 1024
 # single-token layer kernel on one layer of the headline workload, from the ncu
 # capture summarised in the named file. Reported only while the kernel source
 # is the one that capture measured (same sha256 prefix of csrc/fused.cu).
-LAYER_KERNEL_TRAFFIC = {"fused_sha16": None, "bytes_per_layer": None,
+LAYER_KERNEL_TRAFFIC = {"fused_sha16": "2d0a82babcda8407", "bytes_per_layer": (82_425_344 + 1_845_760) // 2,
                         "source": "profiles/fused_layer_kernel_decode_E256_k8.md"}
 
 
@@ -222,12 +222,14 @@ def time_graph(graph, stream, steps, warmup, world=1, dev=None):
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps):
             graph.replay()
         end.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     ms = start.elapsed_time(end)
     if world > 1:
         ms = max_over_ranks(ms, dev)
