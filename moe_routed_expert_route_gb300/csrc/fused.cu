@@ -46,6 +46,7 @@
 #include "dots.cuh"
 #include "kernels.h"
 #include "sync.cuh"
+#include "tc.cuh"
 
 namespace moe {
 
@@ -653,21 +654,82 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             if (lane == 0 && g < g_end) st_tagged(P.h + g, silu_mul(ga, ua), tag);
         };
         {
+            // a warp's pairs are g0 + 16j; the first two go to registers, the
+            // third is copied into this warp's slot of the staging region (idle
+            // until the activation exchange) by cp.async at once, so every
+            // pair of the warp is requested before any has arrived; further
+            // pairs refill the registers
+            const int g0 = g_begin + warp;
+            const int pair_bytes = 2 * rowD + 2 * nb * (int)sizeof(ST);
+            const bool third = g0 + 2 * kFWarps < g_end && (nb * (int)sizeof(ST)) % 16 == 0 &&
+                               (warp + 1) * pair_bytes <= (int)(sizeof(uint64_t) * (size_t)(k * F > D ? k * F : D));
+            uint8_t* slot = reinterpret_cast<uint8_t*>(s_stage) + (size_t)warp * pair_bytes;
             RowPair<QB, ST> A, B;
-            int g = g_begin + warp;
-            load_pair(g, A);
+            load_pair(g0, A);
+            load_pair(g0 + kFWarps, B);
+            if (third) {
+                const int g = g0 + 2 * kFWarps, r = g / F, n = g - r * F;
+                const int e = s_idx[r];
+                const size_t row = (size_t)(e >= 0 ? e : 0) * F + n;
+                const int sbytes = nb * (int)sizeof(ST);
 #pragma unroll 1
-            while (g < g_end) {
-                const int g2 = g + kFWarps;
-                load_pair(g2, B);
-                finish_pair(g, A);
-                if (g2 >= g_end) break;
-                const int g3 = g2 + kFWarps;
-                load_pair(g3, A);
-                finish_pair(g2, B);
-                g = g3;
+                for (int ci = lane; ci < nchunk; ci += 32) {
+                    cp_async16(slot + 16 * ci, GQ + row * rowD + 16 * ci);
+                    cp_async16(slot + rowD + 16 * ci, UQ + row * rowD + 16 * ci);
+                }
+#pragma unroll 1
+                for (int ci = lane; ci < sbytes / 16; ci += 32) {
+                    cp_async16(slot + 2 * rowD + 16 * ci, reinterpret_cast<const uint8_t*>(GS + row * nb) + 16 * ci);
+                    cp_async16(slot + 2 * rowD + sbytes + 16 * ci,
+                               reinterpret_cast<const uint8_t*>(US + row * nb) + 16 * ci);
+                }
+                cp_async_commit();
+            }
+            finish_pair(g0, A);
+            finish_pair(g0 + kFWarps, B);
+            int g = g0 + 2 * kFWarps;
+            if (third) {
+                cp_async_wait<0>();
+                __syncwarp();
+                RowPair<QB, ST> S;
+                const ST* gsc = reinterpret_cast<const ST*>(slot + 2 * rowD);
+                const ST* usc = gsc + nb;
+#pragma unroll
+                for (int q = 0; q < kNCH; q++) {
+                    const int ci = q * 32 + lane;
+                    const bool ok = ci < nchunk;
+                    S.g[q] = ok ? *reinterpret_cast<const uint4*>(slot + 16 * ci) : make_uint4(0, 0, 0, 0);
+                    S.u[q] = ok ? *reinterpret_cast<const uint4*>(slot + rowD + 16 * ci) : make_uint4(0, 0, 0, 0);
+                    const int blk = QB == 8 ? (ci >> 1) : ci;
+                    S.gs[q] = ok ? gsc[blk] : ST(0.f);
+                    S.us[q] = ok ? usc[blk] : ST(0.f);
+                }
+                if (s_idx[g / F] < 0) {  // an expert slot without an id: nothing was meant to be read
+#pragma unroll
+                    for (int q = 0; q < kNCH; q++) {
+                        S.g[q] = S.u[q] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                finish_pair(g, S);
+                g += kFWarps;
+            }
+            // pairs beyond those: two in flight in registers
+            if (g < g_end) {
+                load_pair(g, A);
+#pragma unroll 1
+                while (g < g_end) {
+                    const int g2 = g + kFWarps;
+                    load_pair(g2, B);
+                    finish_pair(g, A);
+                    if (g2 >= g_end) break;
+                    const int g3 = g2 + kFWarps;
+                    load_pair(g3, A);
+                    finish_pair(g2, B);
+                    g = g3;
+                }
             }
         }
+        __syncthreads();  // the staging region is free again
 
         // the down rows are requested once this warp's share of gate/up is
         // in: the gate/up bytes, which the activation exchange waits for, go

@@ -407,31 +407,34 @@ def test_layer_stack_independent_equals_single_layers(cfg1_layers):
 
 # ------------------------------------------------------ bounded waits
 
-def test_wait_limit_runs_out_and_the_workspace_recovers():
-    """A wait limit of a few cycles makes the layer kernel's cross-CTA waits
-    run out: the call must finish, record MOE_ERR_DEVICE_TIMEOUT, and the same
-    workspace must give correct results once the limit is restored."""
-    cfg = small_cfg(256, 8, 2048, 768, cfg_id=95)
-    layer = W.make_layer(cfg, 0, DEV, chunk=64)
-    router = M.Router(layer["Wr"], layer["bias"], cfg.k)
-    experts = M.Experts.from_layer(layer, cfg.qbits)
+def test_wait_limit_runs_out_and_the_workspace_recovers(cfg1_layers):
+    """A wait limit of a few cycles makes the layer kernel's cross-CTA waits run
+    out: a three-layer stack waits, at every layer boundary, for the slowest
+    CTA's output, which never arrives within 16 cycles. The call must finish,
+    record MOE_ERR_DEVICE_TIMEOUT, and the same workspace must give correct
+    results once the limit is restored."""
+    cfg, layers = cfg1_layers
+    L = len(layers)
+    routers = [M.Router(lw["Wr"], lw["bias"], cfg.k) for lw in layers]
+    experts = [M.Experts.from_layer(lw, cfg.qbits) for lw in layers]
     ws = M.workspace(M.MOE_OP_LAYER, 1, cfg.k, cfg.E, cfg.D, cfg.F, DEV)
-    x = W.make_tokens(cfg, 1, 5, DEV)
-    idx = torch.empty(1, cfg.k, dtype=torch.int32, device=DEV)
-    w = torch.empty(1, cfg.k, device=DEV)
-    y = torch.empty(1, cfg.D, device=DEV)
+    xs = [W.make_tokens(cfg, 1, 50 + l, DEV) for l in range(L)]
+    idx = [torch.empty(1, cfg.k, dtype=torch.int32, device=DEV) for _ in range(L)]
+    w = [torch.empty(1, cfg.k, device=DEV) for _ in range(L)]
+    y = [torch.empty(1, cfg.D, device=DEV) for _ in range(L)]
     M.moe_set_wait_limit(ws, 16)
-    M.moe_layer(router, experts, x, idx, w, None, y, None, ws)
+    M.moe_layer_stack(routers, experts, xs, False, idx, w, y, None, ws)
     assert M.moe_check_status(ws) == M.MOE_ERR_DEVICE_TIMEOUT
     assert M.moe_check_status(ws) == M.MOE_OK  # cleared by the read
     M.moe_set_wait_limit(ws, 0)
-    got = gpu_layer(cfg, layer, x)
-    M.moe_layer(router, experts, x, idx, w, None, y, None, ws)
+    M.moe_layer_stack(routers, experts, xs, False, idx, w, y, None, ws)
     assert M.moe_check_status(ws) == M.MOE_OK
-    assert torch.equal(idx.cpu(), got["idx"]) and torch.equal(y.cpu(), got["y"])
-    ref = oracle.router(x, layer["Wr"], layer["bias"], cfg.k)
-    check_routing(ref, dict(idx=idx.cpu(), w=w.cpu()), cfg.k, max_skip_frac=1.0, label="after a timeout")
-    check_y(layer, x, dict(idx=idx.cpu(), w=w.cpu(), y=y.cpu()), cfg.qbits)
+    for l in range(L):
+        one = gpu_layer(cfg, layers[l], xs[l], probs=False)
+        assert torch.equal(one["idx"], idx[l].cpu()) and torch.equal(one["y"], y[l].cpu())
+        ref = oracle.router(xs[l], layers[l]["Wr"], layers[l]["bias"], cfg.k)
+        check_routing(ref, dict(idx=idx[l].cpu(), w=w[l].cpu()), cfg.k, max_skip_frac=1.0, label="after a timeout")
+        check_y(layers[l], xs[l], dict(idx=idx[l].cpu(), w=w[l].cpu(), y=y[l].cpu()), cfg.qbits)
 
 
 # ------------------------------------------------------------- edge cases
