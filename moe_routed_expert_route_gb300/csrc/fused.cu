@@ -52,7 +52,6 @@ namespace moe {
 
 constexpr int kFThreads = 512;
 constexpr int kFWarps = 16;
-constexpr int kNRC = 4;      // router 16-byte chunks per lane
 constexpr int kNCH = 4;      // gate/up 16-byte chunks per lane
 constexpr int kDP = 8;       // down rows per warp task pass (computed together)
 constexpr int kNPL = 4;      // 8-byte down pieces per lane (F <= 1024 int8, 2048 int4)
@@ -213,7 +212,6 @@ template <int QB, typename ST, typename XT, int NL, class SH>
 __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_constant__ FusedArgs<NL> a) {
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ FusedLayer s_ly[2];  // this layer's and the next layer's pointers
-    __shared__ float s_rpart[kFWarps];
     __shared__ float s_rmax[kFWarps];
     __shared__ float s_rsum[kFWarps];
     __shared__ int s_idx[32];  // experts read per slot (after substitution), -1 = none
@@ -256,10 +254,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     const long total = (long)k * F;
     const int g_begin = (int)((long)c * total / G), g_end = (int)((long)(c + 1) * total / G);
     const int e_begin = (int)((long)c * E / G), e_end = (int)((long)(c + 1) * E / G);
-    const int nseg = P.router_nseg;
-    const int rj = warp / nseg, rs = warp - rj * nseg;
-    const int seg = D / nseg;
-    const bool rvalid = P.has_router && e_begin + rj < e_end;
     constexpr int EPC = 16 / sizeof(XT);
     const int nvw = (E + 31) / 32;
     const int nxw = sizeof(XT) == 2 ? D / 2 : D;  // tagged words of a layer's x_next
@@ -310,9 +304,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     for (int l = 0; l < P.nlayers; l++) {
         const FusedLayer& Y = s_ly[l & 1];
         const unsigned tag = seq_tag(seq0 + (unsigned)l);
-        // requested now, used after the logits: bias of this CTA's experts and
-        // the residency of the experts this thread selects among
-        const float bias_r = (P.has_router && Y.bias && tid < e_end - e_begin) ? Y.bias[e_begin + tid] : 0.f;
+        // requested now, used after the logits: the residency of the experts
+        // this thread selects among
         const int e0 = tid, e1 = tid + kFThreads;
         const bool res0 = Y.resident && e0 < E && Y.resident[e0];
         const bool res1 = Y.resident && e1 < E && Y.resident[e1];
@@ -351,38 +344,34 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
         __syncthreads();
 
         if (P.has_router) {
-            if (!mbar_wait(&s_rbar, l & 1, status, lim)) {
-                ab = true;
-                mbar_wait(&s_rbar, l & 1, status);  // the copy must land before anything else happens
-            }
-            router_next = -1;
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < kNRC; i++) {
-                const int ci = i * 32 + lane;
-                if (rvalid && ci * EPC < seg) {
-                    const float* xs = s_x + rs * seg + ci * EPC;
-                    const uint4 wq4 = *reinterpret_cast<const uint4*>(s_wr + (size_t)rj * D + rs * seg + ci * EPC);
+            // one warp per expert of this CTA: the whole row against x, in
+            // 16-byte pieces from shared memory, published without a barrier
+            if (warp < e_end - e_begin) {
+                if (!mbar_wait(&s_rbar, l & 1, status, lim)) {
+                    ab = true;
+                    mbar_wait(&s_rbar, l & 1, status);  // the copy must land before anything else happens
+                }
+                const XT* wrow = s_wr + (size_t)warp * D;
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+                for (int ci = lane; ci * EPC < D; ci += 32) {
+                    const float* xs = s_x + ci * EPC;
+                    const uint4 wq4 = *reinterpret_cast<const uint4*>(wrow + ci * EPC);
                     const uint32_t* wq = reinterpret_cast<const uint32_t*>(&wq4);
 #pragma unroll
                     for (int q = 0; q < EPC; q++) {
                         float wf;
                         if constexpr (sizeof(XT) == 2) wf = (q & 1) ? bf16hi(wq[q >> 1]) : bf16lo(wq[q >> 1]);
                         else wf = __uint_as_float(wq[q]);
-                        acc = fmaf(wf, xs[q], acc);
+                        if (q & 1) acc1 = fmaf(wf, xs[q], acc1);
+                        else acc0 = fmaf(wf, xs[q], acc0);
                     }
                 }
+                const float acc = warp_sum(acc0 + acc1);
+                if (lane == 0) st_tagged(P.logits + e_begin + warp, Y.bias ? acc + Y.bias[e_begin + warp] : acc, tag);
             }
-            acc = warp_sum(acc);
-            if (lane == 0) s_rpart[warp] = acc;
+            router_next = -1;
             __syncthreads();
-            if (tid < e_end - e_begin) {
-                float lg = 0.f;
-#pragma unroll 4
-                for (int s2 = 0; s2 < nseg; s2++) lg += s_rpart[tid * nseg + s2];
-                if (Y.bias) lg += bias_r;
-                st_tagged(P.logits + e_begin + tid, lg, tag);
-            }
         } else if (tid < k) {
             int e = ld_cg_i32(Y.idx_in + tid);
             if (e < 0 || e >= E) {
@@ -929,12 +918,6 @@ int device_sm_count() {
     return cache[dev];
 }
 
-static int pow2ceil(int v) {
-    int p = 1;
-    while (p < v) p <<= 1;
-    return p;
-}
-
 // Grid and per-CTA shape for one layer; false if the fused kernel cannot run it.
 bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes, bool has_router,
                 FusedCommon* fc, size_t* smem, int* grid) {
@@ -947,17 +930,9 @@ bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes,
     if ((qbits == 8 ? F : F / 2) / 8 > 32 * kNPL) return false;
     // bulk copies of whole scale rows of the down matrices
     if (((F / kBlk) * s_bytes) % 16) return false;
-    if (has_router) {
-        const int nexp = fused_nexp(E, G);
-        const int nseg = kFWarps / pow2ceil(nexp);
-        if (nseg < 1 || D % nseg) return false;
-        const int seg = D / nseg;
-        const int epc = 16 / x_bytes;
-        if (seg % epc || seg / epc > 32 * kNRC) return false;
-        fc->router_nseg = nseg;
-    } else {
-        fc->router_nseg = 1;
-    }
+    // one warp per router expert of a CTA
+    if (has_router && fused_nexp(E, G) > kFWarps) return false;
+    fc->router_nseg = 1;
     const FusedLayout L = fused_layout(E, D, F, k, qbits, s_bytes, x_bytes, rows, G);
     if (L.total > 220 * 1024) return false;
     fc->E = E;
