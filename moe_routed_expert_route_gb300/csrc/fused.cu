@@ -114,16 +114,44 @@ __device__ __forceinline__ void fx_store_block1(float v, int blk, int lane, int 
     if (lane == 0) scale[blk] = f.scale;
 }
 
-// Candidate order: {fp32 bits of p + 1, id} (x = 0: no expert); a ranks
-// before b when its probability is larger, or equal with a lower id.
+// Max and sum of the 16 per-warp partials, in a fixed order.
+__device__ __forceinline__ float block_max16(const float* v) {
+    float m2[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) m2[q] = fmaxf(fmaxf(v[4 * q], v[4 * q + 1]), fmaxf(v[4 * q + 2], v[4 * q + 3]));
+    return fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3]));
+}
+__device__ __forceinline__ float block_sum16(const float* v) {
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < kFWarps; i++) sum += v[i];
+    return sum;
+}
+
+// Routing key of a logit: its fp32 bits mapped to an unsigned integer of the
+// same order (negative values complemented, the sign bit set on the others),
+// so that a larger logit has a larger key; 0 is kept for "no expert".
+// Softmax is monotonic, so ranking logits ranks the probabilities.
+__device__ __forceinline__ unsigned logit_key(float v) {
+    const unsigned b = __float_as_uint(v);
+    const unsigned u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return u ? u : 1u;
+}
+__device__ __forceinline__ float key_logit(unsigned u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// Candidate order: {logit key, id} (key 0: no expert); a ranks before b when
+// its logit is larger, or equal with a lower id.
 __device__ __forceinline__ int cand_before(uint2 a, uint2 b) {
     return (a.x > b.x || (a.x == b.x && a.y < b.y)) ? 1 : 0;
 }
 
 // Called by the whole CTA: writes the candidates of list[0..n) whose rank
-// (number of entries ordered before them) is below k to out[rank]. Eight
+// (number of entries ordered before them) is below k to out[rank] (and their
+// ids to ids[rank] when ids is given). Eight
 // threads share a candidate, each comparing it with every eighth entry.
-__device__ __forceinline__ void rank_candidates(const uint2* list, int n, int k, uint2* out, int tid) {
+__device__ __forceinline__ void rank_candidates(const uint2* list, int n, int k, uint2* out, int* ids, int tid) {
     const int q = tid & 7;
 #pragma unroll 1
     for (int base = 0; base < n; base += kFThreads / 8) {
@@ -137,7 +165,10 @@ __device__ __forceinline__ void rank_candidates(const uint2* list, int n, int k,
         part += __shfl_xor_sync(kFull, part, 1);
         part += __shfl_xor_sync(kFull, part, 2);
         part += __shfl_xor_sync(kFull, part, 4);
-        if (me.x != 0u && q == 0 && part < k) out[part] = me;
+        if (me.x != 0u && q == 0 && part < k) {
+            out[part] = me;
+            if (ids) ids[part] = (int)me.y;
+        }
     }
 }
 
@@ -304,11 +335,75 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     for (int l = 0; l < P.nlayers; l++) {
         const FusedLayer& Y = s_ly[l & 1];
         const unsigned tag = seq_tag(seq0 + (unsigned)l);
-        // requested now, used after the logits: the residency of the experts
-        // this thread selects among
+        // requested now, used later: the residency of the experts this thread
+        // selects among, and the bias of the expert this warp scores
         const int e0 = tid, e1 = tid + kFThreads;
         const bool res0 = Y.resident && e0 < E && Y.resident[e0];
         const bool res1 = Y.resident && e1 < E && Y.resident[e1];
+        const float bias_w = (P.has_router && Y.bias && warp < e_end - e_begin) ? Y.bias[e_begin + warp] : 0.f;
+
+        // Called by warp 0 once the k slots are ranked: each slot's weight is
+        // its softmax probability exp(l - max) / sum (the block max and the
+        // fixed-order sum of the per-warp partials), renormalised over the k
+        // when norm_topk; with residency, the substitution rule then sets the
+        // slots' experts. Writes the slots' weights (and experts) to shared
+        // memory and, in CTA 0, the routing outputs.
+        auto route_weights = [&](bool resident) {
+            const float mx = block_max16(s_rmax);
+            const float inv_s = 1.0f / block_sum16(s_rsum);
+            const uint2 sel = lane < k ? s_sel[lane] : make_uint2(0u, 0u);
+            const int sel_e = sel.x ? (int)sel.y : -1;
+            const float sel_p = sel.x ? expf(key_logit(sel.x) - mx) * inv_s : 0.f;
+            const float norm = warp_sum(lane < k ? sel_p : 0.f);
+            const float wv = P.norm_topk ? sel_p / norm : sel_p;
+            int use_e = sel_e;
+            unsigned flg = 0;
+            if (resident) {
+                const bool my_res = lane < k && sel_e >= 0 && Y.resident[sel_e];
+                float mass = 0.f;
+                int nrep = 0;  // replacements used so far
+#pragma unroll 1
+                for (int r = 0; r < k; r++) {
+                    const int er = __shfl_sync(kFull, sel_e, r);
+                    const float wr = __shfl_sync(kFull, wv, r);
+                    const bool rr = __shfl_sync(kFull, my_res, r);
+                    int out = er;
+                    unsigned f;
+                    if (er < 0) {
+                        f = 1;
+                    } else if (rr) {
+                        f = 0;
+                    } else if (r == 0 || wr >= P.threshold) {
+                        f = 1;
+                    } else {
+                        const uint2 b2 = nrep < k ? s_sel[32 + nrep] : make_uint2(0u, 0u);
+                        if (b2.x == 0u) {
+                            f = 3;
+                        } else {
+                            out = (int)b2.y;
+                            f = 2;
+                            mass += wr;
+                            nrep++;
+                        }
+                    }
+                    if (lane == r) {
+                        use_e = out;
+                        flg = f;
+                    }
+                }
+                if (c == 0 && lane == 0 && Y.sub_mass) Y.sub_mass[0] = mass;
+            }
+            if (lane < k) {
+                if (resident) s_idx[lane] = use_e;
+                s_w[lane] = wv;
+                if (c == 0) {
+                    Y.idx[lane] = sel_e;
+                    Y.w[lane] = wv;
+                    if (Y.idx_used) Y.idx_used[lane] = use_e;
+                    if (Y.sub_flag) Y.sub_flag[lane] = (uint8_t)flg;
+                }
+            }
+        };
 
         // ------------------------------------------------------ phase 1
         if (l > 0) {
@@ -368,7 +463,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                     }
                 }
                 const float acc = warp_sum(acc0 + acc1);
-                if (lane == 0) st_tagged(P.logits + e_begin + warp, Y.bias ? acc + Y.bias[e_begin + warp] : acc, tag);
+                if (lane == 0) st_tagged(P.logits + e_begin + warp, Y.bias ? acc + bias_w : acc, tag);
             }
             router_next = -1;
             __syncthreads();
@@ -408,45 +503,21 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                     }
                 }
             }
-            // softmax: block max, then block sum of exp(l - max) in a fixed order
-            float mx = warp_max(fmaxf(lg0, lg1));
-            if (lane == 0) s_rmax[warp] = mx;
-            __syncthreads();
+            // per-warp candidates, ranked by logit (the softmax keeps the
+            // order): every lane counts the lanes of its warp whose key is
+            // larger, the lower lane (lower id) first on equal keys; ranks below
+            // k are kept (and below 2k-1 among resident experts, for the
+            // replacements). The block max is formed alongside.
             {
-                float m2[4];
-#pragma unroll
-                for (int q = 0; q < 4; q++) m2[q] = fmaxf(fmaxf(s_rmax[4 * q], s_rmax[4 * q + 1]),
-                                                          fmaxf(s_rmax[4 * q + 2], s_rmax[4 * q + 3]));
-                mx = fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3]));
+                const float wmx = warp_max(fmaxf(lg0, lg1));
+                if (lane == 0) s_rmax[warp] = wmx;
             }
-            float p0 = e0 < E ? expf(lg0 - mx) : 0.f;
-            float p1 = e1 < E ? expf(lg1 - mx) : 0.f;
-            const float ws = warp_sum(p0 + p1);
-            if (lane == 0) s_rsum[warp] = ws;
-            __syncthreads();
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < kFWarps; i++) sum += s_rsum[i];  // fixed order
-            const float inv_s = 1.0f / sum;
-            p0 *= inv_s;
-            p1 *= inv_s;
-            if (c == 0 && Y.probs) {
-                if (e0 < E) Y.probs[e0] = p0;
-                if (e1 < E) Y.probs[e1] = p1;
-            }
-            // per-warp candidates: every lane counts the lanes of its warp whose
-            // key is larger (key = fp32 bits of p + 1 over ~id: larger p first,
-            // lower id on equal p; keys are unique); ranks below k are kept (and
-            // below 2k-1 among resident experts, for the replacements)
 #pragma unroll 1
             for (int j = 0; j < 2; j++) {
                 const int vw = j * kFWarps + warp;
                 if (vw < nvw) {
                     const int e = vw * 32 + lane;
-                    const float pe = j ? p1 : p0;
-                    // 32-bit key: fp32 bits of p + 1 (0 = no expert); among equal
-                    // keys the lower lane (lower id) ranks first
-                    const unsigned key = e < E ? __float_as_uint(pe) + 1u : 0u;
+                    const unsigned key = e < E ? logit_key(j ? lg1 : lg0) : 0u;
                     const bool re = Y.resident && (j ? res1 : res0);
                     const unsigned rkey = re ? key : 0u;
                     int rank = 0, rrank = 0;
@@ -480,10 +551,24 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 }
             }
             __syncthreads();
-            // the k best candidates, by each candidate's rank among all of them
-            // (eight threads per candidate, each comparing with every eighth entry)
-            rank_candidates(s_cand, nvw * k, k, s_sel, tid);
+            // the k best candidates (eight threads per candidate, each comparing
+            // with every eighth entry; without residency their ids are the
+            // slots' experts), and alongside the softmax partial sums of
+            // exp(l - max) in a fixed order
+            rank_candidates(s_cand, nvw * k, k, s_sel, Y.resident ? nullptr : s_idx, tid);
+            const float mx = block_max16(s_rmax);
+            const float p0 = e0 < E ? expf(lg0 - mx) : 0.f;
+            const float p1 = e1 < E ? expf(lg1 - mx) : 0.f;
+            {
+                const float ws = warp_sum(p0 + p1);
+                if (lane == 0) s_rsum[warp] = ws;
+            }
             __syncthreads();
+            if (c == 0 && Y.probs) {
+                const float inv_s = 1.0f / block_sum16(s_rsum);
+                if (e0 < E) Y.probs[e0] = p0 * inv_s;
+                if (e1 < E) Y.probs[e1] = p1 * inv_s;
+            }
             if (Y.resident) {
                 // replacement candidates: resident experts outside the chosen k,
                 // ranked the same way; the best ones go to the replaced slots in
@@ -498,65 +583,16 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                         if (s_rcand[i].x != 0u && s_sel[r].y == e) s_rcand[i].x = 0u;
                 }
                 __syncthreads();
-                rank_candidates(s_rcand, RC, k, s_sel + 32, tid);
+                rank_candidates(s_rcand, RC, k, s_sel + 32, nullptr, tid);
                 __syncthreads();
-            }
-            if (warp == 0) {
-                const uint2 sel = lane < k ? s_sel[lane] : make_uint2(0u, 0u);
-                const int sel_e = sel.x ? (int)sel.y : -1;
-                const float sel_p = sel.x ? __uint_as_float(sel.x - 1u) : 0.f;
-                const float norm = warp_sum(lane < k ? sel_p : 0.f);
-                const float wv = P.norm_topk ? sel_p / norm : sel_p;
-                int use_e = sel_e;
-                unsigned flg = 0;
-                if (Y.resident) {
-                    const bool my_res = lane < k && sel_e >= 0 && Y.resident[sel_e];
-                    float mass = 0.f;
-                    int nrep = 0;  // replacements used so far
-#pragma unroll 1
-                    for (int r = 0; r < k; r++) {
-                        const int er = __shfl_sync(kFull, sel_e, r);
-                        const float wr = __shfl_sync(kFull, wv, r);
-                        const bool rr = __shfl_sync(kFull, my_res, r);
-                        int out = er;
-                        unsigned f;
-                        if (er < 0) {
-                            f = 1;
-                        } else if (rr) {
-                            f = 0;
-                        } else if (r == 0 || wr >= P.threshold) {
-                            f = 1;
-                        } else {
-                            const uint2 b2 = nrep < k ? s_sel[32 + nrep] : make_uint2(0u, 0u);
-                            if (b2.x == 0u) {
-                                f = 3;
-                            } else {
-                                out = (int)b2.y;
-                                f = 2;
-                                mass += wr;
-                                nrep++;
-                            }
-                        }
-                        if (lane == r) {
-                            use_e = out;
-                            flg = f;
-                        }
-                    }
-                    if (c == 0 && lane == 0 && Y.sub_mass) Y.sub_mass[0] = mass;
-                }
-                if (lane < k) {
-                    s_idx[lane] = use_e;
-                    s_w[lane] = wv;
-                    if (c == 0) {
-                        Y.idx[lane] = sel_e;
-                        Y.w[lane] = wv;
-                        if (Y.idx_used) Y.idx_used[lane] = use_e;
-                        if (Y.sub_flag) Y.sub_flag[lane] = (uint8_t)flg;
-                    }
-                }
+                // the weights decide the substitutions, which decide the slots'
+                // experts: done here, before the streaming
+                if (warp == 0) route_weights(true);
             }
         }
-        __syncthreads();
+        // the slots' experts are set (by the ranking, the substitution or the
+        // given ids) before anything reads them
+        if (!P.has_router || Y.resident) __syncthreads();
 
         // ------------------------------------------------------ phase 3
         // the warps stream their share of the gate/up row pairs with 16-byte
@@ -768,6 +804,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 }
             }
         }
+        // without residency the weights are needed only by the combine
+        if (P.has_router && !Y.resident && warp == 0) route_weights(false);
         if (!mbar_wait(&s_bar, l & 1, status, lim)) {
             ab = true;
             mbar_wait(&s_bar, l & 1, status);  // the copies into this CTA's memory must land first
