@@ -102,6 +102,39 @@ struct RowPair {
     ST gs[kNCH], us[kNCH];  // widened where used, so no load is waited for early
 };
 
+// Four consecutive activations v (units u..u+3, a lane's share of a block of
+// 32 held by 8 lanes) -> the 16-bit fixed-point planes, one power-of-two scale
+// per block. Called by a whole warp (ok: this lane's units exist).
+template <int QB>
+__device__ __forceinline__ void h_quad_to_planes(const float (&v)[4], int u, bool ok, int lane, int8_t* hhi,
+                                                 uint8_t* hlo, float* hs) {
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+    if (!ok) return;
+    const Fx f = fx_of_blockmax(m);
+    if constexpr (QB == 8) {
+        uint32_t hw = 0, lw = 0;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int Xq = fx_code(v[q], f.mul);
+            hw |= (uint32_t)((Xq >> 8) & 0xff) << (8 * q);
+            lw |= (uint32_t)(Xq & 0xff) << (8 * q);
+        }
+        *reinterpret_cast<uint32_t*>(hhi + u) = hw;
+        *reinterpret_cast<uint32_t*>(hlo + u) = lw;
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int Xq = fx_code(v[q], f.mul);
+            hhi[fx_pos(u + q, 4)] = (int8_t)(Xq >> 8);
+            hlo[fx_pos(u + q, 4)] = (uint8_t)(Xq & 0xff);
+        }
+    }
+    if ((lane & 7) == 0) hs[u / kBlk] = QB == 8 ? f.scale : f.scale * (1.0f / 16.0f);
+}
+
 // Fixed-point conversion of one block of 32 values held one per lane.
 __device__ __forceinline__ void fx_store_block1(float v, int blk, int lane, int qbits, int8_t* hi, uint8_t* lo,
                                                 float* scale) {
@@ -754,53 +787,62 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 }
             }
         }
-        __syncthreads();  // the staging region is free again
-
-        // the down rows are requested once this warp's share of gate/up is
-        // in: the gate/up bytes, which the activation exchange waits for, go
-        // first, and the down rows stream in during that exchange
         if (tid == 32) issue_down();
+        __syncthreads();  // the staging region is free again
         // ------------------------------------------------------ phase 4
-        // every slot's activations: each warp stages its chunks of the tagged
-        // words (re-copying chunks that are not all there yet) and turns them
+        // every slot's activations, gathered from the tagged words and turned
         // into 16-bit fixed point, one power-of-two scale per block of 32 units
         // (4 units per lane, 8 lanes per block)
         {
+            // a warp's chunks are c = warp, warp + 16, ...; four units per lane,
+            // read with 16-byte loads straight into registers (the bulk-copy
+            // engine is left to the down rows), up to four chunks in flight,
+            // each converted as soon as all of its words carry the tag
             const int nw_ = k * F;
-            if (!warp_stage_tagged(s_stage, P.h, nw_, tag, &s_wbar[warp], wph, lim, status)) ab = true;
             const int nch = (nw_ + kChunk - 1) / kChunk;
+            const int mine = warp < nch ? (nch - warp + kFWarps - 1) / kFWarps : 0;
+            const long long t0 = clock64();
+            bool gave_up = false;  // warp-uniform
 #pragma unroll 1
-            for (int ch = warp; ch < nch; ch += kFWarps) {
-                const int u = ch * kChunk + 4 * lane;
-                const bool ok = u < nw_;
-                float v[4];
+            for (int i0 = 0; i0 < mine && !gave_up; i0 += 4) {
+                unsigned pend = 0;
 #pragma unroll
-                for (int q = 0; q < 4; q++) v[q] = ok ? tag_val(s_stage[u + q]) : 0.f;
-                float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-                m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
-                m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
-                m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
-                if (ok) {
-                    const Fx f = fx_of_blockmax(m);
-                    if constexpr (QB == 8) {
-                        uint32_t hw = 0, lw = 0;
+                for (int i = 0; i < 4; i++)
+                    if (i0 + i < mine) pend |= 1u << i;
+#pragma unroll 1
+                while (pend) {
+                    uint64_t w[4][4];
 #pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            const int Xq = fx_code(v[q], f.mul);
-                            hw |= (uint32_t)((Xq >> 8) & 0xff) << (8 * q);
-                            lw |= (uint32_t)(Xq & 0xff) << (8 * q);
-                        }
-                        *reinterpret_cast<uint32_t*>(s_hhi + u) = hw;
-                        *reinterpret_cast<uint32_t*>(s_hlo + u) = lw;
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            const int Xq = fx_code(v[q], f.mul);
-                            s_hhi[fx_pos(u + q, 4)] = (int8_t)(Xq >> 8);
-                            s_hlo[fx_pos(u + q, 4)] = (uint8_t)(Xq & 0xff);
+                    for (int i = 0; i < 4; i++) {
+                        const int u = (warp + kFWarps * (i0 + i)) * kChunk + 4 * lane;
+                        if ((pend >> i & 1u) && u < nw_) {
+                            ld_tagged2(P.h + u, w[i][0], w[i][1]);
+                            ld_tagged2(P.h + u + 2, w[i][2], w[i][3]);
+                        } else {
+                            w[i][0] = w[i][1] = w[i][2] = w[i][3] = (uint64_t)tag << 32;
                         }
                     }
-                    if ((lane & 7) == 0) s_hs[u / kBlk] = QB == 8 ? f.scale : f.scale * (1.0f / 16.0f);
+                    unsigned still = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        if (!(pend >> i & 1u)) continue;
+                        const int u = (warp + kFWarps * (i0 + i)) * kChunk + 4 * lane;
+                        const bool good = tag_ok(w[i][0], tag) && tag_ok(w[i][1], tag) && tag_ok(w[i][2], tag) &&
+                                          tag_ok(w[i][3], tag);
+                        if (!__all_sync(kFull, good)) {
+                            still |= 1u << i;
+                            continue;
+                        }
+                        const float v[4] = {tag_val(w[i][0]), tag_val(w[i][1]), tag_val(w[i][2]), tag_val(w[i][3])};
+                        h_quad_to_planes<QB>(v, u, u < nw_, lane, s_hhi, s_hlo, s_hs);
+                    }
+                    pend = still;
+                    if (pend && __shfl_sync(kFull, clock64() - t0 > lim, 0)) {
+                        if (lane == 0) record_error(status, MOE_ERR_DEVICE_TIMEOUT);
+                        ab = true;
+                        gave_up = true;
+                        break;
+                    }
                 }
             }
         }
@@ -887,15 +929,27 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                             }
                         }
                     }
+                    // the eight sums across the warp, halving the values a lane
+                    // holds at each of the first three steps: lane bits 4, 3, 2
+                    // pick the row a lane ends with
+                    static_assert(kDP == 8, "the reduction below is written for 8 rows");
+                    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+                    float a4[4], a2[2];
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                        for (int u = 0; u < kDP; u++) acc[u] += __shfl_xor_sync(kFull, acc[u], o);
-                    if (lane == 0) {
-#pragma unroll
-                        for (int u = 0; u < kDP; u++)
-                            if (row0 + u < i1) s_part[(row0 + u) * k + r] = acc[u];
+                    for (int j = 0; j < 4; j++) {
+                        const float send = b4 ? acc[j] : acc[j + 4];
+                        a4[j] = (b4 ? acc[j + 4] : acc[j]) + __shfl_xor_sync(kFull, send, 16);
                     }
+#pragma unroll
+                    for (int j = 0; j < 2; j++) {
+                        const float send = b3 ? a4[j] : a4[j + 2];
+                        a2[j] = (b3 ? a4[j + 2] : a4[j]) + __shfl_xor_sync(kFull, send, 8);
+                    }
+                    float a1 = (b2 ? a2[1] : a2[0]) + __shfl_xor_sync(kFull, b2 ? a2[0] : a2[1], 4);
+                    a1 += __shfl_xor_sync(kFull, a1, 2);
+                    a1 += __shfl_xor_sync(kFull, a1, 1);
+                    const int ru = (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0);
+                    if ((lane & 3) == 0 && row0 + ru < i1) s_part[(row0 + ru) * k + r] = a1;
                 }
             }
         }
