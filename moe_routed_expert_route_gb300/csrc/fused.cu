@@ -55,7 +55,8 @@ constexpr int kFWarps = 16;
 constexpr int kNCH = 4;      // gate/up 16-byte chunks per lane
 constexpr int kDP = 8;       // down rows per warp task pass (computed together)
 constexpr int kNPL = 4;      // 8-byte down pieces per lane (F <= 1024 int8, 2048 int4)
-constexpr int kChunk = 128;  // tagged words per staged chunk (1 KB)
+constexpr int kChunk = 128;  // tagged words per unit of the activation gather (1 KB)
+constexpr int kXChunk = 64;  // tagged words per staged chunk of x (512 B)
 
 // Shared-memory plan of one CTA.
 struct FusedLayout {
@@ -206,7 +207,7 @@ __device__ __forceinline__ void rank_candidates(const uint2* list, int n, int k,
 }
 
 // Called by a whole warp: brings the n tagged words src[0..n) of the chunks
-// c = warp, warp + 16, ... (kChunk words each) into dst (same offsets) by bulk
+// c = warp, warp + 16, ... (kXChunk words each) into dst (same offsets) by bulk
 // copies, re-copying any chunk that still holds a word without `tag`, until
 // every word of the warp's chunks carries it. Bounded by `lim`; on timeout
 // records MOE_ERR_DEVICE_TIMEOUT and returns false (the copies in flight have
@@ -214,7 +215,7 @@ __device__ __forceinline__ void rank_candidates(const uint2* list, int n, int k,
 __device__ __noinline__ bool warp_stage_tagged(uint64_t* dst, const uint64_t* src, int n, unsigned tag, uint64_t* bar,
                                   unsigned& phase, long long lim, int* status) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nch = (n + kChunk - 1) / kChunk;
+    const int nch = (n + kXChunk - 1) / kXChunk;
     int mine = 0;
     for (int c = warp; c < nch; c += kFWarps) mine++;
     unsigned pending = mine >= 32 ? 0xffffffffu : ((1u << mine) - 1u);
@@ -225,13 +226,13 @@ __device__ __noinline__ bool warp_stage_tagged(uint64_t* dst, const uint64_t* sr
         if (lane == 0) {
             unsigned bytes = 0;
             for (int i = 0; i < mine; i++)
-                if (pending >> i & 1u) bytes += 8u * (unsigned)min(kChunk, n - (warp + kFWarps * i) * kChunk);
+                if (pending >> i & 1u) bytes += 8u * (unsigned)min(kXChunk, n - (warp + kFWarps * i) * kXChunk);
             mbar_arrive_expect_tx(bar, bytes);
             for (int i = 0; i < mine; i++) {
                 if (!(pending >> i & 1u)) continue;
                 const int c = warp + kFWarps * i;
-                bulk_g2s(dst + (size_t)c * kChunk, src + (size_t)c * kChunk,
-                         8u * (unsigned)min(kChunk, n - c * kChunk), bar);
+                bulk_g2s(dst + (size_t)c * kXChunk, src + (size_t)c * kXChunk,
+                         8u * (unsigned)min(kXChunk, n - c * kXChunk), bar);
             }
         }
         // the lanes agree on the outcome: the loop and the return are warp-uniform
@@ -247,8 +248,8 @@ __device__ __noinline__ bool warp_stage_tagged(uint64_t* dst, const uint64_t* sr
             const int c = warp + kFWarps * i;
             bool good = true;
 #pragma unroll
-            for (int q = 0; q < kChunk / 32; q++) {
-                const int wi = c * kChunk + q * 32 + lane;
+            for (int q = 0; q < kXChunk / 32; q++) {
+                const int wi = c * kXChunk + q * 32 + lane;
                 if (wi < n) good &= tag_ok(dst[wi], tag);
             }
             if (!__all_sync(kFull, good)) still |= 1u << i;
@@ -447,9 +448,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             if (!warp_stage_tagged(s_stage, P.xex, nxw, ptag, &s_wbar[warp], wph, lim, status)) ab = true;
             if (P.chain) {
 #pragma unroll 1
-                for (int i = warp * kChunk + lane; i < nxw; i += kFWarps * kChunk)
+                for (int i = warp * kXChunk + lane; i < nxw; i += kFWarps * kXChunk)
 #pragma unroll
-                    for (int q = 0; q < kChunk; q += 32) {
+                    for (int q = 0; q < kXChunk; q += 32) {
                         const int wi = i + q;
                         if (wi < nxw) {
                             const uint32_t v = (uint32_t)s_stage[wi];
@@ -788,6 +789,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             }
         }
         if (tid == 32) issue_down();
+        // without residency the weights are needed only by the combine: the
+        // last warp, which streams the fewest pairs, computes them
+        if (P.has_router && !Y.resident && warp == kFWarps - 1) route_weights(false);
         __syncthreads();  // the staging region is free again
         // ------------------------------------------------------ phase 4
         // every slot's activations, gathered from the tagged words and turned
@@ -846,8 +850,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 }
             }
         }
-        // without residency the weights are needed only by the combine
-        if (P.has_router && !Y.resident && warp == 0) route_weights(false);
         if (!mbar_wait(&s_bar, l & 1, status, lim)) {
             ab = true;
             mbar_wait(&s_bar, l & 1, status);  // the copies into this CTA's memory must land first
