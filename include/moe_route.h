@@ -38,7 +38,7 @@
  *  - Workspace: `ws_bytes` >= moe_workspace_bytes(op, ...). It must be zeroed
  *    once before its first use (cudaMemset). Its header holds a launch sequence
  *    number that keeps growing from call to call; do not clear it afterwards.
- *  - Single-token calls (T <= 3) run a persistent kernel with one CTA per SM
+ *  - Calls of up to 7 tokens run a persistent kernel (one launch per token) with one CTA per SM
  *    whose CTAs wait on one another (bounded waits, about 30 ms by default,
  *    see moe_set_wait_limit). It needs every SM of the device: a kernel running
  *    at the same time on another stream can hold SMs until a wait runs out, in
@@ -155,9 +155,9 @@ moe_status_t moe_substitute(int T, int E, int k, const float* probs, const int32
  *   idx, w  [T][k] routing (int32 ids in [0, E), fp32 weights)
  *   y       [T][D] fp32 out
  *   x_next  [T][D] in x_dtype out, or NULL: x + y rounded to x_dtype (residual)
- * T <= 3 runs one persistent single-token kernel per token (integer dot
+ * T <= 7 runs one persistent single-token kernel per token (integer dot
  * products, fp32 accumulation; an expert shared by tokens is read once per
- * token). T >= 4 with D % 128 == 0, F % 64 == 0, D <= 8192 and E <= 1024 runs
+ * token). T >= 8 with D % 128 == 0, F % 64 == 0, D <= 8192 and E <= 1024 runs
  * the same grouped tensor-core products as moe_prefill, reading each distinct
  * expert once (fp16 operands with exact per-token power-of-two scaling, fp32
  * accumulation); other shapes run CUDA-core kernels. Ids outside [0, E) are skipped and reported by
@@ -171,9 +171,11 @@ moe_status_t moe_decode(const moe_experts_t* experts, const void* x, moe_dtype_t
  * One whole layer for T tokens: moe_route followed by moe_decode, with the
  * router's outputs handed to the expert kernels on the device.
  *   idx, w  [T][k] out    probs [T][E] out or NULL    y, x_next as moe_decode
- * With T >= 4 and bf16 x and router weights (E % 128 == 0), the logits come
- * from the tensor cores (fp32 accumulation in another order than moe_route;
- * probabilities may differ in the last bits).
+ * T <= 7 runs one single-token layer launch per token (as moe_decode). Past
+ * that (or for a shape the single-token kernel cannot run), with bf16 x and
+ * router weights and E % 128 == 0, the logits come from the tensor cores (fp32
+ * accumulation in another order than moe_route; probabilities may differ in
+ * the last bits).
  */
 moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts, const void* x,
                        moe_dtype_t x_dtype, int T, int32_t* idx, float* w, float* probs,
@@ -192,7 +194,7 @@ moe_status_t moe_layer(const moe_router_t* router, const moe_experts_t* experts,
  *   idx_used   [T][k] out: the experts read     sub_flag [T][k], sub_mass [T]
  *              out, as moe_substitute
  *   y, x_next  as moe_decode
- * T <= 3 runs the whole layer, substitution included, in one single-token
+ * T <= 7 runs the whole layer, substitution included, in one single-token
  * launch per token; more tokens run moe_layer's kernels with moe_substitute's
  * kernel between routing and experts. Workspace: MOE_OP_LAYER_RESIDENT.
  */

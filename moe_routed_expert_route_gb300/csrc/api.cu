@@ -16,9 +16,10 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 constexpr int kMaxDecodeT = 256;
 // Up to this many tokens, one single-token layer launch per token is faster
-// than the grouped products (2 tokens: 2 x 25 us against 80 us per layer), even
-// though an expert shared by the tokens is then read once per token.
-constexpr int kFusedTokens = 3;
+// than the grouped products, even though an expert shared by the tokens is then
+// read once per token (E=256 top-8 D=2048 F=768 int8: 14.3 us per token against
+// 57 us for 4 tokens and 73 us for 8 tokens in the grouped products).
+constexpr int kFusedTokens = 7;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 

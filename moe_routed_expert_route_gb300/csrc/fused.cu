@@ -60,7 +60,7 @@ constexpr int kXChunk = 64;  // tagged words per staged chunk of x (512 B)
 
 // Shared-memory plan of one CTA.
 struct FusedLayout {
-    size_t x, xhi, xlo, xs, hhi, hlo, hs, wr, dq, ds, part, cand, rcand, sel, stage;
+    size_t x, xin, xhi, xlo, xs, hhi, hlo, hs, wr, dq, ds, part, cand, rcand, sel, stage;
     size_t total;
 };
 
@@ -78,6 +78,7 @@ __host__ __device__ inline FusedLayout fused_layout(int E, int D, int F, int k, 
     const size_t rowF = qbits == 8 ? F : F / 2;
     const int nvw = (E + 31) / 32;  // warps of 32 experts in the selection
     L.x = o;     o = fl_align(o + sizeof(float) * D, 16);
+    L.xin = o;   o = fl_align(o + (size_t)x_bytes * D, 16);
     L.xhi = o;   o = fl_align(o + D, 16);
     L.xlo = o;   o = fl_align(o + D, 16);
     L.xs = o;    o = fl_align(o + sizeof(float) * (D / kBlk), 16);
@@ -297,6 +298,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     const int rowF = QB == 8 ? F : F / 2;  // bytes of a down row
     const FusedLayout Lo = fused_layout(E, D, F, k, QB, sizeof(ST), sizeof(XT), P.rows, G);
     float* s_x = reinterpret_cast<float*>(sm + Lo.x);
+    const XT* s_xin = reinterpret_cast<const XT*>(sm + Lo.xin);
     int8_t* s_xhi = reinterpret_cast<int8_t*>(sm + Lo.xhi);
     uint8_t* s_xlo = sm + Lo.xlo;
     float* s_xs = reinterpret_cast<float*>(sm + Lo.xs);
@@ -331,10 +333,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             reinterpret_cast<uint32_t*>(&s_ly[b])[t] = reinterpret_cast<const uint32_t*>(&a.L[l])[t];
     };
     // bulk copy of this CTA's router rows (contiguous) of layer l
-    auto request_router = [&](const FusedLayer& Y) {
+    // (and, for a later layer of an unchained stack, the layer's own x)
+    auto request_router = [&](const FusedLayer& Y, bool with_x) {
         const unsigned bytes = (unsigned)((e_end - e_begin) * D * (int)sizeof(XT));
-        mbar_arrive_expect_tx(&s_rbar, bytes);
+        const unsigned xbytes = with_x ? (unsigned)(D * (int)sizeof(XT)) : 0u;
+        mbar_arrive_expect_tx(&s_rbar, bytes + xbytes);
         if (bytes) bulk_g2s(sm + Lo.wr, static_cast<const XT*>(Y.W) + (size_t)e_begin * D, bytes, &s_rbar);
+        if (xbytes) bulk_g2s(sm + Lo.xin, Y.x, xbytes, &s_rbar);
     };
 
     // ---------------------------------------------------------- phase 0
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
         fence_barrier_init();
     }
     __syncthreads();
-    if (tid == 0 && P.has_router) request_router(s_ly[0]);
+    if (tid == 0 && P.has_router) request_router(s_ly[0], false);  // x may still be being written
     pdl_wait();
     pdl_trigger();
     // the previous launch on this workspace has completed: its sequence
@@ -465,7 +470,16 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             }
             if (__syncthreads_or(ab)) break;
         }
-        if (l == 0 || !P.chain) {
+        if (l > 0 && !P.chain && P.has_router) {
+            // this layer's own x, copied in with its router rows during the
+            // last layer
+            if (!mbar_wait(&s_rbar, l & 1, status, lim)) {
+                ab = true;
+                mbar_wait(&s_rbar, l & 1, status);
+            }
+#pragma unroll 4
+            for (int i = tid; i < D; i += kFThreads) s_x[i] = to_f32(s_xin[i]);
+        } else if (l == 0 || !P.chain) {
             const XT* X = reinterpret_cast<const XT*>(Y.x);
 #pragma unroll 4
             for (int i = tid; i < D; i += kFThreads) s_x[i] = ldcg_f32(X + i);
@@ -650,7 +664,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 bulk_g2s(s_ds + (size_t)r * P.rows * nbF, DS + row0 * nbF, nrows * nbF * (int)sizeof(ST), &s_bar);
             }
             // the next layer's router rows (its pointers were loaded before the last barrier)
-            if (l + 1 < P.nlayers && P.has_router) request_router(s_ly[(l + 1) & 1]);
+            if (l + 1 < P.nlayers && P.has_router) request_router(s_ly[(l + 1) & 1], !P.chain);
         };
         if (l + 1 < P.nlayers && P.has_router) router_next = l + 1;
 

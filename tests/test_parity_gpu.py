@@ -320,7 +320,7 @@ def test_substitution_and_int4_decode(cfg3_layer, T, threshold):
 @pytest.mark.parametrize("threshold", [0.15, 0.0, float("inf")])
 def test_layer_resident_matches_oracle(cfg3_layer, T, threshold):
     """moe_layer_resident: routing, substitution and int4 experts in one call
-    (one launch per token for T <= 3)."""
+    (one launch per token for T <= 7)."""
     cfg, layer, mask = cfg3_layer
     k = cfg.k
     x = W.make_tokens(cfg, T, 12, DEV)
