@@ -278,6 +278,7 @@ template <int QB, typename ST, typename XT, int NL, class SH>
 __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_constant__ FusedArgs<NL> a) {
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ FusedLayer s_ly[2];  // this layer's and the next layer's pointers
+    __shared__ float s_rpart[kFWarps * kFWarps];  // router shares [expert of this CTA][warp]
     __shared__ float s_rmax[kFWarps];
     __shared__ float s_rsum[kFWarps];
     __shared__ int s_idx[32];  // experts read per slot (after substitution), -1 = none
@@ -321,7 +322,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
     const long total = (long)k * F;
     const int g_begin = (int)((long)c * total / G), g_end = (int)((long)(c + 1) * total / G);
     const int e_begin = (int)((long)c * E / G), e_end = (int)((long)(c + 1) * E / G);
-    constexpr int EPC = 16 / sizeof(XT);
     const int nvw = (E + 31) / 32;
     const int nxw = sizeof(XT) == 2 ? D / 2 : D;  // tagged words of a layer's x_next
 
@@ -375,11 +375,11 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
         const FusedLayer& Y = s_ly[l & 1];
         const unsigned tag = seq_tag(seq0 + (unsigned)l);
         // requested now, used later: the residency of the experts this thread
-        // selects among, and the bias of the expert this warp scores
+        // selects among, and the bias of the expert whose logit it completes
         const int e0 = tid, e1 = tid + kFThreads;
         const bool res0 = Y.resident && e0 < E && Y.resident[e0];
         const bool res1 = Y.resident && e1 < E && Y.resident[e1];
-        const float bias_w = (P.has_router && Y.bias && warp < e_end - e_begin) ? Y.bias[e_begin + warp] : 0.f;
+        const float bias_w = (P.has_router && Y.bias && tid < e_end - e_begin) ? Y.bias[e_begin + tid] : 0.f;
 
         // Called by warp 0 once the k slots are ranked: each slot's weight is
         // its softmax probability exp(l - max) / sum (the block max and the
@@ -445,76 +445,92 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
         };
 
         // ------------------------------------------------------ phase 1
-        if (l > 0) {
-            // layer l-1's x_next, tagged word by word by the CTAs that wrote it,
-            // staged into shared memory: this layer starts when all of it has
-            // arrived; chained, it is this layer's token
-            const unsigned ptag = seq_tag(seq0 + (unsigned)l - 1u);
-            if (!warp_stage_tagged(s_stage, P.xex, nxw, ptag, &s_wbar[warp], wph, lim, status)) ab = true;
-            if (P.chain) {
+        // the router dots: each warp forms its share over its chunks of x (the
+        // chunks it staged, as soon as they are in); one thread per expert of
+        // this CTA adds the shares in warp order after the barrier
+        auto router_shares = [&]() {
+            __syncwarp();
+            const int nexp = e_end - e_begin;
+#pragma unroll 1
+            for (int j = 0; j < nexp; j++) {
+                const XT* wrow = s_wr + (size_t)j * D;
+                float acc = 0.f;
 #pragma unroll 1
                 for (int i = warp * kXChunk + lane; i < nxw; i += kFWarps * kXChunk)
 #pragma unroll
                     for (int q = 0; q < kXChunk; q += 32) {
                         const int wi = i + q;
                         if (wi < nxw) {
-                            const uint32_t v = (uint32_t)s_stage[wi];
                             if constexpr (sizeof(XT) == 2) {
-                                s_x[2 * wi] = bf16lo(v);
-                                s_x[2 * wi + 1] = bf16hi(v);
+                                const uint32_t w2 = *reinterpret_cast<const uint32_t*>(wrow + 2 * wi);
+                                acc = fmaf(bf16lo(w2), s_x[2 * wi], acc);
+                                acc = fmaf(bf16hi(w2), s_x[2 * wi + 1], acc);
                             } else {
-                                s_x[wi] = __uint_as_float(v);
+                                acc = fmaf(wrow[wi], s_x[wi], acc);
                             }
                         }
                     }
+                acc = warp_sum(acc);
+                if (lane == 0) s_rpart[j * kFWarps + warp] = acc;
             }
+        };
+        if (l > 0) {
+            // layer l-1's x_next, tagged word by word by the CTAs that wrote it,
+            // staged into shared memory: this layer starts when all of it has
+            // arrived. Chained, it is this layer's token; unchained, the
+            // layer's own token (copied in during the last layer) stands in
+            // for it chunk by chunk, so that the work waits as in a chain.
+            const unsigned ptag = seq_tag(seq0 + (unsigned)l - 1u);
+            if (!warp_stage_tagged(s_stage, P.xex, nxw, ptag, &s_wbar[warp], wph, lim, status)) ab = true;
+            if (P.has_router) {
+                // the router rows (and the unchained token) of this layer
+                if (!mbar_wait(&s_rbar, l & 1, status, lim)) {
+                    ab = true;
+                    mbar_wait(&s_rbar, l & 1, status);
+                }
+                router_next = -1;
+            }
+#pragma unroll 1
+            for (int i = warp * kXChunk + lane; i < nxw; i += kFWarps * kXChunk)
+#pragma unroll
+                for (int q = 0; q < kXChunk; q += 32) {
+                    const int wi = i + q;
+                    if (wi < nxw) {
+                        const uint32_t v = (uint32_t)s_stage[wi];
+                        if constexpr (sizeof(XT) == 2) {
+                            s_x[2 * wi] = P.chain ? bf16lo(v) : to_f32(s_xin[2 * wi]);
+                            s_x[2 * wi + 1] = P.chain ? bf16hi(v) : to_f32(s_xin[2 * wi + 1]);
+                        } else {
+                            s_x[wi] = P.chain ? __uint_as_float(v) : s_xin[wi];
+                        }
+                    }
+                }
+            if (P.has_router) router_shares();
             if (__syncthreads_or(ab)) break;
         }
-        if (l > 0 && !P.chain && P.has_router) {
-            // this layer's own x, copied in with its router rows during the
-            // last layer
-            if (!mbar_wait(&s_rbar, l & 1, status, lim)) {
-                ab = true;
-                mbar_wait(&s_rbar, l & 1, status);
-            }
-#pragma unroll 4
-            for (int i = tid; i < D; i += kFThreads) s_x[i] = to_f32(s_xin[i]);
-        } else if (l == 0 || !P.chain) {
+        if (l == 0 || (!P.chain && !P.has_router)) {
             const XT* X = reinterpret_cast<const XT*>(Y.x);
 #pragma unroll 4
             for (int i = tid; i < D; i += kFThreads) s_x[i] = ldcg_f32(X + i);
+            __syncthreads();
+            if (l == 0 && P.has_router) {
+                if (!mbar_wait(&s_rbar, 0, status, lim)) {
+                    ab = true;
+                    mbar_wait(&s_rbar, 0, status);
+                }
+                router_next = -1;
+                router_shares();
+                __syncthreads();
+            }
         }
-        __syncthreads();
 
         if (P.has_router) {
-            // one warp per expert of this CTA: the whole row against x, in
-            // 16-byte pieces from shared memory, published without a barrier
-            if (warp < e_end - e_begin) {
-                if (!mbar_wait(&s_rbar, l & 1, status, lim)) {
-                    ab = true;
-                    mbar_wait(&s_rbar, l & 1, status);  // the copy must land before anything else happens
-                }
-                const XT* wrow = s_wr + (size_t)warp * D;
-                float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-                for (int ci = lane; ci * EPC < D; ci += 32) {
-                    const float* xs = s_x + ci * EPC;
-                    const uint4 wq4 = *reinterpret_cast<const uint4*>(wrow + ci * EPC);
-                    const uint32_t* wq = reinterpret_cast<const uint32_t*>(&wq4);
+            if (tid < e_end - e_begin) {
+                float acc = 0.f;
 #pragma unroll
-                    for (int q = 0; q < EPC; q++) {
-                        float wf;
-                        if constexpr (sizeof(XT) == 2) wf = (q & 1) ? bf16hi(wq[q >> 1]) : bf16lo(wq[q >> 1]);
-                        else wf = __uint_as_float(wq[q]);
-                        if (q & 1) acc1 = fmaf(wf, xs[q], acc1);
-                        else acc0 = fmaf(wf, xs[q], acc0);
-                    }
-                }
-                const float acc = warp_sum(acc0 + acc1);
-                if (lane == 0) st_tagged(P.logits + e_begin + warp, Y.bias ? acc + bias_w : acc, tag);
+                for (int w = 0; w < kFWarps; w++) acc += s_rpart[tid * kFWarps + w];
+                st_tagged(P.logits + e_begin + tid, Y.bias ? acc + bias_w : acc, tag);
             }
-            router_next = -1;
-            __syncthreads();
         } else if (tid < k) {
             int e = ld_cg_i32(Y.idx_in + tid);
             if (e < 0 || e >= E) {
