@@ -472,7 +472,9 @@ def run_substitution(args, dev):
                          used=torch.empty(T, k, dtype=torch.int32, device=dev),
                          flag=torch.empty(T, k, dtype=torch.uint8, device=dev),
                          mass=torch.empty(T, device=dev), y=torch.empty(T, cfg.D, device=dev)) for _ in range(L)]
-            ws = M.workspace(M.MOE_OP_LAYER_RESIDENT, T, k, cfg.E, cfg.D, cfg.F, dev)
+            # one token: all layers in one launch of the stacked kernel
+            ws = (M.workspace(M.MOE_OP_LAYER, 1, k, cfg.E, cfg.D, cfg.F, dev) if T == 1 else
+                  M.workspace(M.MOE_OP_LAYER_RESIDENT, T, k, cfg.E, cfg.D, cfg.F, dev))
             NB = 16 if T > 8 else 64
             bank = W.make_tokens(cfg, NB * L * T, 1, dev).reshape(NB, L, T, cfg.D)
             ctr = torch.zeros(1, dtype=torch.long, device=dev)
@@ -481,6 +483,12 @@ def run_substitution(args, dev):
             def step():
                 torch.index_select(bank, 0, ctr, out=XIN.view(1, L, T, -1))
                 ctr.add_(1).remainder_(NB)
+                if T == 1:
+                    M.moe_layer_stack_resident(routers, experts, [XIN[l] for l in range(L)], False, masks,
+                                               cfg.threshold, *([b[n] for b in bufs] for n in
+                                                                ("idx", "w", "used", "flag", "mass", "y")),
+                                               [XN[l] for l in range(L)], ws)
+                    return
                 for l in range(L):
                     b = bufs[l]
                     M.moe_layer_resident(routers[l], experts[l], XIN[l], masks[l], cfg.threshold, b["idx"], b["w"],
@@ -503,7 +511,8 @@ def run_substitution(args, dev):
                         "us_per_layer": round(ms * 1e3 / L, 2), "distinct_experts_mean": round(sum(U) / L, 2),
                         "routed_gbs": round(gbs, 1),
                         "roofline": roofline("hbm", gbs, hbm, "GB/s",
-                                             "single-token layer kernel with substitution" if T == 1 else
+                                             "stacked single-token layer kernel with substitution (one launch "
+                                             "per step)" if T == 1 else
                                              "router GEMM + substitution + grouped tensor-core products",
                                              {"peak_kind": kind}),
                         "substituted_frac": round(float((flags == 2).float().mean()), 4),

@@ -228,6 +228,26 @@ moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe
                              size_t ws_bytes, void* stream);
 
 /*
+ * moe_layer_stack with residency substitution in every layer (gist.science
+ * "Which expert misses are worth waiting for?", method section; the rule of
+ * moe_substitute, decided in the kernel between the top-k and the experts).
+ *   resident   host array [nlayers] of device pointers to [E] uint8 masks
+ *   threshold  shared by the layers
+ *   idx, w     as moe_layer_stack: the router's top-k and weights
+ *   idx_used   host array [nlayers] of device pointers to [k] int32 outputs:
+ *              the experts read
+ *   sub_flag   host array [nlayers] of device pointers to [k] uint8 outputs
+ *   sub_mass   host array [nlayers] of device pointers to one fp32 output
+ * Every entry is required. Workspace: MOE_OP_LAYER with T = 1.
+ */
+moe_status_t moe_layer_stack_resident(int nlayers, const moe_router_t* routers, const moe_experts_t* experts,
+                                      const void* const* x, moe_dtype_t x_dtype, int chain,
+                                      const uint8_t* const* resident, float threshold, int32_t* const* idx,
+                                      float* const* w, int32_t* const* idx_used, uint8_t* const* sub_flag,
+                                      float* const* sub_mass, float* const* y, void* const* x_next,
+                                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Prefill of T tokens: router, then the (token, slot) assignments grouped by
  * expert (histogram, exclusive scan, stable permutation), a grouped matrix
  * product per expert on the tensor cores, and the weighted un-permute.

@@ -5,7 +5,7 @@ from ._lib import (EXPORTED, LIB_PATH, MOE_BF16, MOE_ERR_BAD_INDEX, MOE_ERR_CUDA
                    MOE_ERR_WORKSPACE, MOE_F16, MOE_F32, MOE_OK, MOE_OP_DECODE, MOE_OP_LAYER,
                    MOE_OP_LAYER_RESIDENT, MOE_OP_PREFILL, MOE_OP_ROUTE, Experts, MoeError, Router,
                    moe_check_status, moe_decode, moe_layer, moe_layer_noalloc, moe_layer_resident,
-                   moe_layer_stack, moe_prefill, moe_route, moe_set_wait_limit, moe_substitute,
+                   moe_layer_stack, moe_layer_stack_resident, moe_prefill, moe_route, moe_set_wait_limit, moe_substitute,
                    moe_workspace_bytes, status_string, workspace)
 
 __all__ = [n for n in dir() if not n.startswith("_")]

@@ -28,7 +28,7 @@ MOE_Q_INT8_SYM_B32, MOE_Q_INT4_SYM_B32 = 0, 1
 MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_LAYER, MOE_OP_PREFILL, MOE_OP_LAYER_RESIDENT = 0, 1, 2, 3, 4
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_substitute", "moe_decode", "moe_layer",
-            "moe_layer_resident", "moe_layer_stack", "moe_prefill", "moe_layer_noalloc",
+            "moe_layer_resident", "moe_layer_stack", "moe_layer_stack_resident", "moe_prefill", "moe_layer_noalloc",
             "moe_check_status", "moe_set_wait_limit", "moe_status_string")
 
 
@@ -68,6 +68,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_noalloc.argtypes = [P, P, P, I, P, P, P, P, P, P]
     lib.moe_layer_resident.argtypes = [P, P, P, I, I, P, ctypes.c_float, P, P, P, P, P, P, P, P, P, S, P]
     lib.moe_layer_stack.argtypes = [I, P, P, P, I, I, P, P, P, P, P, S, P]
+    lib.moe_layer_stack_resident.argtypes = [I, P, P, P, I, I, P, ctypes.c_float, P, P, P, P, P, P, P, P, S, P]
     lib.moe_check_status.argtypes = [P, P]
     lib.moe_set_wait_limit.argtypes = [P, ctypes.c_ulonglong, P]
     lib.moe_status_string.argtypes = [I]
@@ -327,6 +328,19 @@ def moe_layer_stack(routers, experts, x, chain: bool, idx, w, y, x_next, ws, str
     x_next: lists of per-layer tensors ([1][D], [1][k], [1][k], [1][D], [1][D])
     or stacked tensors whose first dimension is the layer; x_next may be None
     when ``chain`` is false."""
+    _layer_stack(routers, experts, x, chain, idx, w, y, x_next, ws, stream)
+
+
+def moe_layer_stack_resident(routers, experts, x, chain: bool, resident, threshold: float, idx, w, idx_used,
+                             sub_flag, sub_mass, y, x_next, ws, stream=None):
+    """moe_layer_stack with residency substitution in every layer: resident is a
+    list of [E] uint8 masks; idx_used [1][k] int32, sub_flag [1][k] uint8 and
+    sub_mass [1] fp32 per layer are outputs."""
+    _layer_stack(routers, experts, x, chain, idx, w, y, x_next, ws, stream,
+                 res=(resident, float(threshold), idx_used, sub_flag, sub_mass))
+
+
+def _layer_stack(routers, experts, x, chain, idx, w, y, x_next, ws, stream, res=None):
     L = len(routers)
     if len(experts) != L:
         raise ValueError("one Experts per Router")
@@ -354,8 +368,19 @@ def moe_layer_stack(routers, experts, x, chain: bool, idx, w, y, x_next, ws, str
     wa = ptrs(w, "w", torch.float32, (1, k))
     ya = ptrs(y, "y", torch.float32, (1, D))
     xn = None if x_next is None else ptrs(x_next, "x_next", xd, (1, D), optional=True)
-    _check("moe_layer_stack", _lib.moe_layer_stack(L, rs, es, xs, _act_dtype(x[0]), 1 if chain else 0, ia, wa,
-                                                   ya, xn, _ptr(ws), ws.numel(), _stream(stream)))
+    if res is None:
+        _check("moe_layer_stack", _lib.moe_layer_stack(L, rs, es, xs, _act_dtype(x[0]), 1 if chain else 0, ia,
+                                                       wa, ya, xn, _ptr(ws), ws.numel(), _stream(stream)))
+        return
+    resident, thr, idx_used, sub_flag, sub_mass = res
+    E = rs[0].E
+    ra = ptrs(resident, "resident", torch.uint8, (E,))
+    ua = ptrs(idx_used, "idx_used", torch.int32, (1, k))
+    fa = ptrs(sub_flag, "sub_flag", torch.uint8, (1, k))
+    ma = ptrs(sub_mass, "sub_mass", torch.float32, (1,))
+    _check("moe_layer_stack_resident", _lib.moe_layer_stack_resident(
+        L, rs, es, xs, _act_dtype(x[0]), 1 if chain else 0, ra, ctypes.c_float(thr), ia, wa, ua, fa, ma, ya, xn,
+        _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_check_status(ws: torch.Tensor, stream=None) -> int:

@@ -588,10 +588,12 @@ moe_status_t moe_layer_resident(const moe_router_t* router, const moe_experts_t*
                       sub_mass, y, x_next, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe_experts_t* experts,
-                             const void* const* x, moe_dtype_t x_dtype, int chain, int32_t* const* idx,
-                             float* const* w, float* const* y, void* const* x_next, void* workspace,
-                             size_t ws_bytes, void* stream) {
+// The stacked launch, with or without residency substitution (resident NULL).
+static moe_status_t layer_stack_impl(int nlayers, const moe_router_t* routers, const moe_experts_t* experts,
+                              const void* const* x, moe_dtype_t x_dtype, int chain, const uint8_t* const* resident,
+                              float threshold, int32_t* const* idx, float* const* w, int32_t* const* idx_used,
+                              uint8_t* const* sub_flag, float* const* sub_mass, float* const* y,
+                              void* const* x_next, void* workspace, size_t ws_bytes, void* stream) {
     if (nlayers < 1 || nlayers > kStackMax || !routers || !experts || !x || !idx || !w || !y)
         return MOE_ERR_INVALID_ARG;
     const moe_router_t& R0 = routers[0];
@@ -608,6 +610,9 @@ moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe
             return MOE_ERR_INVALID_ARG;
         if ((l == 0 || !chain) && !al16(x[l])) return MOE_ERR_INVALID_ARG;
         if (!idx[l] || !w[l] || !al16(y[l])) return MOE_ERR_INVALID_ARG;
+        if (resident && (!resident[l] || !idx_used || !idx_used[l] || !sub_flag || !sub_flag[l] || !sub_mass ||
+                         !sub_mass[l]))
+            return MOE_ERR_INVALID_ARG;
         void* xn = x_next ? x_next[l] : nullptr;
         if (xn && !al16(xn)) return MOE_ERR_INVALID_ARG;
     }
@@ -621,6 +626,7 @@ moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe
                     &fc, &smem, &grid))
         return MOE_ERR_UNSUPPORTED;
     fc.norm_topk = R0.norm_topk ? 1 : 0;
+    fc.threshold = threshold;
     fc.nlayers = nlayers;
     fc.chain = chain ? 1 : 0;
     FusedLayer ly[kStackMax];
@@ -630,9 +636,34 @@ moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe
         ly[l].bias = routers[l].bias;
         ly[l].idx = idx[l];
         ly[l].w = w[l];
+        if (resident) {
+            ly[l].resident = resident[l];
+            ly[l].idx_used = idx_used[l];
+            ly[l].sub_flag = sub_flag[l];
+            ly[l].sub_mass = sub_mass[l];
+        }
     }
     return from_cuda(launch_fused(fc, ly, qbits_of(&X0), X0.s_dtype == MOE_F16, x_dtype == MOE_BF16, grid, smem,
                                   static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_stack(int nlayers, const moe_router_t* routers, const moe_experts_t* experts,
+                             const void* const* x, moe_dtype_t x_dtype, int chain, int32_t* const* idx,
+                             float* const* w, float* const* y, void* const* x_next, void* workspace,
+                             size_t ws_bytes, void* stream) {
+    return layer_stack_impl(nlayers, routers, experts, x, x_dtype, chain, nullptr, 0.f, idx, w, nullptr, nullptr,
+                            nullptr, y, x_next, workspace, ws_bytes, stream);
+}
+
+moe_status_t moe_layer_stack_resident(int nlayers, const moe_router_t* routers, const moe_experts_t* experts,
+                                      const void* const* x, moe_dtype_t x_dtype, int chain,
+                                      const uint8_t* const* resident, float threshold, int32_t* const* idx,
+                                      float* const* w, int32_t* const* idx_used, uint8_t* const* sub_flag,
+                                      float* const* sub_mass, float* const* y, void* const* x_next, void* workspace,
+                                      size_t ws_bytes, void* stream) {
+    if (!resident) return MOE_ERR_INVALID_ARG;
+    return layer_stack_impl(nlayers, routers, experts, x, x_dtype, chain, resident, threshold, idx, w, idx_used,
+                            sub_flag, sub_mass, y, x_next, workspace, ws_bytes, stream);
 }
 
 moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* experts, const void* x,

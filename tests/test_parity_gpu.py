@@ -405,6 +405,50 @@ def test_layer_stack_independent_equals_single_layers(cfg1_layers):
         assert torch.equal(one["y"], y[l].cpu())
 
 
+@pytest.mark.parametrize("threshold", [0.15, 0.0])
+def test_layer_stack_resident_matches_single_layers_and_oracle(cfg3_layer, threshold):
+    """moe_layer_stack_resident: four layers (the cfg3 layer with four masks and
+    four tokens) in one launch give bit-identical outputs to one
+    moe_layer_resident call per layer, and each layer's substitution matches
+    the oracle's routing followed by the oracle's rule."""
+    cfg, layer, mask0 = cfg3_layer
+    L, k = 4, cfg.k
+    masks = [mask0] + [W.make_resident_mask(cfg, l, DEV) for l in range(1, L)]
+    router = M.Router(layer["Wr"], layer["bias"], k)
+    experts = M.Experts.from_layer(layer, cfg.qbits)
+    xs = [W.make_tokens(cfg, 1, 60 + l, DEV) for l in range(L)]
+
+    def outs():
+        return dict(idx=[torch.empty(1, k, dtype=torch.int32, device=DEV) for _ in range(L)],
+                    w=[torch.empty(1, k, device=DEV) for _ in range(L)],
+                    used=[torch.full((1, k), -9, dtype=torch.int32, device=DEV) for _ in range(L)],
+                    flag=[torch.full((1, k), 9, dtype=torch.uint8, device=DEV) for _ in range(L)],
+                    mass=[torch.empty(1, device=DEV) for _ in range(L)],
+                    y=[torch.empty(1, cfg.D, device=DEV) for _ in range(L)],
+                    xn=[torch.empty_like(xs[0]) for _ in range(L)])
+    st = outs()
+    ws = M.workspace(M.MOE_OP_LAYER, 1, k, cfg.E, cfg.D, cfg.F, DEV)
+    M.moe_layer_stack_resident([router] * L, [experts] * L, xs, False, masks, threshold, st["idx"], st["w"],
+                               st["used"], st["flag"], st["mass"], st["y"], st["xn"], ws)
+    assert M.moe_check_status(ws) == M.MOE_OK
+    one = outs()
+    ws1 = M.workspace(M.MOE_OP_LAYER_RESIDENT, 1, k, cfg.E, cfg.D, cfg.F, DEV)
+    for l in range(L):
+        M.moe_layer_resident(router, experts, xs[l], masks[l], threshold, one["idx"][l], one["w"][l], None,
+                             one["used"][l], one["flag"][l], one["mass"][l], one["y"][l], one["xn"][l], ws1)
+    assert M.moe_check_status(ws1) == M.MOE_OK
+    for l in range(L):
+        for n in ("idx", "w", "used", "flag", "mass", "y", "xn"):
+            assert torch.equal(st[n][l], one[n][l]), f"layer {l}: {n} differs from the single-layer call"
+        ref = oracle.router(xs[l], layer["Wr"], layer["bias"], k)
+        label = f"stack_resident E512 thr={threshold} layer {l}"
+        check_routing(ref, dict(idx=st["idx"][l].cpu(), w=st["w"][l].cpu()), k, max_skip_frac=1.0, label=label)
+        parity.check_substitution(ref, masks[l].cpu().numpy(), threshold,
+                                  dict(idx_used=st["used"][l].cpu().numpy(), flag=st["flag"][l].cpu().numpy(),
+                                       mass=st["mass"][l].cpu().numpy()), label=label)
+        check_y(layer, xs[l], dict(idx=st["used"][l].cpu(), w=st["w"][l].cpu(), y=st["y"][l].cpu()), cfg.qbits)
+
+
 # ------------------------------------------------------ bounded waits
 
 def test_wait_limit_runs_out_and_the_workspace_recovers(cfg1_layers):
