@@ -818,9 +818,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                 }
             }
         }
-        if (tid == 32) issue_down();
+        // the down rows are requested by one thread of a warp that streams
+        // the fewest pairs, once that warp's pairs are in: the gate/up bytes,
+        // which the activation exchange waits for, go first, and the down rows
+        // stream in during that exchange
+        if (tid == (kFWarps - 2) * 32) issue_down();
         // without residency the weights are needed only by the combine: the
-        // last warp, which streams the fewest pairs, computes them
+        // last warp, which also streams the fewest pairs, computes them
         if (P.has_router && !Y.resident && warp == kFWarps - 1) route_weights(false);
         __syncthreads();  // the staging region is free again
         // ------------------------------------------------------ phase 4
