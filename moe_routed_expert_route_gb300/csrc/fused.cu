@@ -17,29 +17,35 @@
 // each carries the current tag: no counter, flag or memory fence is involved.
 //   0  before waiting on the previous launch: a bulk copy brings this CTA's
 //      rows of the router weights (1-7 experts) into shared memory
-//   1  x -> shared memory; the CTA's logits -> workspace (tagged); x -> 16-bit
-//      fixed-point planes for the integer dots
-//   2  every CTA polls the E logits (one or two per thread), takes the fp32
-//      softmax with two block reductions, and selects the top k: each warp
-//      extracts the k largest of its 32 probabilities (largest first, lower id
-//      on equal values) with warp max-reductions, and warp 0 extracts the k
-//      largest of those candidates. A residency mask adds the substitution:
-//      each warp also extracts its 2k-1 best resident experts, from which warp
-//      0 takes the replacements in rank order
-//   3  one thread starts bulk copies of this CTA's rows of the k down
-//      matrices into shared memory while the 16 warps stream this CTA's share
-//      of the k*F gate/up row pairs from HBM (two row pairs in flight per warp)
-//      and publish h = silu(g)*u (tagged)
-//   4  the CTA reads all k*F activations once (eight 16-byte loads in flight
-//      per thread) and turns them into 16-bit fixed point (one power-of-two
-//      scale per block of 32 units); each warp takes a (slot, share of the
-//      CTA's rows) task, holds the slot's activations in registers and dots
-//      them with the staged down rows (integer dp4a); the CTA combines the k
-//      slots in slot order, y[d] = sum_r w[r] * o_r[d], and writes x_next = x + y
+//   1  x -> shared memory (in a stack, after the first layer: each warp stages
+//      its 512-byte chunks of the previous layer's tagged x_next); each warp
+//      dots its chunks of x with this CTA's router rows, and one thread per
+//      expert adds the warps' shares in warp order and publishes the logit
+//      (tagged); x -> 16-bit fixed-point planes for the integer dots
+//   2  every CTA polls the E logits (one or two per thread) and selects the
+//      top k by logit (softmax keeps the order): each warp ranks its 32 logits
+//      (largest first, lower id on equal values) and keeps its k best as
+//      candidates, which are then ranked among themselves; the block max and
+//      the fp32 softmax sum are formed alongside, and the weights
+//      exp(l - max)/sum are computed after the streaming. A residency mask adds
+//      the substitution: each warp also ranks its 2k-1 best resident experts,
+//      from which warp 0 takes the replacements in rank order, before streaming
+//   3  the 16 warps stream this CTA's share of the k*F gate/up row pairs from
+//      HBM (all of a warp's pairs requested at once: two in registers, a third
+//      by cp.async into shared memory) and publish h = silu(g)*u (tagged); a
+//      warp that streams two pairs then starts bulk copies of this CTA's rows
+//      of the k down matrices into shared memory
+//   4  each warp reads its chunks of the k*F tagged activations with 16-byte
+//      loads and turns each chunk, once complete, into 16-bit fixed point (one
+//      power-of-two scale per block of 32 units); each warp takes a (slot,
+//      share of the CTA's rows) task, holds the slot's activations in
+//      registers and dots them with the staged down rows (integer dp4a); the
+//      CTA combines the k slots in slot order, y[d] = sum_r w[r] * o_r[d], and
+//      writes x_next = x + y
 // In a stack, layer l+1 starts when every word of layer l's x_next has
-// arrived: in chained mode those words are its token, otherwise its own
-// input, read only after that wait either way. The next layer's router rows
-// are copied in while the current layer streams.
+// arrived: in chained mode those words are its token; otherwise its own token,
+// copied in with its router rows while layer l streams, stands in for them
+// chunk by chunk, so that the work waits as in a chain.
 // Without a router (moe_decode) phases 0-2 are replaced by reading idx/w.
 #include <mutex>
 
