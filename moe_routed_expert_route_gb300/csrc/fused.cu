@@ -35,13 +35,14 @@
 //      by cp.async into shared memory) and publish h = silu(g)*u (tagged); a
 //      warp that streams two pairs then starts bulk copies of this CTA's rows
 //      of the k down matrices into shared memory
-//   4  each warp reads its chunks of the k*F tagged activations with 16-byte
-//      loads and turns each chunk, once complete, into 16-bit fixed point (one
-//      power-of-two scale per block of 32 units); each warp takes a (slot,
-//      share of the CTA's rows) task, holds the slot's activations in
-//      registers and dots them with the staged down rows (integer dp4a); the
-//      CTA combines the k slots in slot order, y[d] = sum_r w[r] * o_r[d], and
-//      writes x_next = x + y
+//   4  each warp takes a (slot, share of the CTA's rows) task; the warps of a
+//      slot read that slot's tagged activations with 16-byte loads and turn
+//      each chunk, once complete, into 16-bit fixed point (one power-of-two
+//      scale per block of 32 units), then, synchronised among themselves only,
+//      hold the slot's activations in registers and dot them with the staged
+//      down rows (integer dp4a), so a slot whose activations arrive early is
+//      not held up by the others; the CTA combines the k slots in slot order,
+//      y[d] = sum_r w[r] * o_r[d], and writes x_next = x + y
 // In a stack, layer l+1 starts when every word of layer l's x_next has
 // arrived: in chained mode those words are its token; otherwise its own token,
 // copied in with its router rows while layer l streams, stands in for them
@@ -153,6 +154,11 @@ __device__ __forceinline__ void fx_store_block1(float v, int blk, int lane, int 
     hi[pos] = (int8_t)(X >> 8);
     lo[pos] = (uint8_t)(X & 0xff);
     if (lane == 0) scale[blk] = f.scale;
+}
+
+// Barrier over the nthreads threads (whole warps) that call it with this id.
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Max and sum of the 16 per-warp partials, in a fixed order.
@@ -837,14 +843,23 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
         // every slot's activations, gathered from the tagged words and turned
         // into 16-bit fixed point, one power-of-two scale per block of 32 units
         // (4 units per lane, 8 lanes per block)
+        // with k * (16 / k) = 16 down tasks and whole chunks per slot, the two
+        // (or more) warps of a slot's down tasks gather that slot's chunks
+        // themselves and start its down dot as soon as they have them
+        const int nsplit = k >= kFWarps ? 1 : kFWarps / k;
+        const int cpr = F / kChunk;  // chunks per slot
+        const bool by_slot = k * nsplit == kFWarps && F % kChunk == 0 && cpr % nsplit == 0;
         {
-            // a warp's chunks are c = warp, warp + 16, ...; four units per lane,
-            // read with 16-byte loads straight into registers (the bulk-copy
-            // engine is left to the down rows), up to four chunks in flight,
-            // each converted as soon as all of its words carry the tag
+            // a warp's chunks are c = warp, warp + 16, ... (or its slot's share);
+            // four units per lane, read with 16-byte loads straight into
+            // registers (the bulk-copy engine is left to the down rows), up to
+            // four chunks in flight, each converted as soon as all of its words
+            // carry the tag
             const int nw_ = k * F;
             const int nch = (nw_ + kChunk - 1) / kChunk;
-            const int mine = warp < nch ? (nch - warp + kFWarps - 1) / kFWarps : 0;
+            const int mine = by_slot ? cpr / nsplit : (warp < nch ? (nch - warp + kFWarps - 1) / kFWarps : 0);
+            const int cbase = by_slot ? (warp / nsplit) * cpr + (warp % nsplit) * (cpr / nsplit) : warp;
+            const int cstep = by_slot ? 1 : kFWarps;
             const long long t0 = clock64();
             bool gave_up = false;  // warp-uniform
 #pragma unroll 1
@@ -858,7 +873,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
                     uint64_t w[4][4];
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
-                        const int u = (warp + kFWarps * (i0 + i)) * kChunk + 4 * lane;
+                        const int u = (cbase + cstep * (i0 + i)) * kChunk + 4 * lane;
                         if ((pend >> i & 1u) && u < nw_) {
                             ld_tagged2(P.h + u, w[i][0], w[i][1]);
                             ld_tagged2(P.h + u + 2, w[i][2], w[i][3]);
@@ -870,7 +885,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
                         if (!(pend >> i & 1u)) continue;
-                        const int u = (warp + kFWarps * (i0 + i)) * kChunk + 4 * lane;
+                        const int u = (cbase + cstep * (i0 + i)) * kChunk + 4 * lane;
                         const bool good = tag_ok(w[i][0], tag) && tag_ok(w[i][1], tag) && tag_ok(w[i][2], tag) &&
                                           tag_ok(w[i][3], tag);
                         if (!__all_sync(kFull, good)) {
@@ -894,7 +909,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             ab = true;
             mbar_wait(&s_bar, l & 1, status);  // the copies into this CTA's memory must land first
         }
-        __syncthreads();
+        if (by_slot) {
+            // the slot's warps (barrier ids 1..k, k <= 8); a slot of one warp needs none
+            if (nsplit > 1) named_bar_sync(1 + warp / nsplit, 32 * nsplit);
+            else __syncwarp();
+        } else {
+            __syncthreads();
+        }
 
         // down: task = (slot, share of the CTA's rows); the warp keeps the
         // slot's activation planes in registers and dots them with each row
@@ -903,7 +924,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_layer_kernel(const __grid_
             constexpr int EPP = QB == 8 ? 8 : 16;
             constexpr int NW = EPP / 4;  // plane words per piece and plane
             const int npieces = rowF / 8;
-            const int nsplit = k >= kFWarps ? 1 : kFWarps / k;
             const int ntask = k * nsplit;
 #pragma unroll 1
             for (int task = warp; task < ntask; task += kFWarps) {
