@@ -154,8 +154,61 @@ static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
     return fn;
 }
 
+// The encoded maps of recent calls, keyed by every argument of the encoding
+// (a map depends on nothing else), so that a layer called again with the same
+// buffers does not pay the driver's encoding on every call.
+namespace {
+struct TmapKey {
+    const void* base;
+    unsigned long long inner, rows, row_bytes;
+    unsigned box_inner, box_rows;
+    int dtype, swizzle;
+    bool operator==(const TmapKey& o) const {
+        return base == o.base && inner == o.inner && rows == o.rows && row_bytes == o.row_bytes &&
+               box_inner == o.box_inner && box_rows == o.box_rows && dtype == o.dtype && swizzle == o.swizzle;
+    }
+};
+constexpr int kTmapCache = 64;
+struct TmapCache {
+    std::mutex mu;
+    TmapKey key[kTmapCache];
+    CUtensorMap map[kTmapCache];
+    int n = 0, next = 0;
+};
+TmapCache& tmap_cache() {
+    static TmapCache c;
+    return c;
+}
+}  // namespace
+
+static bool encode_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long long inner,
+                           unsigned long long rows, unsigned long long row_bytes, unsigned box_inner,
+                           unsigned box_rows, int swizzle);
+
 bool make_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long long inner, unsigned long long rows,
                   unsigned long long row_bytes, unsigned box_inner, unsigned box_rows, int swizzle) {
+    const TmapKey k = {base, inner, rows, row_bytes, box_inner, box_rows, dtype, swizzle};
+    TmapCache& c = tmap_cache();
+    {
+        std::lock_guard<std::mutex> lock(c.mu);
+        for (int i = 0; i < c.n; i++)
+            if (c.key[i] == k) {
+                *m = c.map[i];
+                return true;
+            }
+    }
+    if (!encode_tmap_2d(m, dtype, base, inner, rows, row_bytes, box_inner, box_rows, swizzle)) return false;
+    std::lock_guard<std::mutex> lock(c.mu);
+    const int i = c.n < kTmapCache ? c.n++ : c.next;
+    c.next = (i + 1) % kTmapCache;
+    c.key[i] = k;
+    c.map[i] = *m;
+    return true;
+}
+
+static bool encode_tmap_2d(CUtensorMap* m, int dtype, const void* base, unsigned long long inner,
+                           unsigned long long rows, unsigned long long row_bytes, unsigned box_inner,
+                           unsigned box_rows, int swizzle) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, rows};
