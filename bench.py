@@ -296,10 +296,10 @@ def _host_layer(lw):
 _EXPERT_TENSORS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 
 
-def timed_oracle_moe(layer, x, idx, w, qbits, nthreads) -> float:
+def timed_oracle_moe(layer, x, idx, w, qbits, nthreads):
     """oracle.moe on host copies of the routed experts' rows; returns the
     seconds of the oracle call alone (the device-to-host copy is not timed:
-    its speed depends on the host link, not on the oracle)."""
+    its speed depends on the host link, not on the oracle) and y."""
     import numpy as np
     import oracle
     idx = np.asarray(idx)
@@ -308,8 +308,8 @@ def timed_oracle_moe(layer, x, idx, w, qbits, nthreads) -> float:
     sub = {n: layer[n][sel].cpu() for n in _EXPERT_TENSORS}
     idx_c = remap.reshape(idx.shape).astype(np.int32)
     t0 = time.perf_counter()
-    oracle.moe(sub, x, idx_c, w, qbits, nthreads=nthreads, compact=False)
-    return time.perf_counter() - t0
+    y = oracle.moe(sub, x, idx_c, w, qbits, nthreads=nthreads, compact=False)
+    return time.perf_counter() - t0, y
 
 
 def oracle_decode_rate(cfg, layers, ntok: int, threads: int, warmup: int = 1):
@@ -329,7 +329,7 @@ def oracle_decode_rate(cfg, layers, ntok: int, threads: int, warmup: int = 1):
             t0 = time.perf_counter()
             r = oracle.router(xs[i, l], host[l][0], host[l][1], cfg.k)
             el += time.perf_counter() - t0
-            el += timed_oracle_moe(layers[l], xs[i, l], r["idx"], r["w"], cfg.qbits, threads)
+            el += timed_oracle_moe(layers[l], xs[i, l], r["idx"], r["w"], cfg.qbits, threads)[0]
         return el
 
     for i in range(warmup):
@@ -534,7 +534,7 @@ def run_substitution(args, dev):
             r = oracle.router(xs[i, l], host[l][0], host[l][1], k)
             s = oracle.substitute(r["probs32"], r["idx"], r["w"], hmask[l], cfg.threshold)
             el += time.perf_counter() - t0
-            el += timed_oracle_moe(layers[l], xs[i, l], s["idx"], s["w"], cfg.qbits, nth)
+            el += timed_oracle_moe(layers[l], xs[i, l], s["idx"], s["w"], cfg.qbits, nth)[0]
         return el
 
     token(0)
@@ -600,7 +600,7 @@ def run_prefill(args, dev, stack, T):
     t0 = time.perf_counter()
     r = oracle.router(xs, wr, br, cfg.k)
     el = time.perf_counter() - t0
-    el += timed_oracle_moe(layers[0], xs, r["idx"], r["w"], cfg.qbits, nth)
+    el += timed_oracle_moe(layers[0], xs, r["idx"], r["w"], cfg.qbits, nth)[0]
     del ws
     torch.cuda.empty_cache()
     return {"workload": f"prefill T={T} E=256 top-8 D=2048 F=768 int8 (fp16 tensor-core operands)",
