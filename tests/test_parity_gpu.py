@@ -224,7 +224,7 @@ def test_decode_e256_chain_matches_oracle(cfg1_layers):
     assert skipped <= 1
 
 
-@pytest.mark.parametrize("T", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("T", [1, 2, 4, 7, 8, 16, 32, 64])
 def test_batched_decode_sweep(cfg1_layers, T):
     cfg, layers = cfg1_layers
     layer = layers[0]
@@ -316,7 +316,7 @@ def test_substitution_and_int4_decode(cfg3_layer, T, threshold):
     print(f"T={T} thr={threshold}: substituted {n_sub}/{T * k}, mass mean {mass.mean().item():.4f}")
 
 
-@pytest.mark.parametrize("T", [1, 2, 16])
+@pytest.mark.parametrize("T", [1, 2, 7, 16])
 @pytest.mark.parametrize("threshold", [0.15, 0.0, float("inf")])
 def test_layer_resident_matches_oracle(cfg3_layer, T, threshold):
     """moe_layer_resident: routing, substitution and int4 experts in one call
