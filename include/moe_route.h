@@ -248,6 +248,53 @@ moe_status_t moe_layer_stack_resident(int nlayers, const moe_router_t* routers, 
                                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Router-logit replay simulator (host code, no GPU): gist.science "Which
+ * expert misses are worth waiting for?", method section (the C++ tool that
+ * replays router outputs to compare policies, estimating the time per token
+ * and the cache state; the fetch-all, 0.15 and first-choice rules; background
+ * admission of substituted experts; frequency-based eviction).
+ * Per token and layer: the top-k of the layer's probabilities (descending,
+ * lower id on equal values; weights renormalised over the k in double); each
+ * routed expert's frequency grows by one; slots in rank order: a resident
+ * expert is a hit; a miss the policy fetches is a synchronous fetch and enters
+ * the cache; another miss is substituted by the resident expert of highest
+ * probability neither routed nor already chosen (lower id on ties), its weight
+ * adds to the token's substituted mass and to the missed expert's accumulated
+ * mass, and at admit_mass the expert enters the cache in the background (its
+ * accumulation restarts); a miss with no candidate left is fetched. An expert
+ * entering the cache evicts the resident expert of lowest frequency (lower id
+ * on ties) that the token does not use in that layer; with none it is used
+ * without entering. Time per token = sum over layers of t_layer_us +
+ * (synchronous fetches) * t_fetch_us.
+ *   probs        host [N][L][E] fp32: the router's probabilities per token and layer
+ *   resident     host [L][E] uint8 in/out: the cache (its size per layer is kept)
+ *   freq         host [L][E] int32 in/out: routing counts (zero for a fresh replay)
+ *   acc          host [L][E] double in/out: accumulated substituted mass
+ *   t_token_us, fetches, substituted, sub_mass, admissions
+ *                host [N] out: estimated time, synchronous fetches, substituted
+ *                slots, substituted mass and background admissions of each
+ *                token, summed over its layers
+ * Returns MOE_ERR_INVALID_ARG for bad sizes, pointers or policy values.
+ */
+typedef enum {
+    MOE_POLICY_FETCH_ALL = 0,   /* every miss is fetched */
+    MOE_POLICY_THRESHOLD = 1,   /* a miss is fetched if first choice or weight >= threshold */
+    MOE_POLICY_FIRST_CHOICE = 2 /* only a first-choice miss is fetched */
+} moe_policy_t;
+
+typedef struct {
+    moe_policy_t policy;
+    float threshold;   /* MOE_POLICY_THRESHOLD (0.15 on the page) */
+    float admit_mass;  /* background admission threshold (0.5 on the page); 0 = none */
+    double t_layer_us; /* compute time of one layer */
+    double t_fetch_us; /* time of one synchronous expert fetch */
+} moe_replay_policy_t;
+
+moe_status_t moe_replay(int N, int L, int E, int k, const float* probs, const moe_replay_policy_t* policy,
+                        uint8_t* resident, int32_t* freq, double* acc, double* t_token_us, int32_t* fetches,
+                        int32_t* substituted, double* sub_mass, int32_t* admissions);
+
+/*
  * Prefill of T tokens: router, then the (token, slot) assignments grouped by
  * expert (histogram, exclusive scan, stable permutation), a grouped matrix
  * product per expert on the tensor cores, and the weighted un-permute.

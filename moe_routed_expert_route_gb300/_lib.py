@@ -29,6 +29,7 @@ MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_LAYER, MOE_OP_PREFILL, MOE_OP_LAYER_RESIDENT
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_substitute", "moe_decode", "moe_layer",
             "moe_layer_resident", "moe_layer_stack", "moe_layer_stack_resident", "moe_prefill", "moe_layer_noalloc",
+            "moe_replay",
             "moe_check_status", "moe_set_wait_limit", "moe_status_string")
 
 
@@ -42,6 +43,14 @@ class _Router(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int), ("D", ctypes.c_int), ("k", ctypes.c_int),
                 ("w_dtype", ctypes.c_int), ("W", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("norm_topk", ctypes.c_int)]
+
+
+class _ReplayPolicy(ctypes.Structure):
+    _fields_ = [("policy", ctypes.c_int), ("threshold", ctypes.c_float), ("admit_mass", ctypes.c_float),
+                ("t_layer_us", ctypes.c_double), ("t_fetch_us", ctypes.c_double)]
+
+
+MOE_POLICY_FETCH_ALL, MOE_POLICY_THRESHOLD, MOE_POLICY_FIRST_CHOICE = 0, 1, 2
 
 
 class _Experts(ctypes.Structure):
@@ -68,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_noalloc.argtypes = [P, P, P, I, P, P, P, P, P, P]
     lib.moe_layer_resident.argtypes = [P, P, P, I, I, P, ctypes.c_float, P, P, P, P, P, P, P, P, P, S, P]
     lib.moe_layer_stack.argtypes = [I, P, P, P, I, I, P, P, P, P, P, S, P]
+    lib.moe_replay.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, P]
     lib.moe_layer_stack_resident.argtypes = [I, P, P, P, I, I, P, ctypes.c_float, P, P, P, P, P, P, P, P, S, P]
     lib.moe_check_status.argtypes = [P, P]
     lib.moe_set_wait_limit.argtypes = [P, ctypes.c_ulonglong, P]
@@ -390,3 +400,36 @@ def moe_check_status(ws: torch.Tensor, stream=None) -> int:
 def moe_set_wait_limit(ws: torch.Tensor, cycles: int, stream=None):
     """Longest spin of any device wait on this workspace (clock64 cycles; 0 = default)."""
     _check("moe_set_wait_limit", _lib.moe_set_wait_limit(_ptr(ws), int(cycles), _stream(stream)))
+
+
+def moe_replay(probs, k: int, policy: int, threshold: float = 0.15, admit_mass: float = 0.0,
+               t_layer_us: float = 0.0, t_fetch_us: float = 0.0, resident=None, freq=None, acc=None) -> dict:
+    """Router-logit replay on the host (see moe_replay in the header).
+
+    probs: numpy float32 [N][L][E]. resident [L][E] uint8, freq [L][E] int32 and
+    acc [L][E] float64 are the cache state, updated in place (freq and acc start
+    at zero when not given). Returns the per-token outputs and the state."""
+    import numpy as np
+    probs = np.ascontiguousarray(probs, dtype=np.float32)
+    if probs.ndim != 3:
+        raise ValueError("probs must be [N][L][E]")
+    N, L, E = probs.shape
+    if resident is None:
+        raise ValueError("resident [L][E] is required")
+    for name, a, dt in (("resident", resident, np.uint8), ("freq", freq, np.int32), ("acc", acc, np.float64)):
+        if a is not None and (a.dtype != dt or a.shape != (L, E) or not a.flags["C_CONTIGUOUS"]):
+            raise ValueError(f"{name} must be a contiguous {np.dtype(dt).name} array of shape {(L, E)}")
+    freq = np.zeros((L, E), np.int32) if freq is None else freq
+    acc = np.zeros((L, E), np.float64) if acc is None else acc
+    out = dict(t_token_us=np.zeros(N, np.float64), fetches=np.zeros(N, np.int32),
+               substituted=np.zeros(N, np.int32), sub_mass=np.zeros(N, np.float64),
+               admissions=np.zeros(N, np.int32))
+    pol = _ReplayPolicy(int(policy), float(threshold), float(admit_mass), float(t_layer_us), float(t_fetch_us))
+
+    def p(a):
+        return ctypes.c_void_p(a.ctypes.data)
+    _check("moe_replay", _lib.moe_replay(N, L, E, int(k), p(probs), ctypes.byref(pol), p(resident), p(freq), p(acc),
+                                         p(out["t_token_us"]), p(out["fetches"]), p(out["substituted"]),
+                                         p(out["sub_mass"]), p(out["admissions"])))
+    out.update(resident=resident, freq=freq, acc=acc)
+    return out
