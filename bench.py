@@ -539,16 +539,86 @@ def run_substitution(args, dev):
 
     token(0)
     el = sum(token(i) for i in range(1, ntok + 1))
-    del layers
+    t_layer = next(r["us_per_layer"] for r in res if r["T"] == 1)
+    replay = run_replay(args, dev, cfg, routers, masks, t_layer)
+    del layers, routers, experts
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-    return {"workload": f"substitution 0.15 rule + int4 experts, E=512 top-10 D=2048 F=512, 25% resident, "
+    return replay, {"workload": f"substitution 0.15 rule + int4 experts, E=512 top-10 D=2048 F=512, 25% resident, "
                         f"{L} layers", "unit": "tokens/s", "points": res,
             "cpu_baseline": {"value": round(ntok / el, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
                              "sample": f"{ntok} tokens x {L} layers (router + substitution + routed experts, on host "
                                        f"copies of the routed experts' rows, copies not timed) after "
                                        f"1 warm-up token, {el:.1f} s"},
             "clocks": clk.summary()}
+
+
+def run_replay(args, dev, cfg, routers, masks, t_layer_us):
+    """Router-logit replay: the GPU router logs the probabilities of N tokens
+    through the layers, and the host simulator replays them under the page's
+    policies, with a time model measured here: the one-token layer time of the
+    substitution workload and the time to copy one expert from pinned host
+    memory."""
+    import numpy as np
+    import moe_routed_expert_route_gb300 as M
+    from oracle import replay as oracle_replay
+    L, E, k = len(routers), cfg.E, cfg.k
+    N = 512
+    # the router's probabilities, per layer for the N tokens (on the GPU)
+    x = W.make_tokens(cfg, N * L, 31, dev).view(L, N, cfg.D)
+    probs = torch.empty(L, N, E, device=dev)
+    idx = torch.empty(N, k, dtype=torch.int32, device=dev)
+    w = torch.empty(N, k, device=dev)
+    ws = M.workspace(M.MOE_OP_ROUTE, N, k, E, cfg.D, cfg.F, dev)
+    for l in range(L):
+        M.moe_route(routers[l], x[l], idx, w, probs[l], ws)
+    assert M.moe_check_status(ws) == 0
+    P = probs.transpose(0, 1).contiguous().cpu().numpy()  # [N][L][E]
+    res0 = torch.stack(masks).cpu().numpy().astype(np.uint8)
+    # one expert from pinned host memory to the device
+    nb = W.routed_bytes_per_expert(cfg)
+    host = torch.empty(nb, dtype=torch.uint8, pin_memory=True)
+    devbuf = torch.empty(nb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            devbuf.copy_(host, non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(50):
+            devbuf.copy_(host, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    t_fetch = a.elapsed_time(b) * 1e3 / 50
+    policies = [("fetch every miss", M.MOE_POLICY_FETCH_ALL, 0.0), ("0.15 rule", M.MOE_POLICY_THRESHOLD, 0.0),
+                ("first-choice rule", M.MOE_POLICY_FIRST_CHOICE, 0.0),
+                ("quality-first: 0.15 rule + admission at 0.5", M.MOE_POLICY_THRESHOLD, 0.5),
+                ("speed-first: first-choice rule + admission at 0.5", M.MOE_POLICY_FIRST_CHOICE, 0.5)]
+    out = []
+    for name, pol, beta in policies:
+        t0 = time.perf_counter()
+        r = M.moe_replay(P, k, pol, 0.15, beta, t_layer_us, t_fetch, resident=res0.copy())
+        el = time.perf_counter() - t0
+        ms_tok = float(r["t_token_us"].mean()) / 1e3
+        out.append({"policy": name, "est_ms_per_token": round(ms_tok, 4), "est_tokens_per_s": round(1e3 / ms_tok, 1),
+                    "sync_fetches_per_token": round(float(r["fetches"].mean()), 3),
+                    "substituted_frac": round(float(r["substituted"].sum()) / (N * L * k), 4),
+                    "sub_mass_per_layer": round(float(r["sub_mass"].mean()) / L, 4),
+                    "admissions_per_token": round(float(r["admissions"].mean()), 3),
+                    "replay_tokens_per_s": round(N / el, 1)})
+    # the oracle on a sample, quality-first policy
+    ns = 48
+    t0 = time.perf_counter()
+    oracle_replay.replay(P[:ns], k, oracle_replay.THRESHOLD, 0.15, 0.5, t_layer_us, t_fetch, resident=res0.tolist())
+    el = time.perf_counter() - t0
+    return {"workload": f"router-logit replay: {N} tokens x {L} layers of GPU-logged router probabilities, "
+                        f"E={E} top-{k}, 25% resident; the simulator runs on the host",
+            "unit": "tokens/s (replayed)", "t_layer_us": t_layer_us, "t_fetch_us": round(t_fetch, 2),
+            "expert_bytes": nb, "policies": out,
+            "roofline": None,
+            "cpu_baseline": {"value": round(ns / el, 2), "unit": "tokens/s (replayed)", "cores": 1,
+                             "kind": "oracle", "sample": f"{ns} tokens x {L} layers, quality-first policy, "
+                                                         f"{el:.2f} s"}}
 
 
 def run_prefill(args, dev, stack, T):
@@ -642,7 +712,7 @@ def run_ours(args):
         del stack
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-        extra["substitution"] = run_substitution(args, dev)
+        extra["replay"], extra["substitution"] = run_substitution(args, dev)
         line["workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
