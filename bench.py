@@ -606,8 +606,8 @@ def run_replay(args, dev, cfg, routers, masks, t_layer_us):
                     "sub_mass_per_layer": round(float(r["sub_mass"].mean()) / L, 4),
                     "admissions_per_token": round(float(r["admissions"].mean()), 3),
                     "replay_tokens_per_s": round(N / el, 1)})
-    # the oracle on a sample, quality-first policy
-    ns = 48
+    # the oracle on the same tokens, quality-first policy
+    ns = N
     t0 = time.perf_counter()
     oracle_replay.replay(P[:ns], k, oracle_replay.THRESHOLD, 0.15, 0.5, t_layer_us, t_fetch, resident=res0.tolist())
     el = time.perf_counter() - t0
