@@ -20,7 +20,8 @@
  *            (num_experts, output_dims, input_dims) layout of the lilting.ch
  *            article, section "warm-up vs mmap cache")
  *
- * Conventions for every entry point:
+ * Conventions for every entry point (moe_replay, host code, takes host arrays
+ * and has no stream or workspace):
  *  - All array arguments are DEVICE pointers owned by the caller; descriptor
  *    structs are host memory read during the call only. The library allocates
  *    nothing and keeps no state between calls; it is reentrant as long as two
@@ -38,12 +39,13 @@
  *  - Workspace: `ws_bytes` >= moe_workspace_bytes(op, ...). It must be zeroed
  *    once before its first use (cudaMemset). Its header holds a launch sequence
  *    number that keeps growing from call to call; do not clear it afterwards.
- *  - Calls of up to 7 tokens run a persistent kernel (one launch per token) with one CTA per SM
- *    whose CTAs wait on one another (bounded waits, about 30 ms by default,
- *    see moe_set_wait_limit). It needs every SM of the device: a kernel running
- *    at the same time on another stream can hold SMs until a wait runs out, in
- *    which case the call records MOE_ERR_DEVICE_TIMEOUT and its outputs are not
- *    valid. Do not run other kernels concurrently with these calls.
+ *  - Calls of up to 7 tokens run a persistent kernel (one launch per token)
+ *    with one CTA per SM whose CTAs wait on one another (bounded waits, about
+ *    30 ms by default, see moe_set_wait_limit). It needs every SM of the
+ *    device: a kernel running at the same time on another stream can hold SMs
+ *    until a wait runs out, in which case the call records
+ *    MOE_ERR_DEVICE_TIMEOUT and its outputs are not valid. Do not run other
+ *    kernels concurrently with these calls.
  *  - Alignment: every pointer 16-byte aligned; D and F multiples of 32, so
  *    every int8 row (D or F bytes) and int4 row (D/2 or F/2 bytes) starts on a
  *    16-byte boundary.
