@@ -42,8 +42,10 @@ def _bind(lib):
     lib.oracle_moe.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, P, i]
     lib.oracle_permute.argtypes = [i, i, i, P, P, P, P, P, P]
     lib.oracle_max_threads.argtypes = []
+    lib.oracle_shared_lora.argtypes = [i, i, i, i, i] + [P] * 12 + [ctypes.c_double, P, P]
+    lib.oracle_prerouter.argtypes = [i, i, i, i, i, i] + [P] * 13
     for f in ("oracle_router", "oracle_substitute", "oracle_moe", "oracle_permute",
-              "oracle_max_threads"):
+              "oracle_max_threads", "oracle_shared_lora", "oracle_prerouter"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -184,6 +186,63 @@ def layer_forward(layer: dict, x, k: int, qbits: int, norm_topk: bool = True,
     r = router(x, layer["Wr"], layer.get("bias"), k, norm_topk, lib=lib)
     r["y"] = moe(layer, x, r["idx"], r["w"], qbits, nthreads, lib=lib)
     return r
+
+
+def shared_lora(se: dict, x, lib=None) -> np.ndarray:
+    """Shared expert with its unmerged recovery LoRA, y [T][D] in fp64.
+
+    ``se`` holds gate_q/gate_s/up_q/up_s ([F][D] codes, [F][D/32] scales),
+    down_q/down_s ([D][F], [D][F/32]), qbits, and the adapters gate_A/up_A
+    ([r][D]), down_A ([r][F]), gate_B/up_B ([F][r]), down_B ([D][r]) with
+    ``scale`` = alpha / r; r = 0 (or adapters None) is the base expert alone.
+    """
+    x = _f64(x)
+    T, D = x.shape
+    F = se["gate_q"].shape[0]
+    qbits = int(se["qbits"])
+    r = 0 if se.get("gate_A") is None else int(se["gate_A"].shape[0])
+    q = {n: _u8(se[n]) for n in ("gate_q", "up_q", "down_q")}
+    s = {n: _f64(se[n]) for n in ("gate_s", "up_s", "down_s")}
+    empty = np.zeros(1)
+    ad = {n: (_f64(se[n]) if r > 0 else empty)
+          for n in ("gate_A", "gate_B", "up_A", "up_B", "down_A", "down_B")}
+    y = np.empty((T, D))
+    rc = _load(lib).oracle_shared_lora(
+        T, D, F, r, qbits, _p(q["gate_q"]), _p(s["gate_s"]), _p(q["up_q"]), _p(s["up_s"]),
+        _p(q["down_q"]), _p(s["down_s"]), _p(ad["gate_A"]), _p(ad["gate_B"]), _p(ad["up_A"]),
+        _p(ad["up_B"]), _p(ad["down_A"]), _p(ad["down_B"]), float(se.get("scale", 0.0)), _p(x),
+        _p(y))
+    if rc != 0:
+        raise ValueError(f"oracle_shared_lora rc={rc}")
+    return y
+
+
+def prerouter(head: dict, x, cur, prev, k: int, norm_topk: bool = True, lib=None) -> dict:
+    """Prerouter head on tokens x with the current and previous tokens' routing
+    ids ``cur``/``prev`` [T][k] (negative = absent): logits, probs (fp64),
+    probs32, and the predicted idx / w used as the next layer's routing.
+
+    ``head`` holds fc1 [H][D+2E], b1 [H] or None, fc2 [E][H], L [E][D+2E],
+    bias [E] or None.
+    """
+    x = _f64(x)
+    T, D = x.shape
+    fc1, fc2, Lw = _f64(head["fc1"]), _f64(head["fc2"]), _f64(head["L"])
+    H = fc1.shape[0]
+    E = fc2.shape[0]
+    b1 = None if head.get("b1") is None else _f64(head["b1"])
+    bias = None if head.get("bias") is None else _f64(head["bias"])
+    cur, prev = _i32(cur), _i32(prev)
+    out = dict(logits=np.empty((T, E)), probs=np.empty((T, E)),
+               probs32=np.empty((T, E), np.float32), idx=np.empty((T, k), np.int32),
+               w=np.empty((T, k)))
+    rc = _load(lib).oracle_prerouter(
+        T, D, E, H, k, int(norm_topk), _p(x), _p(cur), _p(prev), _p(fc1),
+        None if b1 is None else _p(b1), _p(fc2), _p(Lw), None if bias is None else _p(bias),
+        _p(out["logits"]), _p(out["probs"]), _p(out["probs32"]), _p(out["idx"]), _p(out["w"]))
+    if rc != 0:
+        raise ValueError(f"oracle_prerouter rc={rc}")
+    return out
 
 
 def near_tie_tokens(probs32: np.ndarray, k: int, eps: float = 1e-6) -> np.ndarray:

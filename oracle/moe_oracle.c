@@ -22,6 +22,11 @@
  *    slot to that expert's own gated activation, and int8 is sign-extended.
  *  - gist.science "Which expert misses are worth waiting for?": method section,
  *    the fetch-all / 0.15 / first-choice rules and the substituted gate mass m.
+ *  - xyznot.com "The Other Half of the Memory Wall: Serving 35B MoEs from SSD
+ *    with Trained Routing Prediction": method section, the prerouter head
+ *    (input of d_model + 2E values, fc2(erf-gelu(fc1 f)) + a linear path) whose
+ *    prediction is used as the routing, and the unmerged recovery LoRA
+ *    y = W(x) + (alpha/r) B A x on the shared expert's projections.
  */
 #include <math.h>
 #include <stdint.h>
@@ -70,6 +75,34 @@ static int ranks_before(float pa, int a, float pb, int b) {
  *                  probs[t][idx[t][r]]                                 (norm_topk=0)
  * bias may be NULL. Returns 0, or -1 on bad arguments.
  */
+/* Softmax of one token's logits and its top k (the last two router steps):
+ * probs = exp(l - max) / sum, the fp32-rounded probs ranked by a full insertion
+ * sort with the lowest-index tie-break, and the k weights (renormalised if
+ * norm_topk). `order` is scratch of E ints. */
+static void softmax_topk(int E, int k, int norm_topk, const double* lt, double* pt, float* p32,
+                         int* order, int32_t* idx_t, double* w_t) {
+    double mx = lt[0];
+    for (int e = 1; e < E; e++) if (lt[e] > mx) mx = lt[e];
+    double sum = 0.0;
+    for (int e = 0; e < E; e++) { pt[e] = exp(lt[e] - mx); sum += pt[e]; }
+    for (int e = 0; e < E; e++) { pt[e] /= sum; p32[e] = (float)pt[e]; }
+    /* full insertion sort of all experts by the fp32 key, then take k */
+    for (int e = 0; e < E; e++) {
+        int j = e;
+        while (j > 0 && ranks_before(p32[e], e, p32[order[j - 1]], order[j - 1])) {
+            order[j] = order[j - 1];
+            j--;
+        }
+        order[j] = e;
+    }
+    double norm = 0.0;
+    for (int r = 0; r < k; r++) norm += pt[order[r]];
+    for (int r = 0; r < k; r++) {
+        idx_t[r] = order[r];
+        w_t[r] = norm_topk ? pt[order[r]] / norm : pt[order[r]];
+    }
+}
+
 int oracle_router(int T, int E, int D, int k, int norm_topk, const double* x,
                   const double* Wr, const double* bias, double* logits, double* probs,
                   float* probs32, int32_t* idx, double* w) {
@@ -79,33 +112,13 @@ int oracle_router(int T, int E, int D, int k, int norm_topk, const double* x,
     for (int t = 0; t < T; t++) {
         const double* xt = x + (int64_t)t * D;
         double* lt = logits + (int64_t)t * E;
-        double* pt = probs + (int64_t)t * E;
-        float* p32 = probs32 + (int64_t)t * E;
         for (int e = 0; e < E; e++) {
             double acc = 0.0;
             for (int d = 0; d < D; d++) acc += xt[d] * Wr[(int64_t)e * D + d];
             lt[e] = acc + (bias ? bias[e] : 0.0);
         }
-        double mx = lt[0];
-        for (int e = 1; e < E; e++) if (lt[e] > mx) mx = lt[e];
-        double sum = 0.0;
-        for (int e = 0; e < E; e++) { pt[e] = exp(lt[e] - mx); sum += pt[e]; }
-        for (int e = 0; e < E; e++) { pt[e] /= sum; p32[e] = (float)pt[e]; }
-        /* full insertion sort of all experts by the fp32 key, then take k */
-        for (int e = 0; e < E; e++) {
-            int j = e;
-            while (j > 0 && ranks_before(p32[e], e, p32[order[j - 1]], order[j - 1])) {
-                order[j] = order[j - 1];
-                j--;
-            }
-            order[j] = e;
-        }
-        double norm = 0.0;
-        for (int r = 0; r < k; r++) norm += pt[order[r]];
-        for (int r = 0; r < k; r++) {
-            idx[(int64_t)t * k + r] = order[r];
-            w[(int64_t)t * k + r] = norm_topk ? pt[order[r]] / norm : pt[order[r]];
-        }
+        softmax_topk(E, k, norm_topk, lt, probs + (int64_t)t * E, probs32 + (int64_t)t * E, order,
+                     idx + (int64_t)t * k, w + (int64_t)t * k);
     }
     free(order);
     return 0;
@@ -244,6 +257,133 @@ int oracle_moe(int T, int E, int k, int D, int F, int qbits, const uint8_t* gate
     }
     free(o);
     return fail ? -1 : 0;
+}
+
+/* ------------------------------------------- shared expert, unmerged LoRA */
+
+/*
+ * One projection served with an unmerged low-rank adapter (xyznot.com "The
+ * Other Half of the Memory Wall", method section "unmerged adapter execution",
+ * and its FAQ on why the adapter is not merged into the 4-bit weights): the
+ * quantised base is kept as it is and the delta runs beside it,
+ *   out[n] = sum_k dq(W)[n][k] * v[k]  +  scale * sum_j B[n][j] * (sum_k A[j][k] * v[k])
+ * with W [N][K] codes/scales, A [r][K], B [N][r] and scale = alpha / r.
+ * r = 0 is the base projection alone.
+ */
+static void lora_projection(int64_t N, int64_t K, int r, int qbits, const uint8_t* codes,
+                            const double* scales, const double* A, const double* B, double scale,
+                            const double* v, double* av, double* out) {
+    for (int j = 0; j < r; j++) {
+        double acc = 0.0;
+        for (int64_t kk = 0; kk < K; kk++) acc += A[j * K + kk] * v[kk];
+        av[j] = acc;
+    }
+    for (int64_t n = 0; n < N; n++) {
+        double base = 0.0;
+        for (int64_t kk = 0; kk < K; kk++) base += dq(codes, scales, qbits, K, n, kk) * v[kk];
+        double delta = 0.0;
+        for (int j = 0; j < r; j++) delta += B[n * r + j] * av[j];
+        out[n] = base + scale * delta;
+    }
+}
+
+/*
+ * The shared expert of a MoE block with its recovery LoRA (same page: the
+ * adapters sit on the attention, linear-attention and shared-expert
+ * projections, never on the streamed experts), applied to each of T tokens:
+ *   g = Gate(x), u = Up(x)       (gate/up codes [F][D], A [r][D], B [F][r])
+ *   h = g * sigmoid(g) * u       (SwiGLU)
+ *   y = Down(h)                  (down codes [D][F], A [r][F], B [D][r])
+ * every projection as lora_projection above. Returns 0, or -1 on bad arguments.
+ */
+int oracle_shared_lora(int T, int D, int F, int r, int qbits, const uint8_t* gate_q,
+                       const double* gate_s, const uint8_t* up_q, const double* up_s,
+                       const uint8_t* down_q, const double* down_s, const double* gate_A,
+                       const double* gate_B, const double* up_A, const double* up_B,
+                       const double* down_A, const double* down_B, double scale, const double* x,
+                       double* y) {
+    if (T < 0 || D < BLK || F < BLK || D % BLK || F % BLK || r < 0 || (qbits != 8 && qbits != 4))
+        return -1;
+    double* g = (double*)malloc(sizeof(double) * F);
+    double* u = (double*)malloc(sizeof(double) * F);
+    double* h = (double*)malloc(sizeof(double) * F);
+    double* av = (double*)malloc(sizeof(double) * (r > 0 ? r : 1));
+    if (!g || !u || !h || !av) {
+        free(g); free(u); free(h); free(av);
+        return -1;
+    }
+    for (int64_t t = 0; t < T; t++) {
+        const double* xt = x + t * D;
+        lora_projection(F, D, r, qbits, gate_q, gate_s, gate_A, gate_B, scale, xt, av, g);
+        lora_projection(F, D, r, qbits, up_q, up_s, up_A, up_B, scale, xt, av, u);
+        for (int n = 0; n < F; n++) h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];
+        lora_projection(D, F, r, qbits, down_q, down_s, down_A, down_B, scale, h, av, y + t * D);
+    }
+    free(g); free(u); free(h); free(av);
+    return 0;
+}
+
+/* ------------------------------------------------------- prerouter head */
+
+/*
+ * Prerouter head (xyznot.com "The Other Half of the Memory Wall", method
+ * section "prerouter head architecture"; glossary "prerouter" and
+ * "prediction-as-routing"). The head held by layer N runs at token t and
+ * predicts the routing of layer N+1 at token t+1. Its input joins the hidden
+ * state with two k-hot routing vectors, of the current and of the previous
+ * token:
+ *   f = [ x (D) ; hot(cur) (E) ; hot(prev) (E) ]      (D + 2E values)
+ *   hot(S)[e] = 1 if e is among the ids S (negative ids: absent), else 0
+ * and the head is
+ *   z      = fc1 f + b1                               (fc1 [H][D+2E], b1 [H])
+ *   a      = gelu(z) = z/2 * (1 + erf(z / sqrt(2)))   (the erf form)
+ *   logits = fc2 a + L f + bias                       (fc2 [E][H], L [E][D+2E], bias [E])
+ * L being the linear residual path warm-started from the next layer's router.
+ * The prediction is consumed as the routing itself, so it goes through the
+ * router's own last steps (softmax_topk above): probs, the k most probable
+ * experts and their weights. b1 and bias may be NULL. Returns 0, -1 on bad
+ * arguments, -2 for an id >= E.
+ */
+int oracle_prerouter(int T, int D, int E, int H, int k, int norm_topk, const double* x,
+                     const int32_t* cur, const int32_t* prev, const double* fc1, const double* b1,
+                     const double* fc2, const double* L, const double* bias, double* logits,
+                     double* probs, float* probs32, int32_t* idx, double* w) {
+    if (T < 0 || D < 1 || E < 1 || H < 1 || k < 1 || k > E) return -1;
+    for (int64_t i = 0; i < (int64_t)T * k; i++)
+        if (cur[i] >= E || prev[i] >= E) return -2;
+    const int64_t nf = (int64_t)D + 2 * (int64_t)E;
+    double* f = (double*)malloc(sizeof(double) * nf);
+    double* a = (double*)malloc(sizeof(double) * H);
+    int* order = (int*)malloc(sizeof(int) * E);
+    if (!f || !a || !order) {
+        free(f); free(a); free(order);
+        return -1;
+    }
+    for (int64_t t = 0; t < T; t++) {
+        for (int64_t i = 0; i < D; i++) f[i] = x[t * D + i];
+        for (int64_t i = D; i < nf; i++) f[i] = 0.0;
+        for (int r = 0; r < k; r++) {
+            if (cur[t * k + r] >= 0) f[D + cur[t * k + r]] = 1.0;
+            if (prev[t * k + r] >= 0) f[D + E + prev[t * k + r]] = 1.0;
+        }
+        for (int j = 0; j < H; j++) {
+            double z = b1 ? b1[j] : 0.0;
+            for (int64_t i = 0; i < nf; i++) z += fc1[j * nf + i] * f[i];
+            a[j] = 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+        }
+        double* lt = logits + t * E;
+        for (int e = 0; e < E; e++) {
+            double head = 0.0;
+            for (int j = 0; j < H; j++) head += fc2[(int64_t)e * H + j] * a[j];
+            double lin = 0.0;
+            for (int64_t i = 0; i < nf; i++) lin += L[e * nf + i] * f[i];
+            lt[e] = head + lin + (bias ? bias[e] : 0.0);
+        }
+        softmax_topk(E, k, norm_topk, lt, probs + t * E, probs32 + t * E, order, idx + t * k,
+                     w + t * k);
+    }
+    free(f); free(a); free(order);
+    return 0;
 }
 
 /* ---------------------------------------------------- prefill permutation */

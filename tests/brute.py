@@ -105,3 +105,58 @@ def substitute_bruteforce(p32, idx, w, resident, threshold):
             flag[t][r] = 2
             mass[t] += w[t][r]
     return idx2, flag, mass
+
+
+def merged_dense_shared_lora(se: dict, x: np.ndarray) -> np.ndarray:
+    """Shared expert with its adapter computed the other way round from the
+    oracle: each projection's adapter is first merged, in fp64, into the
+    dequantised weight (W' = dq(W) + scale * B A, a dense matrix), and the
+    SwiGLU MLP then runs on the merged matrices with NumPy products. Merging is
+    exact in fp64 (no re-quantisation), so it equals the unmerged form up to
+    rounding: the distributive law behind the xyznot.com Edge0 page's parallel
+    delta y = W(x) + (alpha/r) B A x."""
+    qb = int(se["qbits"])
+
+    def merged(p):
+        W_ = dequant(to_np(se[p + "_q"]), to_np(se[p + "_s"]), qb)
+        if se.get(p + "_A") is None:
+            return W_
+        return W_ + float(se["scale"]) * (to_np(se[p + "_B"]) @ to_np(se[p + "_A"]))
+
+    G, U, Dn = merged("gate"), merged("up"), merged("down")
+    x = np.asarray(x, np.float64)
+    g = x @ G.T
+    u = x @ U.T
+    h = g / (1.0 + np.exp(-g)) * u
+    return h @ Dn.T
+
+
+def khot_features(x: np.ndarray, cur: np.ndarray, prev: np.ndarray, E: int) -> np.ndarray:
+    """[x ; hot(cur) ; hot(prev)] per token, negative ids absent."""
+    T, D = x.shape
+    f = np.zeros((T, D + 2 * E))
+    f[:, :D] = x
+    for t in range(T):
+        for e in cur[t]:
+            if e >= 0:
+                f[t, D + e] = 1.0
+        for e in prev[t]:
+            if e >= 0:
+                f[t, D + E + e] = 1.0
+    return f
+
+
+def prerouter_dense(head: dict, x, cur, prev) -> np.ndarray:
+    """Prerouter logits with whole-matrix NumPy products and SciPy's erf."""
+    from scipy.special import erf
+    fc1, fc2, L = to_np(head["fc1"]), to_np(head["fc2"]), to_np(head["L"])
+    E = fc2.shape[0]
+    f = khot_features(np.asarray(x, np.float64), np.asarray(cur), np.asarray(prev), E)
+    z = f @ fc1.T
+    if head.get("b1") is not None:
+        z = z + to_np(head["b1"])
+    a = 0.5 * z * (1.0 + erf(z / np.sqrt(2.0)))
+    logits = a @ fc2.T + f @ L.T
+    if head.get("bias") is not None:
+        logits = logits + to_np(head["bias"])
+    return logits

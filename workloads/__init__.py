@@ -42,7 +42,9 @@ import torch
 
 __all__ = [
     "LayerConfig", "CONFIGS", "seed_for", "quantize_sym_blk32", "pack_int4",
-    "make_layer", "make_tokens", "make_resident_mask", "routed_bytes_per_expert",
+    "make_layer", "make_router", "make_tokens", "make_resident_mask", "routed_bytes_per_expert",
+    "SharedConfig", "SHARED_CONFIGS", "make_shared_expert", "make_shared_tokens",
+    "make_prerouter", "make_routing_history",
 ]
 
 BLOCK = 32
@@ -160,6 +162,19 @@ def _quantized_matrix(cfg: LayerConfig, layer: int, name: str, rows: int, cols: 
     return codes, scales
 
 
+def make_router(cfg: LayerConfig, layer: int = 0, device="cpu"):
+    """Router weights of one layer: ``Wr`` [E][D] (router_dtype) and ``bias`` [E]
+    fp32 (the Zipf log-popularity over a seeded expert order) or None."""
+    g = _gen(device, seed_for(cfg.seed, cfg.cfg_id, layer, "router"))
+    Wr = (torch.randn((cfg.E, cfg.D), generator=g, device=device) * cfg.router_sigma).to(cfg.router_dtype)
+    bias = None
+    if cfg.zipf is not None:
+        gp = _gen("cpu", seed_for(cfg.seed, cfg.cfg_id, layer, "bias_perm"))
+        rank = torch.randperm(cfg.E, generator=gp).to(torch.float64) + 1.0
+        bias = (-cfg.zipf * torch.log(rank)).to(torch.float32).to(device)
+    return Wr.contiguous(), bias
+
+
 def make_layer(cfg: LayerConfig, layer: int = 0, device="cpu", chunk: int = 16) -> dict:
     """All weights of one layer.
 
@@ -168,17 +183,11 @@ def make_layer(cfg: LayerConfig, layer: int = 0, device="cpu", chunk: int = 16) 
     ``down_q`` [E][D][F or F/2], ``down_s`` [E][D][F/32].
     """
     E, D, F = cfg.E, cfg.D, cfg.F
-    g = _gen(device, seed_for(cfg.seed, cfg.cfg_id, layer, "router"))
-    Wr = (torch.randn((E, D), generator=g, device=device) * cfg.router_sigma).to(cfg.router_dtype)
-    bias = None
-    if cfg.zipf is not None:
-        gp = _gen("cpu", seed_for(cfg.seed, cfg.cfg_id, layer, "bias_perm"))
-        rank = torch.randperm(E, generator=gp).to(torch.float64) + 1.0
-        bias = (-cfg.zipf * torch.log(rank)).to(torch.float32).to(device)
+    Wr, bias = make_router(cfg, layer, device)
     gate_q, gate_s = _quantized_matrix(cfg, layer, "gate", F, D, device, chunk)
     up_q, up_s = _quantized_matrix(cfg, layer, "up", F, D, device, chunk)
     down_q, down_s = _quantized_matrix(cfg, layer, "down", D, F, device, chunk)
-    return dict(Wr=Wr.contiguous(), bias=bias, gate_q=gate_q, gate_s=gate_s,
+    return dict(Wr=Wr, bias=bias, gate_q=gate_q, gate_s=gate_s,
                 up_q=up_q, up_s=up_s, down_q=down_q, down_s=down_s)
 
 
@@ -204,3 +213,112 @@ def routed_bytes_per_expert(cfg: LayerConfig) -> int:
     n = 3 * cfg.F * cfg.D
     return int(n * code_bytes + (n // BLOCK) * sb)
 
+
+
+# ------------------------------------------------ shared expert with its LoRA
+
+@dataclasses.dataclass(frozen=True)
+class SharedConfig:
+    """Shape of a MoE block's shared expert and of its recovery LoRA."""
+    name: str
+    D: int                 # d_model
+    F: int                 # the shared expert's d_ff
+    qbits: int             # base weights: 8 or 4
+    scale_dtype: torch.dtype
+    rank: int              # LoRA rank r (0 = no adapter)
+    alpha: float           # the adapter is scaled by alpha / r
+    lora_dtype: torch.dtype
+    x_dtype: torch.dtype
+    weight_sigma: float = 0.02
+    lora_a_sigma: float = 0.01
+    lora_b_sigma: float = 0.0125
+    cfg_id: int = 10
+    seed: int = 0
+
+
+# The shared expert of the 256-expert decode layer served as the Edge0 page
+# serves it: 4-bit base, rank-16 adapter with alpha = 32. sigma_A * sigma_B is
+# chosen so that the delta (alpha/r) B A has an RMS of about 1e-3, the size the
+# page gives for its adapters (below one 4-bit quantisation step).
+SHARED_CONFIGS: Dict[str, SharedConfig] = {
+    "decode": SharedConfig("shared expert D2048 F512 int4 + LoRA r16", D=2048, F=512, qbits=4,
+                           scale_dtype=torch.float16, rank=16, alpha=32.0,
+                           lora_dtype=torch.bfloat16, x_dtype=torch.bfloat16),
+}
+
+
+def _quantized_single(sc: SharedConfig, layer: int, name: str, rows: int, cols: int, device):
+    g = _gen(device, seed_for(sc.seed, sc.cfg_id, layer, name))
+    w = torch.randn((rows, cols), generator=g, device=device) * sc.weight_sigma
+    return quantize_sym_blk32(w, sc.qbits, sc.scale_dtype)
+
+
+def make_shared_expert(sc: SharedConfig, layer: int = 0, device="cpu") -> dict:
+    """A shared expert and its unmerged adapters.
+
+    Keys: ``gate_q``/``up_q`` [F][D or D/2], ``gate_s``/``up_s`` [F][D/32],
+    ``down_q`` [D][F or F/2], ``down_s`` [D][F/32]; ``gate_A``/``up_A`` [r][D],
+    ``down_A`` [r][F], ``gate_B``/``up_B`` [F][r], ``down_B`` [D][r] in
+    lora_dtype (None when r = 0); ``scale`` = alpha / r; ``qbits``.
+    """
+    D, F, r = sc.D, sc.F, sc.rank
+    out = dict(qbits=sc.qbits, scale=(sc.alpha / r) if r > 0 else 0.0)
+    out["gate_q"], out["gate_s"] = _quantized_single(sc, layer, "shared_gate", F, D, device)
+    out["up_q"], out["up_s"] = _quantized_single(sc, layer, "shared_up", F, D, device)
+    out["down_q"], out["down_s"] = _quantized_single(sc, layer, "shared_down", D, F, device)
+    for proj, n_in, n_out in (("gate", D, F), ("up", D, F), ("down", F, D)):
+        if r == 0:
+            out[proj + "_A"] = out[proj + "_B"] = None
+            continue
+        ga = _gen(device, seed_for(sc.seed, sc.cfg_id, layer, proj + "_lora_A"))
+        gb = _gen(device, seed_for(sc.seed, sc.cfg_id, layer, proj + "_lora_B"))
+        out[proj + "_A"] = (torch.randn((r, n_in), generator=ga, device=device) *
+                            sc.lora_a_sigma).to(sc.lora_dtype).contiguous()
+        out[proj + "_B"] = (torch.randn((n_out, r), generator=gb, device=device) *
+                            sc.lora_b_sigma).to(sc.lora_dtype).contiguous()
+    return out
+
+
+def make_shared_tokens(sc: SharedConfig, T: int, stream: int = 0, device="cpu") -> torch.Tensor:
+    """x ~ N(0, 1) of shape [T][D] in the config's activation dtype."""
+    g = _gen(device, seed_for(sc.seed, sc.cfg_id, "x", stream, T))
+    return torch.randn((T, sc.D), generator=g, device=device).to(sc.x_dtype).contiguous()
+
+
+# ------------------------------------------------------------ prerouter head
+
+def make_prerouter(cfg: LayerConfig, layer: int = 0, H: int = 512, device="cpu",
+                   sigma: float = 0.02, hot_sigma: float = 0.1) -> dict:
+    """Prerouter head held by layer ``layer`` that predicts layer ``layer + 1``'s
+    routing. Input width D + 2E (hidden state, k-hot routing of the current and
+    of the previous token).
+
+    Keys: ``fc1`` [H][D+2E] and ``fc2`` [E][H] ~ N(0, sigma) in the router dtype,
+    ``b1`` [H] fp32 ~ N(0, sigma); ``L`` [E][D+2E]: its first D columns are the
+    next layer's router weights (the warm start) and its 2E routing columns
+    ~ N(0, hot_sigma); ``bias`` = the next layer's router bias.
+    """
+    E, D = cfg.E, cfg.D
+    nf = D + 2 * E
+    Wr_next, bias_next = make_router(cfg, layer + 1, device)
+    g = _gen(device, seed_for(cfg.seed, cfg.cfg_id, layer, "prerouter"))
+    fc1 = (torch.randn((H, nf), generator=g, device=device) * sigma).to(cfg.router_dtype)
+    b1 = (torch.randn((H,), generator=g, device=device) * sigma).to(torch.float32)
+    fc2 = (torch.randn((E, H), generator=g, device=device) * sigma).to(cfg.router_dtype)
+    hot = (torch.randn((E, 2 * E), generator=g, device=device) * hot_sigma).to(cfg.router_dtype)
+    L = torch.cat([Wr_next.to(cfg.router_dtype), hot], dim=1)
+    return dict(fc1=fc1.contiguous(), b1=b1.contiguous(), fc2=fc2.contiguous(),
+                L=L.contiguous(), bias=bias_next)
+
+
+def make_routing_history(cfg: LayerConfig, T: int, stream: int = 0, device="cpu",
+                         absent_prev: bool = False):
+    """Seeded k-expert id lists (distinct ids per token) standing in for the
+    current and previous tokens' routing: ``cur``, ``prev`` int32 [T][k]; with
+    ``absent_prev`` the previous token is missing (ids -1)."""
+    g = _gen("cpu", seed_for(cfg.seed, cfg.cfg_id, "history", stream, T))
+    cur = torch.stack([torch.randperm(cfg.E, generator=g)[: cfg.k] for _ in range(T)])
+    prev = torch.stack([torch.randperm(cfg.E, generator=g)[: cfg.k] for _ in range(T)])
+    if absent_prev:
+        prev = torch.full_like(prev, -1)
+    return cur.to(torch.int32).to(device).contiguous(), prev.to(torch.int32).to(device).contiguous()
