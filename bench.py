@@ -14,7 +14,8 @@ The same run also measures, under "workloads", the other configurations on
 the same resident weights: the batched decode sweep (T = 1..64), residency
 substitution with int4 experts (T = 1, 16) and prefill (T = 2048, 16384), each
 with its roofline, the CPU oracle's rate on a bounded sample, and the clocks
-seen while it ran.
+seen while it ran; then the shared expert with its unmerged LoRA and the
+prerouter head (T = 1, 16).
 
 Prints ONE JSON line (rank 0). With --impl reference the CPU oracle is timed on
 a bounded sample of the headline workload instead.
@@ -691,6 +692,116 @@ def run_prefill(args, dev, stack, T):
             "clocks": clk.summary()}
 
 
+def _tensor_bytes(d: dict) -> int:
+    return sum(v.numel() * v.element_size() for v in d.values() if isinstance(v, torch.Tensor))
+
+
+def _time_calls(args, dev, calls, n_copies):
+    """Captures one pass of `calls` (one call per copy) in a CUDA graph and
+    returns the CUDA-event milliseconds of one call."""
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        calls()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        calls()
+    steps = max(20, args.steps // 20)
+    return time_graph(g, stream, steps, max(3, args.warmup)) / steps / n_copies
+
+
+def run_edge0(args, dev):
+    """The shared expert with its unmerged LoRA and the prerouter head (the
+    xyznot.com Edge0 page, method section) at decode size. Each step calls
+    every copy once: 80 shared experts (int4 base + rank-16 adapters, 1.9 MB
+    each) and 40 heads (input 2048 + 2*256, hidden 512, bf16, 4.2 MB each), so
+    more bytes than L2 pass per step."""
+    import numpy as np
+    import moe_routed_expert_route_gb300 as M
+    import oracle
+    hbm, _, _, kind = peaks()
+    nth = os.cpu_count() or 1
+    out = {}
+
+    sc = W.SHARED_CONFIGS["decode"]
+    n_sh = 80
+    shared = [W.make_shared_expert(sc, l, dev) for l in range(n_sh)]
+    objs = [M.Shared.from_dict(s) for s in shared]
+    sh_bytes = _tensor_bytes(shared[0])
+    host0 = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in shared[0].items()}
+    for T in (1, 16):
+        x = W.make_shared_tokens(sc, T, 0, dev)
+        y = torch.empty(T, sc.D, device=dev)
+        ws = M.workspace(M.MOE_OP_SHARED, T, 1, 1, sc.D, sc.F, dev)
+
+        def calls():
+            for o in objs:
+                M.moe_shared_lora(o, x, y, False, ws)
+        with ClockSampler(dev.index or 0) as clk:
+            ms = _time_calls(args, dev, calls, n_sh)
+        assert M.moe_check_status(ws) == 0
+        gbs = sh_bytes / (ms * 1e-3) / 1e9
+        xs = x.cpu()
+        t0 = time.perf_counter()
+        nrep = 3
+        for _ in range(nrep):
+            oracle.shared_lora(host0, xs)
+        el = (time.perf_counter() - t0) / nrep
+        out[f"shared_lora_T{T}"] = {
+            "workload": f"shared expert D=2048 F=512 int4 blk32 fp16 scales + unmerged LoRA r=16 (bf16), "
+                        f"T={T}, 80 copies", "T": T, "unit": "tokens/s",
+            "tokens_per_s": round(T / (ms * 1e-3), 1), "us_per_call": round(ms * 1e3, 3),
+            "bytes_per_call": sh_bytes, "weight_gbs": round(gbs, 1),
+            "roofline": roofline("hbm", gbs, hbm, "GB/s", "lora_a + shared_gateup + lora_a + shared_down",
+                                 {"peak_kind": kind}),
+            "cpu_baseline": {"value": round(T / el, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{nrep} calls of one copy on T={T} tokens, {el * nrep:.2f} s"},
+            "clocks": clk.summary()}
+        del ws
+    del shared, objs
+    torch.cuda.empty_cache()
+
+    cfg = W.CONFIGS[1]
+    n_h = 40
+    heads = [W.make_prerouter(cfg, l, H=512, device=dev) for l in range(n_h)]
+    hobjs = [M.Prerouter.from_dict(h, cfg.k) for h in heads]
+    h_bytes = _tensor_bytes(heads[0])
+    hhost = {k: v.cpu() for k, v in heads[0].items()}
+    for T in (1, 16):
+        x = W.make_tokens(cfg, T, 7, dev)
+        cur, prev = W.make_routing_history(cfg, T, stream=7, device=dev)
+        idx = torch.empty(T, cfg.k, dtype=torch.int32, device=dev)
+        w = torch.empty(T, cfg.k, device=dev)
+        ws = M.workspace(M.MOE_OP_PREROUTE, T, cfg.k, cfg.E, cfg.D, 512, dev)
+
+        def calls():
+            for o in hobjs:
+                M.moe_preroute(o, x, cur, prev, idx, w, None, ws)
+        with ClockSampler(dev.index or 0) as clk:
+            ms = _time_calls(args, dev, calls, n_h)
+        assert M.moe_check_status(ws) == 0
+        gbs = h_bytes / (ms * 1e-3) / 1e9
+        xs, cs, ps = x.cpu(), cur.cpu(), prev.cpu()
+        t0 = time.perf_counter()
+        nrep = 3
+        for _ in range(nrep):
+            oracle.prerouter(hhost, xs, cs, ps, cfg.k)
+        el = (time.perf_counter() - t0) / nrep
+        out[f"prerouter_T{T}"] = {
+            "workload": f"prerouter head D=2048 E=256 k=8 H=512 (input 2560, bf16), T={T}, 40 heads",
+            "T": T, "unit": "tokens/s", "tokens_per_s": round(T / (ms * 1e-3), 1),
+            "us_per_call": round(ms * 1e3, 3), "bytes_per_call": h_bytes, "weight_gbs": round(gbs, 1),
+            "roofline": roofline("hbm", gbs, hbm, "GB/s", "preroute_hidden + preroute_logits + topk",
+                                 {"peak_kind": kind}),
+            "cpu_baseline": {"value": round(T / el, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{nrep} calls of one head on T={T} tokens, {el * nrep:.2f} s"},
+            "clocks": clk.summary()}
+        del ws
+    del heads, hobjs
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -713,6 +824,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         extra["replay"], extra["substitution"] = run_substitution(args, dev)
+        try:
+            extra["edge0"] = run_edge0(args, dev)
+        except Exception as e:  # reported, never at the cost of the line above
+            extra["edge0"] = {"error": f"{type(e).__name__}: {e}"[:300]}
         line["workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)

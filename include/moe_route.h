@@ -107,7 +107,9 @@ enum {
     MOE_OP_DECODE = 1,
     MOE_OP_LAYER = 2,         /* also moe_layer_stack (with T = 1) */
     MOE_OP_PREFILL = 3,
-    MOE_OP_LAYER_RESIDENT = 4 /* moe_layer_resident */
+    MOE_OP_LAYER_RESIDENT = 4, /* moe_layer_resident */
+    MOE_OP_SHARED = 5,         /* moe_shared_lora: D, F = the shared expert's d_ff; k, E unused (pass 1) */
+    MOE_OP_PREROUTE = 6        /* moe_preroute: D, E, k, F = the head's hidden width H */
 };
 
 /*
@@ -310,6 +312,77 @@ moe_status_t moe_prefill(const moe_router_t* router, const moe_experts_t* expert
                          moe_dtype_t x_dtype, int T, float* y, int32_t* idx, float* w,
                          int32_t* counts, int32_t* perm, void* workspace, size_t ws_bytes,
                          void* stream);
+
+/* Shared expert of a MoE block with its recovery LoRA kept unmerged. Base
+ * weights as one expert of moe_experts_t (no E dimension):
+ *   gate_q, up_q [F][D] (int4: [F][D/2] bytes), gate_s, up_s [F][D/32]
+ *   down_q       [D][F] (int4: [D][F/2] bytes), down_s       [D][F/32]
+ * Adapters in lora_dtype (MOE_BF16 or MOE_F32), rank r (0 = none, A/B unused):
+ *   gate_A, up_A [r][D], down_A [r][F]; gate_B, up_B [F][r], down_B [D][r]
+ * lora_scale is alpha / r. */
+typedef struct {
+    int D, F, r;
+    moe_qfmt_t q;
+    moe_dtype_t s_dtype;
+    const void *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
+    moe_dtype_t lora_dtype;
+    const void *gate_A, *gate_B, *up_A, *up_B, *down_A, *down_B;
+    float lora_scale;
+} moe_shared_t;
+
+/*
+ * Shared expert with an unmerged LoRA for T tokens (xyznot.com "The Other Half
+ * of the Memory Wall", method section "unmerged adapter execution": the
+ * quantised base is kept and the low-rank delta runs in parallel,
+ * P(v) = dq(W) v + (alpha/r) B (A v), on the shared expert's projections):
+ *   g = Gate(x_t), u = Up(x_t), h = silu(g) * u, o = Down(h)
+ *   y[t] = o            (accumulate = 0)
+ *   y[t] = y[t] + o     (accumulate = 1: adds the shared expert to a routed
+ *                        output computed earlier on the same stream)
+ *   x   [T][D] in x_dtype (MOE_F32 or MOE_BF16);  y [T][D] fp32
+ * D and F multiples of 32, 0 <= r <= 64. Workspace: moe_workspace_bytes(
+ * MOE_OP_SHARED, T, 1, 1, D, F). Four launches (two when r = 0).
+ */
+moe_status_t moe_shared_lora(const moe_shared_t* shared, const void* x, moe_dtype_t x_dtype, int T,
+                             float* y, int accumulate, void* workspace, size_t ws_bytes, void* stream);
+
+/* Prerouter head held by layer N that predicts layer N+1's routing. w_dtype
+ * (MOE_BF16 or MOE_F32) is the type of fc1, fc2 and L:
+ *   fc1 [H][D+2E], b1 [H] fp32 or NULL, fc2 [E][H], L [E][D+2E], bias [E] fp32 or NULL
+ * E is the number of experts of layer N+1, k its routed experts per token;
+ * norm_topk as in moe_router_t. */
+typedef struct {
+    int D, E, H, k;
+    moe_dtype_t w_dtype;
+    const void* fc1;
+    const float* b1;
+    const void* fc2;
+    const void* L;
+    const float* bias;
+    int norm_topk;
+} moe_prerouter_t;
+
+/*
+ * Prerouter for T tokens (xyznot.com "The Other Half of the Memory Wall",
+ * method section "prerouter head architecture", glossary "prediction-as-
+ * routing"). Input of the head: f = [x ; hot(cur) ; hot(prev)], hot(S)[e] = 1
+ * when e is one of the ids S (a repeated id counts once, a negative id is an
+ * absent entry, e.g. no previous token):
+ *   logits = fc2 gelu(fc1 f + b1) + L f + bias,  gelu(z) = z/2 (1 + erf(z/sqrt 2))
+ * then the router's fp32 softmax and top-k. The prediction is meant to be used
+ * as the next layer's routing: idx/w go to moe_decode as they are.
+ *   x          [T][D] in x_dtype (MOE_F32 or MOE_BF16)
+ *   cur, prev  [T][k] int32: the current and previous tokens' routing ids
+ *   idx, w     [T][k] out: predicted experts (most probable first, equal fp32
+ *              probabilities by lower id) and their weights
+ *   probs      [T][E] fp32 out, or NULL
+ * D and H multiples of 32; E a multiple of 4, at most 1024; k <= 32. An id
+ * >= E in cur/prev is recorded as MOE_ERR_BAD_INDEX (moe_check_status) and
+ * skipped. Workspace: moe_workspace_bytes(MOE_OP_PREROUTE, T, k, E, D, H).
+ */
+moe_status_t moe_preroute(const moe_prerouter_t* head, const void* x, moe_dtype_t x_dtype, int T,
+                          const int32_t* cur, const int32_t* prev, int32_t* idx, float* w, float* probs,
+                          void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * moe_layer for ONE token (T = 1) without a workspace: no counterpart in the

@@ -26,10 +26,11 @@ MOE_ERR_BAD_INDEX, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_WORKSPACE = 4, 5, 6
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_Q_INT8_SYM_B32, MOE_Q_INT4_SYM_B32 = 0, 1
 MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_LAYER, MOE_OP_PREFILL, MOE_OP_LAYER_RESIDENT = 0, 1, 2, 3, 4
+MOE_OP_SHARED, MOE_OP_PREROUTE = 5, 6
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_substitute", "moe_decode", "moe_layer",
             "moe_layer_resident", "moe_layer_stack", "moe_layer_stack_resident", "moe_prefill", "moe_layer_noalloc",
-            "moe_replay",
+            "moe_replay", "moe_shared_lora", "moe_preroute",
             "moe_check_status", "moe_set_wait_limit", "moe_status_string")
 
 
@@ -61,6 +62,26 @@ class _Experts(ctypes.Structure):
                 ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p)]
 
 
+class _Shared(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int), ("F", ctypes.c_int), ("r", ctypes.c_int),
+                ("q", ctypes.c_int), ("s_dtype", ctypes.c_int),
+                ("gate_q", ctypes.c_void_p), ("gate_s", ctypes.c_void_p),
+                ("up_q", ctypes.c_void_p), ("up_s", ctypes.c_void_p),
+                ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p),
+                ("lora_dtype", ctypes.c_int),
+                ("gate_A", ctypes.c_void_p), ("gate_B", ctypes.c_void_p),
+                ("up_A", ctypes.c_void_p), ("up_B", ctypes.c_void_p),
+                ("down_A", ctypes.c_void_p), ("down_B", ctypes.c_void_p),
+                ("lora_scale", ctypes.c_float)]
+
+
+class _Prerouter(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int), ("E", ctypes.c_int), ("H", ctypes.c_int), ("k", ctypes.c_int),
+                ("w_dtype", ctypes.c_int), ("fc1", ctypes.c_void_p), ("b1", ctypes.c_void_p),
+                ("fc2", ctypes.c_void_p), ("L", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("norm_topk", ctypes.c_int)]
+
+
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(f"{path} is missing: build it with moe_routed_expert_route_gb300/build.py "
@@ -79,13 +100,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_stack.argtypes = [I, P, P, P, I, I, P, P, P, P, P, S, P]
     lib.moe_replay.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, P]
     lib.moe_layer_stack_resident.argtypes = [I, P, P, P, I, I, P, ctypes.c_float, P, P, P, P, P, P, P, P, S, P]
+    lib.moe_shared_lora.argtypes = [P, P, I, I, P, I, P, S, P]
+    lib.moe_preroute.argtypes = [P, P, I, I, P, P, P, P, P, P, S, P]
     lib.moe_check_status.argtypes = [P, P]
     lib.moe_set_wait_limit.argtypes = [P, ctypes.c_ulonglong, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for f in ("moe_route", "moe_substitute", "moe_decode", "moe_layer", "moe_prefill",
               "moe_layer_noalloc", "moe_layer_resident", "moe_layer_stack", "moe_check_status",
-              "moe_set_wait_limit"):
+              "moe_set_wait_limit", "moe_shared_lora", "moe_preroute"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -195,6 +218,104 @@ class Experts:
                         self.up_s.data_ptr(), self.down_q.data_ptr(), self.down_s.data_ptr())
 
 
+@dataclass
+class Shared:
+    """A shared expert ([F][D] gate/up, [D][F] down, quantised as the routed
+    experts, no E dimension) and its unmerged adapters: A [r][in], B [out][r]
+    in bf16/fp32 (None for r = 0), scale = alpha / r."""
+    gate_q: torch.Tensor
+    gate_s: torch.Tensor
+    up_q: torch.Tensor
+    up_s: torch.Tensor
+    down_q: torch.Tensor
+    down_s: torch.Tensor
+    qbits: int = 8
+    gate_A: Optional[torch.Tensor] = None
+    gate_B: Optional[torch.Tensor] = None
+    up_A: Optional[torch.Tensor] = None
+    up_B: Optional[torch.Tensor] = None
+    down_A: Optional[torch.Tensor] = None
+    down_B: Optional[torch.Tensor] = None
+    scale: float = 0.0
+
+    @classmethod
+    def from_dict(cls, se: dict) -> "Shared":
+        return cls(**{k: se[k] for k in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
+                                         "qbits", "gate_A", "gate_B", "up_A", "up_B", "down_A",
+                                         "down_B", "scale")})
+
+    @property
+    def D(self):
+        return self.down_q.shape[0]
+
+    @property
+    def F(self):
+        return self.gate_q.shape[0]
+
+    def struct(self) -> _Shared:
+        F, D = self.F, self.D
+        cb = 1 if self.qbits == 8 else 2
+        qd = (torch.int8, torch.uint8)
+        sd = (torch.float32, torch.float16)
+        _dev(self.gate_q, "gate_q", qd, (F, D // cb))
+        _dev(self.up_q, "up_q", qd, (F, D // cb))
+        _dev(self.down_q, "down_q", qd, (D, F // cb))
+        _dev(self.gate_s, "gate_s", sd, (F, D // 32))
+        _dev(self.up_s, "up_s", self.gate_s.dtype, (F, D // 32))
+        _dev(self.down_s, "down_s", self.gate_s.dtype, (D, F // 32))
+        r = 0 if self.gate_A is None else self.gate_A.shape[0]
+        lt = (torch.float32, torch.bfloat16)
+        if r > 0:
+            _dev(self.gate_A, "gate_A", lt, (r, D))
+            _dev(self.up_A, "up_A", self.gate_A.dtype, (r, D))
+            _dev(self.down_A, "down_A", self.gate_A.dtype, (r, F))
+            _dev(self.gate_B, "gate_B", self.gate_A.dtype, (F, r))
+            _dev(self.up_B, "up_B", self.gate_A.dtype, (F, r))
+            _dev(self.down_B, "down_B", self.gate_A.dtype, (D, r))
+        ld = MOE_BF16 if r > 0 and self.gate_A.dtype == torch.bfloat16 else MOE_F32
+        return _Shared(D, F, r, MOE_Q_INT8_SYM_B32 if self.qbits == 8 else MOE_Q_INT4_SYM_B32,
+                       MOE_F32 if self.gate_s.dtype == torch.float32 else MOE_F16,
+                       self.gate_q.data_ptr(), self.gate_s.data_ptr(), self.up_q.data_ptr(),
+                       self.up_s.data_ptr(), self.down_q.data_ptr(), self.down_s.data_ptr(), ld,
+                       *[(None if t is None or r == 0 else t.data_ptr())
+                         for t in (self.gate_A, self.gate_B, self.up_A, self.up_B, self.down_A,
+                                   self.down_B)],
+                       float(self.scale) if r > 0 else 0.0)
+
+
+@dataclass
+class Prerouter:
+    """Prerouter head: fc1 [H][D+2E], b1 [H] fp32 or None, fc2 [E][H],
+    L [E][D+2E] (fc1/fc2/L all fp32 or all bf16), bias [E] fp32 or None."""
+    fc1: torch.Tensor
+    b1: Optional[torch.Tensor]
+    fc2: torch.Tensor
+    L: torch.Tensor
+    bias: Optional[torch.Tensor]
+    k: int
+    norm_topk: bool = True
+
+    @classmethod
+    def from_dict(cls, head: dict, k: int, norm_topk: bool = True) -> "Prerouter":
+        return cls(head["fc1"], head.get("b1"), head["fc2"], head["L"], head.get("bias"), k, norm_topk)
+
+    def struct(self) -> _Prerouter:
+        E, H = self.fc2.shape
+        D = self.fc1.shape[1] - 2 * E
+        _dev(self.fc1, "fc1", (torch.float32, torch.bfloat16), (H, D + 2 * E))
+        _dev(self.fc2, "fc2", self.fc1.dtype, (E, H))
+        _dev(self.L, "L", self.fc1.dtype, (E, D + 2 * E))
+        if self.b1 is not None:
+            _dev(self.b1, "b1", torch.float32, (H,))
+        if self.bias is not None:
+            _dev(self.bias, "bias", torch.float32, (E,))
+        return _Prerouter(D, E, H, self.k, MOE_F32 if self.fc1.dtype == torch.float32 else MOE_BF16,
+                          self.fc1.data_ptr(), None if self.b1 is None else self.b1.data_ptr(),
+                          self.fc2.data_ptr(), self.L.data_ptr(),
+                          None if self.bias is None else self.bias.data_ptr(),
+                          1 if self.norm_topk else 0)
+
+
 def moe_workspace_bytes(op: int, T: int, k: int, E: int, D: int, F: int) -> int:
     return int(_lib.moe_workspace_bytes(op, T, k, E, D, F))
 
@@ -220,6 +341,34 @@ def moe_route(router: Router, x: torch.Tensor, idx: torch.Tensor, w: torch.Tenso
         _dev(probs, "probs", torch.float32, (T, r.E))
     _check("moe_route", _lib.moe_route(ctypes.byref(r), _ptr(x), _act_dtype(x), T, _ptr(idx),
                                        _ptr(w), _ptr(probs), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_shared_lora(shared: Shared, x: torch.Tensor, y: torch.Tensor, accumulate: bool,
+                    ws: torch.Tensor, stream=None):
+    s = shared.struct()
+    T = x.shape[0]
+    _dev(x, "x", (torch.float32, torch.bfloat16), (T, s.D))
+    _dev(y, "y", torch.float32, (T, s.D))
+    _check("moe_shared_lora", _lib.moe_shared_lora(ctypes.byref(s), _ptr(x), _act_dtype(x), T, _ptr(y),
+                                                   1 if accumulate else 0, _ptr(ws), ws.numel(),
+                                                   _stream(stream)))
+
+
+def moe_preroute(head: Prerouter, x: torch.Tensor, cur: torch.Tensor, prev: torch.Tensor,
+                 idx: torch.Tensor, w: torch.Tensor, probs: Optional[torch.Tensor], ws: torch.Tensor,
+                 stream=None):
+    h = head.struct()
+    T = x.shape[0]
+    _dev(x, "x", (torch.float32, torch.bfloat16), (T, h.D))
+    _dev(cur, "cur", torch.int32, (T, h.k))
+    _dev(prev, "prev", torch.int32, (T, h.k))
+    _dev(idx, "idx", torch.int32, (T, h.k))
+    _dev(w, "w", torch.float32, (T, h.k))
+    if probs is not None:
+        _dev(probs, "probs", torch.float32, (T, h.E))
+    _check("moe_preroute", _lib.moe_preroute(ctypes.byref(h), _ptr(x), _act_dtype(x), T, _ptr(cur),
+                                             _ptr(prev), _ptr(idx), _ptr(w), _ptr(probs), _ptr(ws),
+                                             ws.numel(), _stream(stream)))
 
 
 def moe_substitute(probs, idx_in, w_in, resident, threshold: float, idx_out, w_out, sub_flag,

@@ -479,6 +479,8 @@ size_t moe_workspace_bytes(int op, int T, int k, int E, int D, int F) {
     if (op != MOE_OP_ROUTE && (F < kBlk || F % kBlk)) return 0;
     if (op == MOE_OP_PREFILL) return prefill_shape_ok(E, D, F) ? prefill_layout(T, k, E, D, F).total : 0;
     if (op == MOE_OP_LAYER_RESIDENT) return layer_bytes(T, k, E, D, F) + sizeof(float) * (size_t)T * E;
+    if (op == MOE_OP_SHARED) return shared_ws_bytes(T, F);
+    if (op == MOE_OP_PREROUTE) return preroute_ws_bytes(T, E, F);
     if (op < MOE_OP_ROUTE || op > MOE_OP_LAYER) return 0;
     if (op == MOE_OP_ROUTE) return layout(op, T, k, E, D, F).total;
     // several tokens through the grouped products (see moe_decode / moe_layer)

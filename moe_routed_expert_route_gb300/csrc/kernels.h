@@ -241,6 +241,9 @@ bool fused_plan(int E, int D, int F, int k, int qbits, int s_bytes, int x_bytes,
 cudaError_t launch_fused(const FusedCommon& fc, const FusedLayer* layers, int qbits, bool s_f16, bool x_bf16,
                          int grid, size_t smem, cudaStream_t s);
 int device_sm_count();
+// workspace bytes of moe_shared_lora / moe_preroute (edge0.cu)
+size_t shared_ws_bytes(int T, int F);
+size_t preroute_ws_bytes(int T, int E, int H);
 cudaError_t launch_router(const RouterParams& p, bool w_bf16, bool x_bf16, cudaStream_t s, bool pdl);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_experts(const ExpertParams& p, cudaStream_t s);

@@ -128,3 +128,57 @@ def test_binding_requires_cuda_tensors():
     W = torch.zeros(8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         M.Router(W, None, 2).struct()
+
+
+def _shared(D=64, F=64, r=4, q=L.MOE_Q_INT8_SYM_B32, s=L.MOE_F16, ld=L.MOE_BF16, A=16, scale=2.0):
+    return L._Shared(D, F, r, q, s, 16, 16, 16, 16, 16, 16, ld, A, 16, 16, 16, 16, 16, scale)
+
+
+def test_shared_lora_rejects_bad_arguments_before_launch():
+    lib = L._lib
+    null = None
+    ws = M.moe_workspace_bytes(M.MOE_OP_SHARED, 4, 1, 1, 64, 64)
+    assert ws > M.moe_workspace_bytes(M.MOE_OP_SHARED, 1, 1, 1, 64, 64) > 0
+    assert M.moe_workspace_bytes(M.MOE_OP_SHARED, 1, 1, 1, 64, 48) == 0
+
+    def call(s, x=16, xd=L.MOE_BF16, T=4, y=16, w=256, n=ws):
+        return lib.moe_shared_lora(ctypes.byref(s), x, xd, T, y, 0, w, n, null)
+    assert call(_shared(F=48)) == M.MOE_ERR_INVALID_ARG          # F not a multiple of 32
+    assert call(_shared(r=65)) == M.MOE_ERR_INVALID_ARG          # rank above 64
+    assert call(_shared(r=-1)) == M.MOE_ERR_INVALID_ARG
+    assert call(_shared(A=18)) == M.MOE_ERR_INVALID_ARG          # misaligned adapter
+    assert call(_shared(A=None)) == M.MOE_ERR_INVALID_ARG        # missing adapter with r > 0
+    assert call(_shared(scale=float("inf"))) == M.MOE_ERR_INVALID_ARG
+    assert call(_shared(ld=L.MOE_F16)) == M.MOE_ERR_UNSUPPORTED  # fp16 adapters
+    assert call(_shared(s=L.MOE_BF16)) == M.MOE_ERR_UNSUPPORTED  # bf16 scales
+    assert call(_shared(), xd=L.MOE_F16) == M.MOE_ERR_UNSUPPORTED
+    assert call(_shared(), T=0) == M.MOE_ERR_INVALID_ARG
+    assert call(_shared(), y=null) == M.MOE_ERR_INVALID_ARG
+    assert call(_shared(), n=ws - 1) == M.MOE_ERR_WORKSPACE
+    assert call(_shared(), w=272) == M.MOE_ERR_WORKSPACE
+    assert lib.moe_shared_lora(null, 16, L.MOE_BF16, 1, 16, 0, 256, ws, null) == M.MOE_ERR_INVALID_ARG
+
+
+def test_preroute_rejects_bad_arguments_before_launch():
+    lib = L._lib
+    null = None
+    ws = M.moe_workspace_bytes(M.MOE_OP_PREROUTE, 2, 2, 8, 64, 32)
+    assert ws > 0
+
+    def head(D=64, E=8, H=32, k=2, wd=L.MOE_BF16, fc1=16, b1=None):
+        return L._Prerouter(D, E, H, k, wd, fc1, b1, 16, 16, None, 1)
+
+    def call(h, T=2, xd=L.MOE_BF16, cur=16, n=ws):
+        return lib.moe_preroute(ctypes.byref(h), 16, xd, T, cur, 16, 16, 16, null, 256, n, null)
+    assert call(head(E=6)) == M.MOE_ERR_INVALID_ARG      # E not a multiple of 4
+    assert call(head(E=2048)) == M.MOE_ERR_INVALID_ARG   # E above 1024
+    assert call(head(k=9)) == M.MOE_ERR_INVALID_ARG      # k > E
+    assert call(head(H=40)) == M.MOE_ERR_INVALID_ARG     # H not a multiple of 32
+    assert call(head(D=48)) == M.MOE_ERR_INVALID_ARG
+    assert call(head(fc1=24)) == M.MOE_ERR_INVALID_ARG   # misaligned weights
+    assert call(head(b1=18)) == M.MOE_ERR_INVALID_ARG    # misaligned bias
+    assert call(head(wd=L.MOE_F16)) == M.MOE_ERR_UNSUPPORTED
+    assert call(head(), xd=L.MOE_F16) == M.MOE_ERR_UNSUPPORTED
+    assert call(head(), cur=null) == M.MOE_ERR_INVALID_ARG
+    assert call(head(), T=0) == M.MOE_ERR_INVALID_ARG
+    assert call(head(), n=ws - 1) == M.MOE_ERR_WORKSPACE
