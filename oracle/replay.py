@@ -10,7 +10,10 @@ gate mass substituted for an expert accumulates, and at the threshold -- 0.5
 on the page -- the expert is admitted to the cache); frequency-based eviction.
 
 Plain Python loops over tokens, layers and slots, in that order, with sets
-and dictionaries for the cache. The open points are read as follows:
+and dictionaries for the cache. Besides the per-token totals it reports, per
+token and layer, the expert that serves each slot, how it was obtained and
+which experts were admitted, so that a cache that really moves experts can be
+checked decision by decision. The open points are read as follows:
 - the ranking is by fp32 probability, descending, lower id on equal values;
   weights are the k probabilities over their sum, in double, summed in rank
   order;
@@ -55,7 +58,8 @@ def replay(probs, k, policy, threshold=0.15, admit_mass=0.0, t_layer_us=0.0, t_f
     threshold = _f32(threshold)
     admit_mass = _f32(admit_mass)
     admit = admit_mass > 0 and math.isfinite(admit_mass)
-    out = dict(t_token_us=[], fetches=[], substituted=[], sub_mass=[], admissions=[])
+    out = dict(t_token_us=[], fetches=[], substituted=[], sub_mass=[], admissions=[],
+               used=[], flags=[], admitted=[])
 
     def insert(l, e, busy):
         candidates = [c for c in cache[l] if c not in busy]
@@ -68,6 +72,7 @@ def replay(probs, k, policy, threshold=0.15, admit_mass=0.0, t_layer_us=0.0, t_f
 
     for t in range(N):
         time_us, mass, n_fetch, n_sub, n_adm = 0.0, 0.0, 0, 0, 0
+        used_t, flags_t, admitted_t = [], [], []
         for l in range(L):
             p = [float(v) for v in probs[t][l]]
             order = sorted(range(E), key=lambda e: (-p[e], e))
@@ -80,6 +85,12 @@ def replay(probs, k, policy, threshold=0.15, admit_mass=0.0, t_layer_us=0.0, t_f
                 count[l][e] += 1
             busy = set(chosen)
             fetched_here = 0
+            # per slot: the expert that serves it, and how (0 hit; 1 fetched
+            # by the rule and cached; 2 substituted; 3 fetched for want of a
+            # stand-in and cached; 4 fetched, not cached: nothing evictable)
+            used = list(chosen)
+            flags = [0] * k
+            admitted = []
             for r, e in enumerate(chosen):
                 if e in cache[l]:
                     continue
@@ -96,9 +107,12 @@ def replay(probs, k, policy, threshold=0.15, admit_mass=0.0, t_layer_us=0.0, t_f
                         stand_in = max(pool, key=lambda c: (p[c], -c))
                 if stand_in is None:
                     fetched_here += 1
-                    insert(l, e, busy)
+                    entered = insert(l, e, busy)
+                    flags[r] = (1 if want else 3) if entered else 4
                     continue
                 busy.add(stand_in)
+                used[r] = stand_in
+                flags[r] = 2
                 n_sub += 1
                 mass += weights[r]
                 mass_of[l][e] += weights[r]
@@ -106,6 +120,10 @@ def replay(probs, k, policy, threshold=0.15, admit_mass=0.0, t_layer_us=0.0, t_f
                     if insert(l, e, busy):
                         n_adm += 1
                         mass_of[l][e] = 0.0
+                        admitted.append(e)
+            used_t.append(used)
+            flags_t.append(flags)
+            admitted_t.append(admitted)
             n_fetch += fetched_here
             time_us += t_layer_us + fetched_here * t_fetch_us
         out["t_token_us"].append(time_us)
@@ -113,6 +131,9 @@ def replay(probs, k, policy, threshold=0.15, admit_mass=0.0, t_layer_us=0.0, t_f
         out["substituted"].append(n_sub)
         out["sub_mass"].append(mass)
         out["admissions"].append(n_adm)
+        out["used"].append(used_t)
+        out["flags"].append(flags_t)
+        out["admitted"].append(admitted_t)
     out["resident"] = [[1 if e in cache[l] else 0 for e in range(E)] for l in range(L)]
     out["freq"] = count
     out["acc"] = mass_of

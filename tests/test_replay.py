@@ -44,7 +44,8 @@ def test_worked_example_golden():
     o = R.replay(probs, g["k"], R.THRESHOLD, g["threshold"], g["admit_mass"], g["t_layer_us"],
                  g["t_fetch_us"], resident=g["resident"])
     ex = g["expect"]
-    for n in ("t_token_us", "fetches", "substituted", "admissions", "resident", "freq", "acc"):
+    for n in ("t_token_us", "fetches", "substituted", "admissions", "resident", "freq", "acc",
+              "used", "flags", "admitted"):
         assert o[n] == ex[n], n
     for t, terms in enumerate(ex["sub_mass_terms"]):
         m = 0.0
@@ -52,6 +53,18 @@ def test_worked_example_golden():
             pa, pb = probs[t][0][a], probs[t][0][b]
             m += pa / (pb + pa)
         assert math.isclose(o["sub_mass"][t], m, rel_tol=0, abs_tol=1e-15)
+
+
+def test_oracle_miss_with_nothing_evictable_is_used_without_entering():
+    # E=4, k=3, experts 0 and 1 resident, both routed: the third choice e2
+    # (weight 0.2/0.9 >= 0.15) is fetched, but every resident is in use, so it
+    # serves its slot without entering the cache (flag 4)
+    p = [[[f32(0.4), f32(0.3), f32(0.2), f32(0.1)]]]
+    o = R.replay(p, 3, R.THRESHOLD, 0.15, 0.0, 1.0, 1.0, resident=[[1, 1, 0, 0]])
+    assert o["used"] == [[[0, 1, 2]]]
+    assert o["flags"] == [[[0, 0, 4]]]
+    assert o["fetches"] == [1]
+    assert o["resident"] == [[1, 1, 0, 0]]
 
 
 @pytest.mark.parametrize("seed", range(6))
