@@ -384,6 +384,102 @@ moe_status_t moe_preroute(const moe_prerouter_t* head, const void* x, moe_dtype_
                           const int32_t* cur, const int32_t* prev, int32_t* idx, float* w, float* probs,
                           void* workspace, size_t ws_bytes, void* stream);
 
+/* Expert cache of one layer. The experts live in host memory (all E, in the
+ * layout of moe_experts_t); a device pool (moe_experts_t with E = S + k) holds
+ * the S cached experts in slots 0..S-1, and slots S..S+k-1 are transient, for
+ * a fetched miss that cannot enter the cache. The state is host memory owned
+ * by the caller, and it is updated in place:
+ *   slot_of   [E] int32: slot of expert e, or -1 (not cached)
+ *   expert_of [S] int32: expert held by slot s (every slot holds one)
+ *   freq      [E] int32: times the layer's router chose e
+ *   acc       [E] double: routing weight substituted for e since its last admission */
+typedef struct {
+    int E, S, k;
+    int32_t* slot_of;
+    int32_t* expert_of;
+    int32_t* freq;
+    double* acc;
+} moe_cache_t;
+
+/* One token's decisions at one layer; every array is the caller's, [k] long.
+ *   expert, slot  the expert serving each routed slot (a resident stand-in for
+ *                 a substituted one) and the pool slot it is read from
+ *   w             the routing weight of each routed slot
+ *   flag          0 hit; 1 fetched by the rule and cached; 2 substituted;
+ *                 3 fetched for want of a stand-in and cached; 4 fetched
+ *                 into its transient slot (every cached expert in use)
+ *   fetch_*       the n_fetch synchronous fetches (expert, slot)
+ *   admit_*       the n_admit background admissions (expert, slot)
+ *   mass          routing weight served by stand-ins */
+typedef struct {
+    int32_t* expert;
+    int32_t* slot;
+    float* w;
+    uint8_t* flag;
+    int32_t *fetch_expert, *fetch_slot;
+    int32_t *admit_expert, *admit_slot;
+    int n_fetch, n_admit;
+    double mass;
+} moe_cache_step_t;
+
+/*
+ * Host code: the decisions of one token at one layer from the router's fp32
+ * probabilities `probs` [E] (host), with the rules of moe_replay (gist.science
+ * "Which expert misses are worth waiting for?", method section): top-k by
+ * probability (lower id on equal values), weights over their sum; every
+ * routed expert's frequency grows by one; in rank order a cached expert is a
+ * hit, a miss the policy keeps is fetched (entering the cache in the slot of
+ * the least frequent cached expert the token does not use, lower id on ties,
+ * or its transient slot S + r when there is none), any other miss is served by
+ * the cached expert of highest probability that is neither routed nor already
+ * a stand-in (fetched when there is none) and its weight accumulates for the
+ * missed expert, which is admitted (same eviction) once the accumulation
+ * reaches policy->admit_mass (0 or +inf: never). policy->t_layer_us and
+ * t_fetch_us are not used. The slot table must be consistent (checked).
+ */
+moe_status_t moe_cache_plan(moe_cache_t* cache, const float* probs, const moe_replay_policy_t* policy,
+                            moe_cache_step_t* step);
+
+/*
+ * Copies n experts from host memory into pool slots: expert experts[i] of
+ * `host` into slot slots[i] of `pool` (same D, F, formats), one
+ * cudaMemcpyAsync per tensor, in stream order. Pinned host memory makes the
+ * copies asynchronous (copy engines over NVLink-C2C on GB300); pageable
+ * memory works but the host waits. experts/slots are host arrays.
+ */
+moe_status_t moe_pool_fetch(const moe_experts_t* host, const moe_experts_t* pool, int n,
+                            const int32_t* experts, const int32_t* slots, void* stream);
+
+/* Workspace bytes of moe_cached_layer (0 for an invalid shape); *host_bytes,
+ * if not NULL, receives the size of its host scratch. */
+size_t moe_cache_workspace_bytes(int E, int S, int k, int D, int F, size_t* host_bytes);
+
+/*
+ * One token (T = 1) through a layer whose experts are cached (the miss fetch
+ * and background admission of the gist.science page, method section):
+ *   1. the router on the GPU (moe_route), its probabilities copied to
+ *      host_scratch, the stream waited for;
+ *   2. moe_cache_plan on the host (`step` receives the decisions);
+ *   3. the synchronous fetches into the pool on `stream`, after every earlier
+ *      admission has landed;
+ *   4. moe_decode of the served experts from the pool: y [T][D] fp32 (and
+ *      x_next = x + y in x's dtype if x_next is not NULL);
+ *   5. the admissions: on copy_stream, started once the work already on
+ *      `stream` before the decode is done (ev_issued) and announced by
+ *      ev_copied, which the next call waits for; with copy_stream NULL they
+ *      follow the decode on `stream`.
+ * host_scratch: host memory of the size moe_cache_workspace_bytes gives
+ * (pinned for asynchronous copies), untouched by the caller until `stream` has
+ * passed the call. ev_issued/ev_copied: cudaEvent_t (required with a
+ * copy_stream). Workspace: moe_cache_workspace_bytes, zeroed once. The call
+ * returns after step 2 has run, with steps 3-5 enqueued.
+ */
+moe_status_t moe_cached_layer(const moe_router_t* router, const moe_experts_t* host, const moe_experts_t* pool,
+                              moe_cache_t* cache, const moe_replay_policy_t* policy, const void* x,
+                              moe_dtype_t x_dtype, float* y, void* x_next, moe_cache_step_t* step,
+                              void* host_scratch, void* workspace, size_t ws_bytes, void* stream,
+                              void* copy_stream, void* ev_issued, void* ev_copied);
+
 /*
  * moe_layer for ONE token (T = 1) without a workspace: no counterpart in the
  * pages; it exists for callers that cannot allocate device memory where they

@@ -30,7 +30,8 @@ MOE_OP_SHARED, MOE_OP_PREROUTE = 5, 6
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_substitute", "moe_decode", "moe_layer",
             "moe_layer_resident", "moe_layer_stack", "moe_layer_stack_resident", "moe_prefill", "moe_layer_noalloc",
-            "moe_replay", "moe_shared_lora", "moe_preroute",
+            "moe_replay", "moe_shared_lora", "moe_preroute", "moe_cache_plan", "moe_pool_fetch",
+            "moe_cache_workspace_bytes", "moe_cached_layer",
             "moe_check_status", "moe_set_wait_limit", "moe_status_string")
 
 
@@ -82,6 +83,19 @@ class _Prerouter(ctypes.Structure):
                 ("norm_topk", ctypes.c_int)]
 
 
+class _Cache(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("S", ctypes.c_int), ("k", ctypes.c_int),
+                ("slot_of", ctypes.c_void_p), ("expert_of", ctypes.c_void_p),
+                ("freq", ctypes.c_void_p), ("acc", ctypes.c_void_p)]
+
+
+class _CacheStep(ctypes.Structure):
+    _fields_ = [("expert", ctypes.c_void_p), ("slot", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("flag", ctypes.c_void_p), ("fetch_expert", ctypes.c_void_p), ("fetch_slot", ctypes.c_void_p),
+                ("admit_expert", ctypes.c_void_p), ("admit_slot", ctypes.c_void_p),
+                ("n_fetch", ctypes.c_int), ("n_admit", ctypes.c_int), ("mass", ctypes.c_double)]
+
+
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(f"{path} is missing: build it with moe_routed_expert_route_gb300/build.py "
@@ -102,13 +116,19 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_stack_resident.argtypes = [I, P, P, P, I, I, P, ctypes.c_float, P, P, P, P, P, P, P, P, S, P]
     lib.moe_shared_lora.argtypes = [P, P, I, I, P, I, P, S, P]
     lib.moe_preroute.argtypes = [P, P, I, I, P, P, P, P, P, P, S, P]
+    lib.moe_cache_plan.argtypes = [P, P, P, P]
+    lib.moe_pool_fetch.argtypes = [P, P, I, P, P, P]
+    lib.moe_cache_workspace_bytes.argtypes = [I, I, I, I, I, P]
+    lib.moe_cache_workspace_bytes.restype = S
+    lib.moe_cached_layer.argtypes = [P, P, P, P, P, P, I, P, P, P, P, P, S, P, P, P, P]
     lib.moe_check_status.argtypes = [P, P]
     lib.moe_set_wait_limit.argtypes = [P, ctypes.c_ulonglong, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for f in ("moe_route", "moe_substitute", "moe_decode", "moe_layer", "moe_prefill",
               "moe_layer_noalloc", "moe_layer_resident", "moe_layer_stack", "moe_check_status",
-              "moe_set_wait_limit", "moe_shared_lora", "moe_preroute"):
+              "moe_set_wait_limit", "moe_shared_lora", "moe_preroute", "moe_cache_plan", "moe_pool_fetch",
+              "moe_cached_layer"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -137,6 +157,18 @@ def _stream(stream=None):
 def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _host(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
@@ -200,18 +232,21 @@ class Experts:
         return cls(layer["gate_q"], layer["gate_s"], layer["up_q"], layer["up_s"],
                    layer["down_q"], layer["down_s"], qbits)
 
-    def struct(self) -> _Experts:
+    def struct(self, host: bool = False) -> _Experts:
+        """host: the tensors are in host memory (an expert store for
+        moe_pool_fetch / moe_cached_layer), else on the device."""
         E, F = self.gate_q.shape[:2]
         D = self.down_q.shape[1]
         cb = 1 if self.qbits == 8 else 2
         qd = (torch.int8, torch.uint8)
         sd = (torch.float32, torch.float16)
-        _dev(self.gate_q, "gate_q", qd, (E, F, D // cb))
-        _dev(self.up_q, "up_q", qd, (E, F, D // cb))
-        _dev(self.down_q, "down_q", qd, (E, D, F // cb))
-        _dev(self.gate_s, "gate_s", sd, (E, F, D // 32))
-        _dev(self.up_s, "up_s", self.gate_s.dtype, (E, F, D // 32))
-        _dev(self.down_s, "down_s", self.gate_s.dtype, (E, D, F // 32))
+        chk = _host if host else _dev
+        chk(self.gate_q, "gate_q", qd, (E, F, D // cb))
+        chk(self.up_q, "up_q", qd, (E, F, D // cb))
+        chk(self.down_q, "down_q", qd, (E, D, F // cb))
+        chk(self.gate_s, "gate_s", sd, (E, F, D // 32))
+        chk(self.up_s, "up_s", self.gate_s.dtype, (E, F, D // 32))
+        chk(self.down_s, "down_s", self.gate_s.dtype, (E, D, F // 32))
         return _Experts(E, D, F, MOE_Q_INT8_SYM_B32 if self.qbits == 8 else MOE_Q_INT4_SYM_B32,
                         MOE_F32 if self.gate_s.dtype == torch.float32 else MOE_F16,
                         self.gate_q.data_ptr(), self.gate_s.data_ptr(), self.up_q.data_ptr(),
@@ -314,6 +349,99 @@ class Prerouter:
                           self.fc2.data_ptr(), self.L.data_ptr(),
                           None if self.bias is None else self.bias.data_ptr(),
                           1 if self.norm_topk else 0)
+
+
+class ExpertCache:
+    """Host state of one layer's expert cache (slot table, routing counts,
+    accumulated substituted weight) and the arrays of one token's decisions,
+    all numpy arrays handed to the C calls by address."""
+
+    def __init__(self, E: int, k: int, cached):
+        import numpy as np
+        cached = [int(e) for e in cached]
+        self.E, self.S, self.k = E, len(cached), k
+        self.slot_of = np.full(E, -1, np.int32)
+        self.expert_of = np.asarray(cached, np.int32).copy()
+        for s_, e in enumerate(cached):
+            self.slot_of[e] = s_
+        self.freq = np.zeros(E, np.int32)
+        self.acc = np.zeros(E, np.float64)
+        self.step = {n: np.zeros(k, t) for n, t in (
+            ("expert", np.int32), ("slot", np.int32), ("w", np.float32), ("flag", np.uint8),
+            ("fetch_expert", np.int32), ("fetch_slot", np.int32), ("admit_expert", np.int32),
+            ("admit_slot", np.int32))}
+        self._c = _Cache(E, self.S, k, *(a.ctypes.data for a in (self.slot_of, self.expert_of, self.freq,
+                                                                  self.acc)))
+        self._st = _CacheStep(*(self.step[n].ctypes.data for n in (
+            "expert", "slot", "w", "flag", "fetch_expert", "fetch_slot", "admit_expert", "admit_slot")), 0, 0, 0.0)
+
+    def decisions(self) -> dict:
+        d = {n: a.copy() for n, a in self.step.items()}
+        d["fetch_expert"] = d["fetch_expert"][: self._st.n_fetch]
+        d["fetch_slot"] = d["fetch_slot"][: self._st.n_fetch]
+        d["admit_expert"] = d["admit_expert"][: self._st.n_admit]
+        d["admit_slot"] = d["admit_slot"][: self._st.n_admit]
+        d["mass"] = self._st.mass
+        return d
+
+
+def _policy(policy: int, threshold: float, admit_mass: float) -> _ReplayPolicy:
+    return _ReplayPolicy(policy, threshold, admit_mass, 0.0, 0.0)
+
+
+def moe_cache_plan(cache: ExpertCache, probs, policy: int, threshold: float = 0.15,
+                   admit_mass: float = 0.0) -> dict:
+    """One token's decisions at one layer from its fp32 probabilities [E] (host)."""
+    import numpy as np
+    p = np.ascontiguousarray(probs, dtype=np.float32)
+    if p.shape != (cache.E,):
+        raise ValueError(f"probs has shape {p.shape}, expected ({cache.E},)")
+    pol = _policy(policy, threshold, admit_mass)
+    _check("moe_cache_plan", _lib.moe_cache_plan(ctypes.byref(cache._c), p.ctypes.data, ctypes.byref(pol),
+                                                 ctypes.byref(cache._st)))
+    return cache.decisions()
+
+
+def moe_pool_fetch(host: "Experts", pool: "Experts", experts, slots, stream=None):
+    import numpy as np
+    ex = np.ascontiguousarray(experts, dtype=np.int32)
+    sl = np.ascontiguousarray(slots, dtype=np.int32)
+    if ex.shape != sl.shape or ex.ndim != 1:
+        raise ValueError("experts and slots must be 1-D of the same length")
+    h, d = host.struct(host=True), pool.struct()
+    _check("moe_pool_fetch", _lib.moe_pool_fetch(ctypes.byref(h), ctypes.byref(d), int(ex.size), ex.ctypes.data,
+                                                 sl.ctypes.data, _stream(stream)))
+
+
+def moe_cache_workspace_bytes(E: int, S: int, k: int, D: int, F: int):
+    hb = ctypes.c_size_t(0)
+    n = int(_lib.moe_cache_workspace_bytes(E, S, k, D, F, ctypes.byref(hb)))
+    return n, int(hb.value)
+
+
+def moe_cached_layer(router: "Router", host: "Experts", pool: "Experts", cache: ExpertCache, policy: int,
+                     threshold: float, admit_mass: float, x: torch.Tensor, y: torch.Tensor,
+                     x_next: Optional[torch.Tensor], host_scratch: torch.Tensor, ws: torch.Tensor,
+                     stream=None, copy_stream=None, ev_issued=None, ev_copied=None) -> dict:
+    """One token through a cached layer; returns the token's decisions.
+    ev_issued / ev_copied are torch.cuda.Event objects that have been recorded
+    once (so that they exist)."""
+    r = router.struct()
+    _dev(x, "x", (torch.float32, torch.bfloat16), (1, r.D))
+    _dev(y, "y", torch.float32, (1, r.D))
+    if x_next is not None:
+        _dev(x_next, "x_next", x.dtype, (1, r.D))
+    _host(host_scratch, "host_scratch", torch.uint8)
+    h, d = host.struct(host=True), pool.struct()
+    pol = _policy(policy, threshold, admit_mass)
+    cs = None if copy_stream is None else ctypes.c_void_p(copy_stream.cuda_stream)
+    e1 = None if ev_issued is None else ctypes.c_void_p(ev_issued.cuda_event)
+    e2 = None if ev_copied is None else ctypes.c_void_p(ev_copied.cuda_event)
+    _check("moe_cached_layer", _lib.moe_cached_layer(
+        ctypes.byref(r), ctypes.byref(h), ctypes.byref(d), ctypes.byref(cache._c), ctypes.byref(pol), _ptr(x),
+        _act_dtype(x), _ptr(y), _ptr(x_next), ctypes.byref(cache._st), _ptr(host_scratch), _ptr(ws), ws.numel(),
+        _stream(stream), cs, e1, e2))
+    return cache.decisions()
 
 
 def moe_workspace_bytes(op: int, T: int, k: int, E: int, D: int, F: int) -> int:
