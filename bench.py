@@ -15,7 +15,8 @@ the same resident weights: the batched decode sweep (T = 1..64), residency
 substitution with int4 experts (T = 1, 16) and prefill (T = 2048, 16384), each
 with its roofline, the CPU oracle's rate on a bounded sample, and the clocks
 seen while it ran; then the shared expert with its unmerged LoRA and the
-prerouter head (T = 1, 16).
+prerouter head (T = 1, 16), and the expert cache with miss fetch and
+background admission (512 experts, a quarter cached in HBM).
 
 Prints ONE JSON line (rank 0). With --impl reference the CPU oracle is timed on
 a bounded sample of the headline workload instead.
@@ -802,6 +803,110 @@ def run_edge0(args, dev):
     return out
 
 
+def run_expert_cache(args, dev, n_tok: int = 96, warm: int = 16, L: int = 2):
+    """Miss fetch and background admission (gist.science page, method
+    section) on the 512-expert top-10 int4 layer: all experts in pinned host
+    memory, a quarter of them (128) cached in an HBM pool per layer, the 0.15
+    rule with admission at 0.5. One token at a time through L layers: router
+    on the GPU, decisions on the host, kept misses copied in by the copy
+    engines, decode from the pool, admissions on a copy stream. The path waits
+    for the router once per layer, so the time is wall clock around the token
+    loop (with a device synchronisation at its end)."""
+    import numpy as np
+    import moe_routed_expert_route_gb300 as M
+    import oracle
+    from oracle import replay as R
+    cfg = W.CONFIGS[3]
+    names = _EXPERT_TENSORS
+    hbm, _, _, kind = peaks()
+    per_expert = W.routed_bytes_per_expert(cfg)
+    layers = []
+    for l in range(L):
+        lw = W.make_layer(cfg, l, dev)
+        host = {n: lw[n].cpu().pin_memory() for n in names}
+        pool = {n: torch.zeros((cfg.resident + cfg.k,) + tuple(lw[n].shape[1:]), dtype=lw[n].dtype, device=dev)
+                for n in names}
+        hx, px = M.Experts.from_layer(host, cfg.qbits), M.Experts.from_layer(pool, cfg.qbits)
+        cached = torch.nonzero(W.make_resident_mask(cfg, l)).flatten().numpy()
+        M.moe_pool_fetch(hx, px, cached, np.arange(cfg.resident))
+        n, hb = M.moe_cache_workspace_bytes(cfg.E, cfg.resident, cfg.k, cfg.D, cfg.F)
+        layers.append(dict(router=M.Router(lw["Wr"], lw["bias"], cfg.k), host=host, pool=pool, hx=hx, px=px,
+                           cache=M.ExpertCache(cfg.E, cfg.k, cached), cached0=cached.copy(),
+                           ws=torch.zeros(n, dtype=torch.uint8, device=dev),
+                           scratch=torch.zeros(hb, dtype=torch.uint8).pin_memory(),
+                           Wr=lw["Wr"].cpu(), bias=lw["bias"].cpu()))
+        del lw
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    x = W.make_tokens(cfg, n_tok + warm, 11, dev)
+    y = torch.empty(1, cfg.D, device=dev)
+    cs = torch.cuda.Stream(dev)
+    ev1, ev2 = torch.cuda.Event(), torch.cuda.Event()
+    ev1.record()
+    ev2.record()
+    stats = dict(fetch=0, sub=0, adm=0, mass=0.0)
+
+    def token(t, count):
+        for ly in layers:
+            d = M.moe_cached_layer(ly["router"], ly["hx"], ly["px"], ly["cache"], M.MOE_POLICY_THRESHOLD, 0.15, 0.5,
+                                   x[t:t + 1], y, None, ly["scratch"], ly["ws"], None, cs, ev1, ev2)
+            if count:
+                stats["fetch"] += len(d["fetch_expert"])
+                stats["sub"] += int((d["flag"] == 2).sum())
+                stats["adm"] += len(d["admit_expert"])
+                stats["mass"] += d["mass"]
+    for t in range(warm):
+        token(t, False)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        t0 = time.perf_counter()
+        for t in range(warm, warm + n_tok):
+            token(t, True)
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+    for ly in layers:
+        assert M.moe_check_status(ly["ws"]) == 0
+    us_layer = el / (n_tok * L) * 1e6
+    served = cfg.k * per_expert  # expert bytes the decode reads per token and layer
+    fetched = (stats["fetch"] + stats["adm"]) * per_expert
+    # the oracle on a sample: router, decisions, and the MoE on the served
+    # experts, one layer, from the cache state the GPU run started with
+    ns = 4
+    ly0 = layers[0]
+    xs = x[:ns].cpu()
+    t1 = time.perf_counter()
+    r = oracle.router(xs, ly0["Wr"], ly0["bias"], cfg.k)
+    res = np.zeros((1, cfg.E), np.uint8)
+    res[0, ly0["cached0"]] = 1
+    rp = R.replay(r["probs32"][:, None, :], cfg.k, R.THRESHOLD, 0.15, 0.5, 0.0, 0.0, resident=res.tolist())
+    for t in range(ns):
+        used = np.asarray(rp["used"][t][0], np.int64)
+        sub = {n: ly0["host"][n][torch.from_numpy(used)] for n in names}
+        oracle.moe(sub, xs[t:t + 1], np.arange(cfg.k, dtype=np.int32)[None], r["w"][t:t + 1], cfg.qbits,
+                   nthreads=os.cpu_count() or 1, compact=False)
+    el_o = time.perf_counter() - t1
+    out = {"workload": f"expert cache: 1 token x {L} layers, E=512 top-10 D=2048 F=512 int4, 128 of 512 experts "
+                       "cached in HBM per layer, all in pinned host memory; 0.15 rule, admission at 0.5",
+           "T": 1, "unit": "tokens/s", "tokens_per_s": round(n_tok / el, 2), "us_per_layer": round(us_layer, 2),
+           "sync_fetches_per_token_layer": round(stats["fetch"] / (n_tok * L), 3),
+           "substituted_per_token_layer": round(stats["sub"] / (n_tok * L), 3),
+           "admissions_per_token_layer": round(stats["adm"] / (n_tok * L), 3),
+           "substituted_mass_per_token_layer": round(stats["mass"] / (n_tok * L), 4),
+           "host_to_device_gbs": round(fetched / el / 1e9, 2),
+           "roofline": roofline("hbm", served / (us_layer * 1e-6) / 1e9, hbm, "GB/s",
+                                "route + host decisions + copies + decode (wall clock per layer)",
+                                {"peak_kind": kind, "note": "served expert bytes per layer over the wall-clock "
+                                 "time of a layer, which includes the host round trip for the decisions"}),
+           "cpu_baseline": {"value": round(ns / (el_o * L), 4), "unit": "tokens/s", "cores": os.cpu_count() or 1,
+                            "kind": "oracle", "sample": f"router, replay decisions and MoE on the served experts "
+                                                        f"for {ns} tokens of one layer, {el_o:.1f} s, scaled to {L} layers"},
+           "timing": "wall clock (perf_counter) around the token loop, device synchronised at its end",
+           "clocks": clk.summary()}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -824,10 +929,11 @@ def run_ours(args):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         extra["replay"], extra["substitution"] = run_substitution(args, dev)
-        try:
-            extra["edge0"] = run_edge0(args, dev)
-        except Exception as e:  # reported, never at the cost of the line above
-            extra["edge0"] = {"error": f"{type(e).__name__}: {e}"[:300]}
+        for key, fn in (("edge0", run_edge0), ("expert_cache", run_expert_cache)):
+            try:
+                extra[key] = fn(args, dev)
+            except Exception as e:  # reported, never at the cost of the line above
+                extra[key] = {"error": f"{type(e).__name__}: {e}"[:300]}
         line["workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
