@@ -31,8 +31,12 @@ DEV = "cuda"
 REL_TOL = parity.REL_TOL
 
 
-def _to(se: dict, dev):
-    return {k: (v.to(dev) if hasattr(v, "to") else v) for k, v in se.items()}
+def _to(d: dict, dev):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+# Inputs are drawn on the CPU and moved to the device, so that they are the
+# same wherever the test runs (and the near ties among them can be counted
+# without a GPU: none at the shapes below).
 
 
 def gpu_shared(se: dict, x: torch.Tensor, y0=None):
@@ -58,8 +62,8 @@ def test_shared_lora_tiny(qbits, rank, T):
     sc = W.SharedConfig("t", D=64, F=96, qbits=qbits, scale_dtype=torch.float32, rank=rank,
                         alpha=2.0 * max(rank, 1), lora_dtype=torch.float32, x_dtype=torch.float32,
                         weight_sigma=0.1, lora_a_sigma=0.2, lora_b_sigma=0.2, cfg_id=400 + rank)
-    se = W.make_shared_expert(sc, 0, DEV)
-    x = W.make_shared_tokens(sc, T, 0, DEV)
+    se = _to(W.make_shared_expert(sc, 0, "cpu"), DEV)
+    x = W.make_shared_tokens(sc, T, 0, "cpu").to(DEV)
     _check_y(gpu_shared(se, x), oracle.shared_lora(se, x))
 
 
@@ -68,8 +72,8 @@ def test_shared_lora_decode_shape(T):
     # the shared expert of the 2048-wide decode layer: int4 base, fp16 scales,
     # rank-16 bf16 adapters, bf16 x
     sc = W.SHARED_CONFIGS["decode"]
-    se = W.make_shared_expert(sc, 0, DEV)
-    x = W.make_shared_tokens(sc, T, 1, DEV)
+    se = _to(W.make_shared_expert(sc, 0, "cpu"), DEV)
+    x = W.make_shared_tokens(sc, T, 1, "cpu").to(DEV)
     y_ref = oracle.shared_lora(se, x)
     _check_y(gpu_shared(se, x), y_ref)
     # the adapter's contribution is resolved, not lost in the tolerance
@@ -88,8 +92,8 @@ def test_shared_lora_decode_shape(T):
 def test_shared_lora_accumulates_into_y_and_int8_bf16_adapters():
     sc = W.SharedConfig("t8", D=256, F=128, qbits=8, scale_dtype=torch.float16, rank=8, alpha=16.0,
                         lora_dtype=torch.bfloat16, x_dtype=torch.bfloat16, cfg_id=410)
-    se = W.make_shared_expert(sc, 0, DEV)
-    x = W.make_shared_tokens(sc, 5, 0, DEV)
+    se = _to(W.make_shared_expert(sc, 0, "cpu"), DEV)
+    x = W.make_shared_tokens(sc, 5, 0, "cpu").to(DEV)
     y0 = torch.randn(5, sc.D, device=DEV, generator=torch.Generator(DEV).manual_seed(3))
     y = gpu_shared(se, x, y0)
     _check_y(y, y0.cpu().numpy().astype(np.float64) + oracle.shared_lora(se, x))
@@ -119,8 +123,8 @@ def tiny_head_cfg(seed):
 @pytest.mark.parametrize("T", [1, 5, 11])
 def test_preroute_tiny(T):
     cfg = tiny_head_cfg(T)
-    head = W.make_prerouter(cfg, 0, H=32, device=DEV, sigma=0.3, hot_sigma=0.5)
-    x = W.make_tokens(cfg, T, 0, DEV)
+    head = _to(W.make_prerouter(cfg, 0, H=32, device="cpu", sigma=0.3, hot_sigma=0.5), DEV)
+    x = W.make_tokens(cfg, T, 0, "cpu").to(DEV)
     cur, prev = W.make_routing_history(cfg, T, stream=T, device=DEV)
     prev[0] = -1                  # the first token has no previous token
     if T > 1:
@@ -137,8 +141,8 @@ def test_preroute_decode_shape_feeds_decode(T):
     # predicts the next layer's routing, which is then used as that layer's
     # routing by moe_decode (prediction-as-routing)
     cfg = W.CONFIGS[1]
-    head = W.make_prerouter(cfg, 0, H=512, device=DEV)
-    x = W.make_tokens(cfg, T, 5, DEV)
+    head = _to(W.make_prerouter(cfg, 0, H=512, device="cpu"), DEV)
+    x = W.make_tokens(cfg, T, 5, "cpu").to(DEV)
     cur, prev = W.make_routing_history(cfg, T, stream=5, device=DEV, absent_prev=(T == 1))
     got, status = gpu_preroute(cfg, head, x, cur, prev)
     assert status == M.MOE_OK
@@ -158,8 +162,8 @@ def test_preroute_decode_shape_feeds_decode(T):
 
 def test_preroute_records_an_out_of_range_id_and_skips_it():
     cfg = tiny_head_cfg(9)
-    head = W.make_prerouter(cfg, 0, H=32, device=DEV, sigma=0.3, hot_sigma=0.5)
-    x = W.make_tokens(cfg, 2, 0, DEV)
+    head = _to(W.make_prerouter(cfg, 0, H=32, device="cpu", sigma=0.3, hot_sigma=0.5), DEV)
+    x = W.make_tokens(cfg, 2, 0, "cpu").to(DEV)
     cur, prev = W.make_routing_history(cfg, 2, stream=9, device=DEV)
     bad = cur.clone()
     bad[1, 0] = cfg.E + 5
