@@ -499,8 +499,11 @@ moe_status_t moe_cached_layer(const moe_router_t* router, const moe_experts_t* h
  * GPU, e.g. on two streams, race and must be avoided. Device-side conditions
  * (an expert id out of range, a wait that ran out because another kernel held
  * SMs) are not reported by this entry point, and outputs after such a
- * condition are not valid: a caller that needs to detect them uses moe_layer
- * with a workspace and moe_check_status. Arguments as moe_layer with T = 1.
+ * condition are not valid. An idx entry of -1 marks a slot the call could not
+ * route (a wait that ran out before the routing was complete), so check that
+ * every idx entry lies in [0, E) before using y; the converse does not hold, and
+ * a caller that needs to detect every such condition uses moe_layer with a
+ * workspace and moe_check_status. Arguments as moe_layer with T = 1.
  */
 moe_status_t moe_layer_noalloc(const moe_router_t* router, const moe_experts_t* experts, const void* x,
                                moe_dtype_t x_dtype, int32_t* idx, float* w, float* probs, float* y,
