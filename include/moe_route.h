@@ -472,7 +472,9 @@ size_t moe_cache_workspace_bytes(int E, int S, int k, int D, int F, size_t* host
  * (pinned for asynchronous copies), untouched by the caller until `stream` has
  * passed the call. ev_issued/ev_copied: cudaEvent_t (required with a
  * copy_stream). Workspace: moe_cache_workspace_bytes, zeroed once. The call
- * returns after step 2 has run, with steps 3-5 enqueued.
+ * returns after step 2 has run, with steps 3-5 enqueued. A status other than
+ * MOE_OK returned after step 2 leaves the slot table ahead of the pool: copy
+ * expert_of[s] into every slot s with moe_pool_fetch before the next call.
  */
 moe_status_t moe_cached_layer(const moe_router_t* router, const moe_experts_t* host, const moe_experts_t* pool,
                               moe_cache_t* cache, const moe_replay_policy_t* policy, const void* x,

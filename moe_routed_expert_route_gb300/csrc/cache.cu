@@ -38,12 +38,14 @@ constexpr int kMaxK = 32;
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-// The cached expert to evict: lowest frequency, lower id on ties, not in use.
+// The cached expert to evict: lowest frequency, lower id on ties, not in use
+// (a scan of the S slots).
 int victim(const moe_cache_t* c, const std::vector<uint8_t>& in_use) {
     int best = -1;
-    for (int e = 0; e < c->E; e++) {
-        if (c->slot_of[e] < 0 || in_use[e]) continue;
-        if (best < 0 || c->freq[e] < c->freq[best]) best = e;
+    for (int sl = 0; sl < c->S; sl++) {
+        const int e = c->expert_of[sl];
+        if (in_use[e]) continue;
+        if (best < 0 || c->freq[e] < c->freq[best] || (c->freq[e] == c->freq[best] && e < best)) best = e;
     }
     return best;
 }
@@ -164,15 +166,21 @@ extern "C" moe_status_t moe_cache_plan(moe_cache_t* c, const float* p, const moe
     std::vector<int> idx(k);
     std::vector<double> w(k);
     std::vector<uint8_t> taken(E, 0), in_use(E, 0);
-    // 1. top-k by repeated selection of the largest untaken probability (the
-    //    strict comparison keeps the lower id among equal values)
-    for (int r = 0; r < k; r++) {
-        int b = -1;
-        for (int e = 0; e < E; e++)
-            if (!taken[e] && (b < 0 || p[e] > p[b])) b = e;
-        taken[b] = 1;
-        idx[r] = b;
+    // 1. top-k in one pass over the experts in id order, keeping the best k
+    //    sorted by probability; an expert enters or moves up only past strictly
+    //    smaller values, so equal values keep the lower id first
+    int n = 0;
+    for (int e = 0; e < E; e++) {
+        const float v = p[e];
+        if (n == k && !(v > p[idx[k - 1]])) continue;
+        int pos = n < k ? n++ : k - 1;
+        while (pos > 0 && v > p[idx[pos - 1]]) {
+            idx[pos] = idx[pos - 1];
+            pos--;
+        }
+        idx[pos] = e;
     }
+    for (int r = 0; r < k; r++) taken[idx[r]] = 1;
     double sum = 0.0;
     for (int r = 0; r < k; r++) sum += (double)p[idx[r]];
     for (int r = 0; r < k; r++) w[r] = sum > 0.0 ? (double)p[idx[r]] / sum : 0.0;
@@ -198,10 +206,13 @@ extern "C" moe_status_t moe_cache_plan(moe_cache_t* c, const float* p, const moe
         if (pol->policy == MOE_POLICY_FETCH_ALL) want = true;
         else if (pol->policy == MOE_POLICY_FIRST_CHOICE) want = r == 0;
         else want = r == 0 || w[r] >= thr;
-        int rep = -1;
+        int rep = -1;  // the stand-in: the most probable cached expert not taken, lower id on ties
         if (!want)
-            for (int cand = 0; cand < E; cand++)
-                if (c->slot_of[cand] >= 0 && !taken[cand] && (rep < 0 || p[cand] > p[rep])) rep = cand;
+            for (int sl = 0; sl < S; sl++) {
+                const int cand = c->expert_of[sl];
+                if (taken[cand]) continue;
+                if (rep < 0 || p[cand] > p[rep] || (p[cand] == p[rep] && cand < rep)) rep = cand;
+            }
         if (rep < 0) {  // fetched: into a victim's slot, else into the transient slot S + r
             const int s = enter(c, in_use, e);
             st->slot[r] = s >= 0 ? s : S + r;
