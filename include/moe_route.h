@@ -482,6 +482,49 @@ moe_status_t moe_cached_layer(const moe_router_t* router, const moe_experts_t* h
                               void* host_scratch, void* workspace, size_t ws_bytes, void* stream,
                               void* copy_stream, void* ev_issued, void* ev_copied);
 
+/* Staged slot table: a pool of n_slots >= 2k expert slots (moe_experts_t with
+ * E = n_slots) holding the experts predicted for the coming step. Host state
+ * owned by the caller, updated in place:
+ *   slot_of   [E] int32: slot of expert e, or -1
+ *   expert_of [n_slots] int32: expert in slot s, or -1 (empty)
+ *   in_flight [k] int32: the slots the previous step's decode reads (-1: none) */
+typedef struct {
+    int E, n_slots, k;
+    int32_t* slot_of;
+    int32_t* expert_of;
+    int32_t* in_flight;
+} moe_stage_t;
+
+/*
+ * Host code: the slots of one step's predicted experts ids [k] (host), for
+ * the staged decode and the incremental sticky-slot stack of xyznot.com "The
+ * Other Half of the Memory Wall" (glossary): an expert already staged keeps
+ * its slot; any other takes the lowest slot that holds neither one of this
+ * step's experts nor one the step in flight reads, and is listed as a load
+ * (load_expert/load_slot, n_load of them; only changed slots are rewritten).
+ * A repeated id maps to one slot. slot [k] receives each id's slot and becomes
+ * the new in_flight.
+ */
+moe_status_t moe_stage_plan(moe_stage_t* stage, const int32_t* ids, int32_t* slot, int32_t* load_expert,
+                            int32_t* load_slot, int* n_load);
+
+/*
+ * Stages a prediction (prediction-as-routing: the prerouter's ids for the
+ * next step, pred_idx [k] on the device, e.g. moe_preroute's idx of one
+ * token): copies the ids to host_scratch ([2k] int32, pinned for asynchronous
+ * copies) and waits for `stream`; plans (moe_stage_plan: slot, loads); then,
+ * on copy_stream (NULL: on `stream`), copies the slot ids to slot_idx [k]
+ * (device) and the loaded experts from `host` into their `pool` slots, and
+ * records ev_staged (a cudaEvent_t, required with a copy_stream). The decode
+ * of that step is moe_decode on `pool` with idx = slot_idx and the predicted
+ * weights, on a stream made to wait for ev_staged. Use two slot_idx buffers
+ * in turn, as the decode of the step in flight still reads the other one.
+ */
+moe_status_t moe_stage_prediction(moe_stage_t* stage, const moe_experts_t* host, const moe_experts_t* pool,
+                                  const int32_t* pred_idx, int32_t* slot_idx, int32_t* host_scratch, int32_t* slot,
+                                  int32_t* load_expert, int32_t* load_slot, int* n_load, void* stream,
+                                  void* copy_stream, void* ev_staged);
+
 /*
  * moe_layer for ONE token (T = 1) without a workspace: no counterpart in the
  * pages; it exists for callers that cannot allocate device memory where they

@@ -7,6 +7,7 @@ from ._lib import (EXPORTED, LIB_PATH, MOE_BF16, MOE_POLICY_FETCH_ALL, MOE_POLIC
                    MOE_OP_LAYER_RESIDENT, MOE_OP_PREFILL, MOE_OP_PREROUTE, MOE_OP_ROUTE,
                    MOE_OP_SHARED, ExpertCache, Experts, MoeError, Prerouter, Router, Shared,
                    moe_cache_plan, moe_cache_workspace_bytes, moe_cached_layer, moe_pool_fetch,
+                   StageTable, moe_stage_plan, moe_stage_prediction,
                    moe_check_status, moe_decode, moe_layer, moe_layer_noalloc, moe_layer_resident,
                    moe_layer_stack, moe_layer_stack_resident, moe_prefill, moe_preroute, moe_replay, moe_route,
                    moe_set_wait_limit, moe_shared_lora, moe_substitute,

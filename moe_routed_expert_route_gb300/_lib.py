@@ -31,7 +31,7 @@ MOE_OP_SHARED, MOE_OP_PREROUTE = 5, 6
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_substitute", "moe_decode", "moe_layer",
             "moe_layer_resident", "moe_layer_stack", "moe_layer_stack_resident", "moe_prefill", "moe_layer_noalloc",
             "moe_replay", "moe_shared_lora", "moe_preroute", "moe_cache_plan", "moe_pool_fetch",
-            "moe_cache_workspace_bytes", "moe_cached_layer",
+            "moe_cache_workspace_bytes", "moe_cached_layer", "moe_stage_plan", "moe_stage_prediction",
             "moe_check_status", "moe_set_wait_limit", "moe_status_string")
 
 
@@ -96,6 +96,11 @@ class _CacheStep(ctypes.Structure):
                 ("n_fetch", ctypes.c_int), ("n_admit", ctypes.c_int), ("mass", ctypes.c_double)]
 
 
+class _Stage(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("n_slots", ctypes.c_int), ("k", ctypes.c_int),
+                ("slot_of", ctypes.c_void_p), ("expert_of", ctypes.c_void_p), ("in_flight", ctypes.c_void_p)]
+
+
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(f"{path} is missing: build it with moe_routed_expert_route_gb300/build.py "
@@ -121,6 +126,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_cache_workspace_bytes.argtypes = [I, I, I, I, I, P]
     lib.moe_cache_workspace_bytes.restype = S
     lib.moe_cached_layer.argtypes = [P, P, P, P, P, P, I, P, P, P, P, P, S, P, P, P, P]
+    lib.moe_stage_plan.argtypes = [P, P, P, P, P, P]
+    lib.moe_stage_prediction.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.moe_check_status.argtypes = [P, P]
     lib.moe_set_wait_limit.argtypes = [P, ctypes.c_ulonglong, P]
     lib.moe_status_string.argtypes = [I]
@@ -128,7 +135,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for f in ("moe_route", "moe_substitute", "moe_decode", "moe_layer", "moe_prefill",
               "moe_layer_noalloc", "moe_layer_resident", "moe_layer_stack", "moe_check_status",
               "moe_set_wait_limit", "moe_shared_lora", "moe_preroute", "moe_cache_plan", "moe_pool_fetch",
-              "moe_cached_layer"):
+              "moe_cached_layer", "moe_stage_plan", "moe_stage_prediction"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -383,6 +390,59 @@ class ExpertCache:
         d["admit_slot"] = d["admit_slot"][: self._st.n_admit]
         d["mass"] = self._st.mass
         return d
+
+
+class StageTable:
+    """Host state of a staged slot table (slot of each expert, expert of each
+    slot, the slots of the step in flight) and one step's outputs, numpy arrays
+    handed to the C calls by address. All slots start empty."""
+
+    def __init__(self, E: int, n_slots: int, k: int):
+        import numpy as np
+        self.E, self.n_slots, self.k = E, n_slots, k
+        self.slot_of = np.full(E, -1, np.int32)
+        self.expert_of = np.full(n_slots, -1, np.int32)
+        self.in_flight = np.full(k, -1, np.int32)
+        self.slot = np.zeros(k, np.int32)
+        self.load_expert = np.zeros(k, np.int32)
+        self.load_slot = np.zeros(k, np.int32)
+        self.n_load = ctypes.c_int(0)
+        self._c = _Stage(E, n_slots, k, self.slot_of.ctypes.data, self.expert_of.ctypes.data,
+                         self.in_flight.ctypes.data)
+        self._out = (self.slot.ctypes.data, self.load_expert.ctypes.data, self.load_slot.ctypes.data,
+                     ctypes.byref(self.n_load))
+
+    def step(self) -> dict:
+        n = self.n_load.value
+        return dict(slot=self.slot.copy(), load_expert=self.load_expert[:n].copy(),
+                    load_slot=self.load_slot[:n].copy())
+
+
+def moe_stage_plan(stage: StageTable, ids) -> dict:
+    import numpy as np
+    a = np.ascontiguousarray(ids, dtype=np.int32)
+    if a.shape != (stage.k,):
+        raise ValueError(f"ids has shape {a.shape}, expected ({stage.k},)")
+    _check("moe_stage_plan", _lib.moe_stage_plan(ctypes.byref(stage._c), a.ctypes.data, *stage._out))
+    return stage.step()
+
+
+def moe_stage_prediction(stage: StageTable, host: "Experts", pool: "Experts", pred_idx: torch.Tensor,
+                         slot_idx: torch.Tensor, host_scratch: torch.Tensor, stream=None, copy_stream=None,
+                         ev_staged=None) -> dict:
+    """Stages one predicted id list [k] (device); slot_idx [k] int32 (device)
+    receives the slot ids for the decode, once ev_staged has been reached."""
+    k = stage.k
+    _dev(pred_idx, "pred_idx", torch.int32, (k,))
+    _dev(slot_idx, "slot_idx", torch.int32, (k,))
+    _host(host_scratch, "host_scratch", torch.int32, (2 * k,))
+    h, d = host.struct(host=True), pool.struct()
+    cs = None if copy_stream is None else ctypes.c_void_p(copy_stream.cuda_stream)
+    ev = None if ev_staged is None else ctypes.c_void_p(ev_staged.cuda_event)
+    _check("moe_stage_prediction", _lib.moe_stage_prediction(
+        ctypes.byref(stage._c), ctypes.byref(h), ctypes.byref(d), _ptr(pred_idx), _ptr(slot_idx),
+        _ptr(host_scratch), *stage._out, _stream(stream), cs, ev))
+    return stage.step()
 
 
 def _policy(policy: int, threshold: float, admit_mass: float) -> _ReplayPolicy:

@@ -22,6 +22,18 @@
 //                     probabilities to the host, the plan, the synchronous
 //                     fetches, the decode of the served experts from the pool,
 //                     and the admissions on a copy stream behind the decode
+//
+// Staged slot table (xyznot.com "The Other Half of the Memory Wall", glossary:
+// "staged decode", "incremental sticky-slot stack"; method: "prediction-as-
+// routing"): the prerouter's prediction for the next token is staged into a
+// pool of fixed slots (at least 2k: double buffering) before that token runs,
+// rewriting only the slots whose expert changed.
+//   moe_stage_plan        host: slots of one step's predicted experts (a staged
+//                         expert keeps its slot, any other takes the lowest
+//                         slot held by neither this step's experts nor the
+//                         step in flight) and the loads
+//   moe_stage_prediction  the predicted ids to the host, the plan, the loads
+//                         and the slot ids on a copy stream, an event when done
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -322,5 +334,90 @@ extern "C" moe_status_t moe_cached_layer(const moe_router_t* router, const moe_e
     if (stt != MOE_OK) return stt;
     if (step->n_admit > 0 && !copy_stream)
         return moe_pool_fetch(host, pool, step->n_admit, step->admit_expert, step->admit_slot, stream);
+    return MOE_OK;
+}
+
+namespace {
+
+bool stage_ok(const moe_stage_t* st) {
+    return st && st->E >= 1 && st->k >= 1 && st->k <= kMaxK && st->n_slots >= 2 * st->k && st->slot_of &&
+           st->expert_of && st->in_flight;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_stage_plan(moe_stage_t* st, const int32_t* ids, int32_t* slot, int32_t* load_expert,
+                                       int32_t* load_slot, int* n_load) {
+    if (!stage_ok(st) || !ids || !slot || !load_expert || !load_slot || !n_load) return MOE_ERR_INVALID_ARG;
+    const int E = st->E, NS = st->n_slots, k = st->k;
+    for (int r = 0; r < k; r++)
+        if (ids[r] < 0 || ids[r] >= E || st->in_flight[r] < -1 || st->in_flight[r] >= NS) return MOE_ERR_INVALID_ARG;
+    // the slot table must be a consistent partial map
+    for (int e = 0; e < E; e++)
+        if (st->slot_of[e] < -1 || st->slot_of[e] >= NS || (st->slot_of[e] >= 0 && st->expert_of[st->slot_of[e]] != e))
+            return MOE_ERR_INVALID_ARG;
+    for (int sl = 0; sl < NS; sl++)
+        if (st->expert_of[sl] < -1 || st->expert_of[sl] >= E ||
+            (st->expert_of[sl] >= 0 && st->slot_of[st->expert_of[sl]] != sl))
+            return MOE_ERR_INVALID_ARG;
+    // slots this step may not take: the in-flight step's, and those of this
+    // step's experts that are staged already
+    std::vector<uint8_t> locked(NS, 0);
+    for (int r = 0; r < k; r++) {
+        if (st->in_flight[r] >= 0) locked[st->in_flight[r]] = 1;
+        if (st->slot_of[ids[r]] >= 0) locked[st->slot_of[ids[r]]] = 1;
+    }
+    int n = 0, next_free = 0;
+    for (int r = 0; r < k; r++) {
+        const int e = ids[r];
+        if (st->slot_of[e] >= 0) {  // staged (possibly by an earlier slot of this step)
+            slot[r] = st->slot_of[e];
+            continue;
+        }
+        while (next_free < NS && locked[next_free]) next_free++;
+        if (next_free == NS) return MOE_ERR_INVALID_ARG;  // cannot happen with 2k slots
+        const int s = next_free;
+        const int old = st->expert_of[s];
+        if (old >= 0) st->slot_of[old] = -1;
+        st->expert_of[s] = e;
+        st->slot_of[e] = s;
+        locked[s] = 1;
+        slot[r] = s;
+        load_expert[n] = e;
+        load_slot[n] = s;
+        n++;
+    }
+    for (int r = 0; r < k; r++) st->in_flight[r] = slot[r];
+    *n_load = n;
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_stage_prediction(moe_stage_t* st, const moe_experts_t* host, const moe_experts_t* pool,
+                                             const int32_t* pred_idx, int32_t* slot_idx, int32_t* host_scratch,
+                                             int32_t* slot, int32_t* load_expert, int32_t* load_slot, int* n_load,
+                                             void* stream, void* copy_stream, void* ev_staged) {
+    if (!stage_ok(st) || !pred_idx || !slot_idx || !host_scratch || !slot || !load_expert || !load_slot || !n_load)
+        return MOE_ERR_INVALID_ARG;
+    if (!experts_ok(host) || !experts_ok(pool) || !same_format(host, pool) || host->E != st->E ||
+        pool->E != st->n_slots)
+        return MOE_ERR_INVALID_ARG;
+    if (copy_stream && !ev_staged) return MOE_ERR_INVALID_ARG;
+    const int k = st->k;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs = copy_stream ? static_cast<cudaStream_t>(copy_stream) : s;
+    int32_t* h_ids = host_scratch;
+    int32_t* h_slot = host_scratch + k;
+    // the prediction, and every earlier decode that read a slot, are done after this
+    if (cudaMemcpyAsync(h_ids, pred_idx, sizeof(int32_t) * k, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    moe_status_t stt = moe_stage_plan(st, h_ids, slot, load_expert, load_slot, n_load);
+    if (stt != MOE_OK) return stt;
+    for (int r = 0; r < k; r++) h_slot[r] = slot[r];
+    if (cudaMemcpyAsync(slot_idx, h_slot, sizeof(int32_t) * k, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    stt = moe_pool_fetch(host, pool, *n_load, load_expert, load_slot, copy_stream ? copy_stream : stream);
+    if (stt != MOE_OK) return stt;
+    if (copy_stream && cudaEventRecord(static_cast<cudaEvent_t>(ev_staged), cs) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -1,9 +1,11 @@
 """The staged slot table: the oracle (``oracle/staging.py``) pinned by a
 hand-worked example and by the invariants the glossary of the xyznot.com Edge0
 page fixes (staged decode: fixed slots reached through a slot table, double
-buffering; incremental sticky-slot stack: only changed slots are rewritten)."""
+buffering; incremental sticky-slot stack: only changed slots are rewritten),
+and the library's moe_stage_plan matched to it step by step (no GPU)."""
 from __future__ import annotations
 
+import ctypes
 import json
 import os
 import types
@@ -11,6 +13,8 @@ import types
 import numpy as np
 import pytest
 
+import moe_routed_expert_route_gb300 as M
+from moe_routed_expert_route_gb300 import _lib as L
 from oracle import staging as S
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "staging_worked.json")
@@ -94,3 +98,34 @@ def test_staging_planted_mistake_is_caught(name):
     except (ValueError, KeyError):
         held = False
     assert not held, f"planted mistake {name} passed every pin"
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_stage_plan_matches_the_oracle(seed):
+    rng = np.random.default_rng(50 + seed)
+    E = int(rng.integers(4, 300))
+    k = int(rng.integers(1, min(E // 2, 16) + 1))
+    n_slots = 2 * k + int(rng.integers(0, 5))
+    pred = _random_pred(rng, 40, E, k, sticky=float(rng.uniform(0.2, 0.9)))
+    if seed % 3 == 0:
+        pred[5][1 % k] = pred[5][0]  # a repeated id maps to one slot
+    ref = S.stage(pred, n_slots)
+    st = M.StageTable(E, n_slots, k)
+    for t, ids in enumerate(pred):
+        got = M.moe_stage_plan(st, ids)
+        assert got["slot"].tolist() == ref["slots"][t], t
+        assert list(zip(got["load_expert"].tolist(), got["load_slot"].tolist())) == ref["loads"][t], t
+    assert st.expert_of.tolist() == ref["expert_of"]
+    assert st.in_flight.tolist() == ref["in_flight"]
+
+
+def test_stage_plan_rejects_bad_arguments():
+    lib = L._lib
+    st = M.StageTable(8, 4, 2)
+    ids = np.array([1, 9], np.int32)  # 9 >= E
+    out = st._out
+    assert lib.moe_stage_plan(ctypes.byref(st._c), ids.ctypes.data, *out) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_stage_plan(ctypes.byref(st._c), None, *out) == M.MOE_ERR_INVALID_ARG
+    bad = M.StageTable(8, 3, 2)  # fewer than 2k slots
+    ids = np.array([1, 2], np.int32)
+    assert lib.moe_stage_plan(ctypes.byref(bad._c), ids.ctypes.data, *bad._out) == M.MOE_ERR_INVALID_ARG

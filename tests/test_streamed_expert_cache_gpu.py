@@ -114,3 +114,68 @@ def test_cached_layer_against_the_oracles(use_copy_stream, S, N, what):
     for s_, e in enumerate(cache.expert_of):
         for n in NAMES:
             assert torch.equal(pool[n][s_].cpu(), host[n][e]), (s_, int(e), n)
+
+
+def test_prediction_staged_one_token_ahead_through_the_slot_table():
+    """Prediction-as-routing with a staged slot table (xyznot.com "The Other
+    Half of the Memory Wall": prerouter; glossary: staged decode, incremental
+    sticky-slot stack): at token t the prerouter predicts the routing of token
+    t+1, the predicted experts are staged from host memory into a pool of 2k
+    slots on a copy stream (only changed slots are loaded), and token t+1 is
+    decoded from the pool with the predicted ids and weights. Checked: the
+    predicted routing against the oracle prerouter, every slot and load
+    against the staging oracle, y against the oracle's MoE on the predicted
+    experts, and the pool's bytes."""
+    from oracle import staging as S
+    cfg = W.LayerConfig("stage E32 k4 D256 F128", E=32, k=4, D=256, F=128, T=1, qbits=8,
+                        scale_dtype=torch.float16, x_dtype=torch.bfloat16, router_dtype=torch.bfloat16,
+                        router_sigma=0.035, zipf=1.1, layers=2, cfg_id=520)
+    k, NS = cfg.k, 2 * cfg.k
+    layer = W.make_layer(cfg, 1, "cpu")  # the layer whose routing the head predicts
+    head_cpu = W.make_prerouter(cfg, 0, H=32, device="cpu")
+    head = {n: v.to(DEV) for n, v in head_cpu.items()}
+    host = {n: layer[n].pin_memory() for n in NAMES}
+    pool = {n: torch.zeros((NS,) + tuple(layer[n].shape[1:]), dtype=layer[n].dtype, device=DEV) for n in NAMES}
+    hx, px = M.Experts.from_layer(host, cfg.qbits), M.Experts.from_layer(pool, cfg.qbits)
+    N = 13
+    x = W.make_tokens(cfg, N, 4, "cpu").to(DEV)
+    cur, prev = W.make_routing_history(cfg, N, stream=4, device=DEV)
+    st = M.StageTable(cfg.E, NS, k)
+    cs = torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    ev.record()
+    scratch = torch.zeros(2 * k, dtype=torch.int32).pin_memory()
+    slot_bufs = [torch.empty(k, dtype=torch.int32, device=DEV) for _ in range(2)]
+    ws_p = M.workspace(M.MOE_OP_PREROUTE, 1, k, cfg.E, cfg.D, 32, DEV)
+    ws_d = M.workspace(M.MOE_OP_DECODE, 1, k, NS, cfg.D, cfg.F, DEV)
+    pre = M.Prerouter.from_dict(head, k)
+    preds, wts, steps, ys = [], [], [], []
+    for t in range(N - 1):
+        idx = torch.empty(1, k, dtype=torch.int32, device=DEV)
+        w = torch.empty(1, k, dtype=torch.float32, device=DEV)
+        M.moe_preroute(pre, x[t:t + 1], cur[t:t + 1], prev[t:t + 1], idx, w, None, ws_p)
+        sb = slot_bufs[t % 2]
+        steps.append(M.moe_stage_prediction(st, hx, px, idx[0], sb, scratch, None, cs, ev))
+        torch.cuda.current_stream().wait_event(ev)
+        y = torch.empty(1, cfg.D, dtype=torch.float32, device=DEV)
+        M.moe_decode(px, x[t + 1:t + 2], sb.view(1, k), w, y, None, ws_d)
+        preds.append(idx.cpu().numpy()[0])
+        wts.append(w.cpu().numpy()[0])
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert M.moe_check_status(ws_p) == M.MOE_OK and M.moe_check_status(ws_d) == M.MOE_OK
+    preds, wts = np.stack(preds), np.stack(wts)
+    ref = oracle.prerouter(head_cpu, x[:N - 1], cur[:N - 1], prev[:N - 1], k)
+    parity.check_routing(ref, {"idx": preds, "w": wts}, k, label="staged prediction")
+    so = S.stage(preds.tolist(), NS)
+    n_loads = 0
+    for t in range(N - 1):
+        assert steps[t]["slot"].tolist() == so["slots"][t], t
+        assert list(zip(steps[t]["load_expert"].tolist(), steps[t]["load_slot"].tolist())) == so["loads"][t], t
+        n_loads += len(so["loads"][t])
+        parity.check_y(layer, x[t + 1:t + 2], preds[t][None], wts[t][None], ys[t].cpu().numpy(), cfg.qbits)
+    assert n_loads < (N - 1) * k  # sticky slots: some predicted experts were staged already
+    for s_, e in enumerate(st.expert_of):
+        if e >= 0:
+            for n in NAMES:
+                assert torch.equal(pool[n][s_].cpu(), host[n][e]), (s_, int(e), n)
