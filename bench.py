@@ -15,8 +15,9 @@ the same resident weights: the batched decode sweep (T = 1..64), residency
 substitution with int4 experts (T = 1, 16) and prefill (T = 2048, 16384), each
 with its roofline, the CPU oracle's rate on a bounded sample, and the clocks
 seen while it ran; then the shared expert with its unmerged LoRA and the
-prerouter head (T = 1, 16), and the expert cache with miss fetch and
-background admission (512 experts, a quarter cached in HBM).
+prerouter head (T = 1, 16), the expert cache with miss fetch and
+background admission (512 experts, a quarter cached in HBM), and the
+prerouter's prediction staged one token ahead through a slot table.
 
 Prints ONE JSON line (rank 0). With --impl reference the CPU oracle is timed on
 a bounded sample of the headline workload instead.
@@ -907,6 +908,95 @@ def run_expert_cache(args, dev, n_tok: int = 96, warm: int = 16, L: int = 2):
     return out
 
 
+def run_staged(args, dev, n_tok: int = 64, warm: int = 8):
+    """Prediction-as-routing through the staged slot table (xyznot.com Edge0
+    page: prerouter; glossary: staged decode, incremental sticky-slot stack)
+    on the 256-expert top-8 int8 layer: all experts in pinned host memory, a
+    pool of 2k = 16 HBM slots. Per token t: the prerouter predicts token
+    t+1's routing, the changed slots are loaded on a copy stream, and token
+    t+1 is decoded from the pool once they are in. The staging waits for the
+    prediction on the host, so the time is wall clock around the token loop."""
+    import numpy as np
+    import moe_routed_expert_route_gb300 as M
+    import oracle
+    cfg = W.CONFIGS[1]
+    k, NS, H = cfg.k, 2 * cfg.k, 512
+    names = _EXPERT_TENSORS
+    hbm, _, _, kind = peaks()
+    lw = W.make_layer(cfg, 1, dev)
+    host = {n: lw[n].cpu().pin_memory() for n in names}
+    del lw
+    torch.cuda.empty_cache()
+    pool = {n: torch.zeros((NS,) + tuple(host[n].shape[1:]), dtype=host[n].dtype, device=dev) for n in names}
+    hx, px = M.Experts.from_layer(host, cfg.qbits), M.Experts.from_layer(pool, cfg.qbits)
+    head = W.make_prerouter(cfg, 0, H=H, device=dev)
+    pre = M.Prerouter.from_dict(head, k)
+    T = n_tok + warm + 1
+    x = W.make_tokens(cfg, T, 13, dev)
+    cur, prev = W.make_routing_history(cfg, T, stream=13, device=dev)
+    st = M.StageTable(cfg.E, NS, k)
+    cs = torch.cuda.Stream(dev)
+    ev = torch.cuda.Event()
+    ev.record()
+    scratch = torch.zeros(2 * k, dtype=torch.int32).pin_memory()
+    slot_bufs = [torch.empty(k, dtype=torch.int32, device=dev) for _ in range(2)]
+    idx_bufs = [torch.empty(1, k, dtype=torch.int32, device=dev) for _ in range(2)]
+    w_bufs = [torch.empty(1, k, device=dev) for _ in range(2)]
+    y = torch.empty(1, cfg.D, device=dev)
+    ws_p = M.workspace(M.MOE_OP_PREROUTE, 1, k, cfg.E, cfg.D, H, dev)
+    ws_d = M.workspace(M.MOE_OP_DECODE, 1, k, NS, cfg.D, cfg.F, dev)
+    loads = [0]
+
+    def token(t, count):
+        b = t % 2
+        M.moe_preroute(pre, x[t:t + 1], cur[t:t + 1], prev[t:t + 1], idx_bufs[b], w_bufs[b], None, ws_p)
+        step = M.moe_stage_prediction(st, hx, px, idx_bufs[b][0], slot_bufs[b], scratch, None, cs, ev)
+        torch.cuda.current_stream().wait_event(ev)
+        M.moe_decode(px, x[t + 1:t + 2], slot_bufs[b].view(1, k), w_bufs[b], y, None, ws_d)
+        if count:
+            loads[0] += len(step["load_expert"])
+    for t in range(warm):
+        token(t, False)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        t0 = time.perf_counter()
+        for t in range(warm, warm + n_tok):
+            token(t, True)
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+    assert M.moe_check_status(ws_p) == 0 and M.moe_check_status(ws_d) == 0
+    per_expert = W.routed_bytes_per_expert(cfg)
+    us_tok = el / n_tok * 1e6
+    # the oracle on a sample: prerouter and the MoE on the predicted experts
+    ns = 2
+    hh = {n: v.cpu() for n, v in head.items()}
+    t1 = time.perf_counter()
+    r = oracle.prerouter(hh, x[:ns].cpu(), cur[:ns].cpu(), prev[:ns].cpu(), k)
+    for t in range(ns):
+        sub = {n: host[n][torch.from_numpy(r["idx"][t].astype("int64"))] for n in names}
+        oracle.moe(sub, x[t + 1:t + 2].cpu(), np.arange(k, dtype=np.int32)[None], r["w"][t:t + 1],
+                   cfg.qbits, nthreads=os.cpu_count() or 1, compact=False)
+    el_o = time.perf_counter() - t1
+    out = {"workload": "staged prediction: 1 token, E=256 top-8 D=2048 F=768 int8 layer in pinned host memory, "
+                       "16 HBM slots; prerouter (input 2560, hidden 512) one token ahead, changed slots loaded "
+                       "on a copy stream, decode from the pool",
+           "T": 1, "unit": "tokens/s", "tokens_per_s": round(n_tok / el, 2), "us_per_token": round(us_tok, 2),
+           "loads_per_token": round(loads[0] / n_tok, 3),
+           "host_to_device_gbs": round(loads[0] * per_expert / el / 1e9, 2),
+           "roofline": roofline("hbm", k * per_expert / (us_tok * 1e-6) / 1e9, hbm, "GB/s",
+                                "preroute + host staging + copies + decode (wall clock per token)",
+                                {"peak_kind": kind, "note": "decoded expert bytes per token over the wall-clock "
+                                 "time of a token, which includes the host round trip for the staging"}),
+           "cpu_baseline": {"value": round(ns / el_o, 4), "unit": "tokens/s", "cores": os.cpu_count() or 1,
+                            "kind": "oracle", "sample": f"prerouter and MoE on the predicted experts for {ns} tokens, "
+                                                        f"{el_o:.1f} s"},
+           "timing": "wall clock (perf_counter) around the token loop, device synchronised at its end",
+           "clocks": clk.summary()}
+    del pool, host
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -929,7 +1019,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         extra["replay"], extra["substitution"] = run_substitution(args, dev)
-        for key, fn in (("edge0", run_edge0), ("expert_cache", run_expert_cache)):
+        for key, fn in (("edge0", run_edge0), ("expert_cache", run_expert_cache), ("staged_prediction", run_staged)):
             try:
                 extra[key] = fn(args, dev)
             except Exception as e:  # reported, never at the cost of the line above
