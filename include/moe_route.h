@@ -20,15 +20,17 @@
  *            (num_experts, output_dims, input_dims) layout of the lilting.ch
  *            article, section "warm-up vs mmap cache")
  *
- * Conventions for every entry point (moe_replay, host code, takes host arrays
- * and has no stream or workspace):
+ * Conventions for every entry point:
  *  - All array arguments are DEVICE pointers owned by the caller; descriptor
  *    structs are host memory read during the call only. The library allocates
  *    nothing and keeps no state between calls; it is reentrant as long as two
  *    concurrent calls do not share a workspace.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Work is enqueued asynchronously; outputs are valid once the stream reaches
- *    them. Launches use programmatic dependent launch between the library's
+ *    them. Two calls decide on the host and wait for their stream once:
+ *    moe_cached_layer (for the router's probabilities) and
+ *    moe_stage_prediction (for the predicted ids). The host-code calls
+ *    (moe_replay, moe_cache_plan, moe_stage_plan) take host arrays only. Launches use programmatic dependent launch between the library's
  *    own kernels, so they can be captured into a CUDA graph.
  *  - Synchronous argument checks return MOE_ERR_INVALID_ARG / MOE_ERR_WORKSPACE
  *    / MOE_ERR_UNSUPPORTED before anything is launched. A failed launch returns

@@ -31,12 +31,11 @@ DEV = "cuda"
 REL_TOL = parity.REL_TOL
 
 
-def _to(d: dict, dev):
-    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-
 # Inputs are drawn on the CPU and moved to the device, so that they are the
 # same wherever the test runs (and the near ties among them can be counted
 # without a GPU: none at the shapes below).
+def _to(d: dict, dev):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
 def gpu_shared(se: dict, x: torch.Tensor, y0=None):
