@@ -407,9 +407,11 @@ typedef struct {
  *   expert, slot  the expert serving each routed slot (a resident stand-in for
  *                 a substituted one) and the pool slot it is read from
  *   w             the routing weight of each routed slot
- *   flag          0 hit; 1 fetched by the rule and cached; 2 substituted;
- *                 3 fetched for want of a stand-in and cached; 4 fetched
- *                 into its transient slot (every cached expert in use)
+ *   flag          0 hit; 1 fetched and cached; 2 substituted; 4 fetched
+ *                 into its transient slot (every cached expert in use; a
+ *                 miss left without a stand-in always ends here, as stand-ins
+ *                 and evictions come from the same cached experts); 3 is
+ *                 not used
  *   fetch_*       the n_fetch synchronous fetches (expert, slot)
  *   admit_*       the n_admit background admissions (expert, slot)
  *   mass          routing weight served by stand-ins */

@@ -228,7 +228,7 @@ extern "C" moe_status_t moe_cache_plan(moe_cache_t* c, const float* p, const moe
         if (rep < 0) {  // fetched: into a victim's slot, else into the transient slot S + r
             const int s = enter(c, in_use, e);
             st->slot[r] = s >= 0 ? s : S + r;
-            st->flag[r] = s < 0 ? 4 : (want ? 1 : 3);
+            st->flag[r] = s < 0 ? 4 : 1;
             st->fetch_expert[st->n_fetch] = e;
             st->fetch_slot[st->n_fetch] = st->slot[r];
             st->n_fetch++;

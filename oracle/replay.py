@@ -86,8 +86,10 @@ def replay(probs, k, policy, threshold=0.15, admit_mass=0.0, t_layer_us=0.0, t_f
             busy = set(chosen)
             fetched_here = 0
             # per slot: the expert that serves it, and how (0 hit; 1 fetched
-            # by the rule and cached; 2 substituted; 3 fetched for want of a
-            # stand-in and cached; 4 fetched, not cached: nothing evictable)
+            # and cached; 2 substituted; 4 fetched, not cached: nothing
+            # evictable). Stand-ins and evictions are drawn from the same
+            # experts (cached, not used by the token), so a miss fetched for
+            # want of a stand-in always takes 4.
             used = list(chosen)
             flags = [0] * k
             admitted = []
@@ -107,8 +109,7 @@ def replay(probs, k, policy, threshold=0.15, admit_mass=0.0, t_layer_us=0.0, t_f
                         stand_in = max(pool, key=lambda c: (p[c], -c))
                 if stand_in is None:
                     fetched_here += 1
-                    entered = insert(l, e, busy)
-                    flags[r] = (1 if want else 3) if entered else 4
+                    flags[r] = 1 if insert(l, e, busy) else 4
                     continue
                 busy.add(stand_in)
                 used[r] = stand_in

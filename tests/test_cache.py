@@ -48,7 +48,8 @@ def _check_slots(cache: M.ExpertCache, d: dict):
             # served from the cache: the slot holds the serving expert
             assert 0 <= d["slot"][r] < S
             assert cache.expert_of[d["slot"][r]] == d["expert"][r]
-        if d["flag"][r] in (1, 3, 4):
+        assert d["flag"][r] in (0, 1, 2, 4)
+        if d["flag"][r] in (1, 4):
             fetched.append((int(d["expert"][r]), int(d["slot"][r])))
     assert list(zip(d["fetch_expert"].tolist(), d["fetch_slot"].tolist())) == fetched
     for e, s_ in zip(d["admit_expert"], d["admit_slot"]):
