@@ -530,18 +530,19 @@ def run_substitution(args, dev):
     ntok = 4
     xs = W.make_tokens(cfg, (ntok + 1) * L, 9, "cpu").double().numpy().reshape(ntok + 1, L, 1, -1)
 
-    def token(i):
+    def token(i, threads=nth):
         el = 0.0
         for l in range(L):
             t0 = time.perf_counter()
             r = oracle.router(xs[i, l], host[l][0], host[l][1], k)
             s = oracle.substitute(r["probs32"], r["idx"], r["w"], hmask[l], cfg.threshold)
             el += time.perf_counter() - t0
-            el += timed_oracle_moe(layers[l], xs[i, l], s["idx"], s["w"], cfg.qbits, nth)[0]
+            el += timed_oracle_moe(layers[l], xs[i, l], s["idx"], s["w"], cfg.qbits, threads)[0]
         return el
 
     token(0)
     el = sum(token(i) for i in range(1, ntok + 1))
+    el1 = token(1, threads=1)  # one token on one core
     t_layer = next(r["us_per_layer"] for r in res if r["T"] == 1)
     replay = run_replay(args, dev, cfg, routers, masks, t_layer)
     del layers, routers, experts
@@ -552,7 +553,9 @@ def run_substitution(args, dev):
             "cpu_baseline": {"value": round(ntok / el, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
                              "sample": f"{ntok} tokens x {L} layers (router + substitution + routed experts, on host "
                                        f"copies of the routed experts' rows, copies not timed) after "
-                                       f"1 warm-up token, {el:.1f} s"},
+                                       f"1 warm-up token, {el:.1f} s",
+                             "single_thread": {"value": round(1 / el1, 4), "unit": "tokens/s", "cores": 1,
+                                               "sample": f"1 token x {L} layers, {el1:.1f} s"}},
             "clocks": clk.summary()}
 
 
@@ -674,6 +677,12 @@ def run_prefill(args, dev, stack, T):
     r = oracle.router(xs, wr, br, cfg.k)
     el = time.perf_counter() - t0
     el += timed_oracle_moe(layers[0], xs, r["idx"], r["w"], cfg.qbits, nth)[0]
+    # and 2 of those tokens on one core
+    ns1 = 2
+    t0 = time.perf_counter()
+    r1 = oracle.router(xs[:ns1], wr, br, cfg.k)
+    el1 = time.perf_counter() - t0
+    el1 += timed_oracle_moe(layers[0], xs[:ns1], r1["idx"], r1["w"], cfg.qbits, 1)[0]
     del ws
     torch.cuda.empty_cache()
     return {"workload": f"prefill T={T} E=256 top-8 D=2048 F=768 int8 (fp16 tensor-core operands)",
@@ -690,7 +699,9 @@ def run_prefill(args, dev, stack, T):
                                   "note": "fp16 operands: the bf16 peak applies (same nominal rate)"}),
             "cpu_baseline": {"value": round(ns / el, 4), "unit": "tokens/s", "cores": nth, "kind": "oracle",
                              "sample": f"{ns} of the {T} tokens through one layer (on host copies of the routed "
-                                       f"experts' rows, copies not timed), {el:.1f} s"},
+                                       f"experts' rows, copies not timed), {el:.1f} s",
+                             "single_thread": {"value": round(ns1 / el1, 4), "unit": "tokens/s", "cores": 1,
+                                               "sample": f"{ns1} of those tokens through one layer, {el1:.1f} s"}},
             "clocks": clk.summary()}
 
 
