@@ -1,5 +1,7 @@
 """Host-side checks of the seeded synthetic inputs (no GPU): the shapes and
 formats the layer consumes, the documented distributions, and determinism."""
+import dataclasses
+
 import numpy as np
 import torch
 
@@ -70,3 +72,47 @@ def test_quantised_codes_stay_in_range():
     hi = (((packed >> 4) & 0xF) ^ 8) - 8
     assert lo.min() >= -7 and lo.max() <= 7 and hi.min() >= -7 and hi.max() <= 7
     assert L["gate_q"].shape[-1] == cfg4.D // 2
+
+
+def test_shared_expert_generator():
+    sc = W.SHARED_CONFIGS["decode"]
+    a = W.make_shared_expert(sc, 0)
+    b = W.make_shared_expert(sc, 0)
+    D, F, r = sc.D, sc.F, sc.rank
+    assert a["gate_q"].shape == (F, D // 2) and a["down_q"].shape == (D, F // 2)  # int4, packed
+    assert a["gate_s"].shape == (F, D // 32) and a["gate_s"].dtype == torch.float16
+    assert a["gate_A"].shape == (r, D) and a["down_A"].shape == (r, F)
+    assert a["gate_B"].shape == (F, r) and a["down_B"].shape == (D, r)
+    assert a["gate_A"].dtype == torch.bfloat16 and a["scale"] == sc.alpha / r
+    for n in ("gate_q", "gate_s", "down_q", "gate_A", "up_B", "down_B"):
+        assert torch.equal(a[n], b[n])  # seeded
+    assert not torch.equal(a["gate_A"], W.make_shared_expert(sc, 1)["gate_A"])
+    # the adapters' delta (alpha/r) B A has an RMS of about 1e-3, the size the
+    # Edge0 page gives for its recovery LoRA (below one 4-bit step)
+    for p in ("gate", "up", "down"):
+        delta = a["scale"] * (a[p + "_B"].double() @ a[p + "_A"].double())
+        rms = float(delta.pow(2).mean().sqrt())
+        assert 0.8e-3 < rms < 1.25e-3, (p, rms)
+    z = W.make_shared_expert(dataclasses.replace(sc, rank=0), 0)
+    assert z["gate_A"] is None and z["scale"] == 0.0
+
+
+def test_prerouter_generator_warm_starts_from_the_next_router():
+    cfg = W.CONFIGS[1]
+    h = W.make_prerouter(cfg, 3, H=512)
+    E, D = cfg.E, cfg.D
+    assert h["fc1"].shape == (512, D + 2 * E) and h["fc2"].shape == (E, 512) and h["L"].shape == (E, D + 2 * E)
+    Wr, bias = W.make_router(cfg, 4)
+    assert torch.equal(h["L"][:, :D], Wr) and torch.equal(h["bias"], bias)
+    assert torch.equal(W.make_layer(W.CONFIGS[0], 0)["Wr"], W.make_router(W.CONFIGS[0], 0)[0])
+    assert torch.equal(h["fc1"], W.make_prerouter(cfg, 3, H=512)["fc1"])
+
+
+def test_routing_history_generator():
+    cfg = W.CONFIGS[1]
+    cur, prev = W.make_routing_history(cfg, 20, stream=2)
+    assert cur.shape == (20, cfg.k) and cur.dtype == torch.int32
+    for row in torch.cat([cur, prev]).tolist():
+        assert len(set(row)) == cfg.k and all(0 <= e < cfg.E for e in row)
+    _, none = W.make_routing_history(cfg, 5, absent_prev=True)
+    assert (none == -1).all()
