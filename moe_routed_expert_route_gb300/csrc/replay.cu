@@ -36,26 +36,36 @@
 
 namespace {
 
+// One layer's cache: the caller's residency flags, frequencies and
+// accumulated mass, plus the list of resident experts (kept in step with the
+// flags, in no particular order) so that stand-in and eviction searches visit
+// the residents only.
 struct LayerState {
     uint8_t* res;
     int32_t* freq;
     double* acc;
+    std::vector<int> list;  // resident experts
+    std::vector<int> pos;   // position of e in list, or -1
 };
 
 // The resident expert to evict: lowest frequency, lower id on ties, not in use.
-int victim(const LayerState& s, const std::vector<uint8_t>& in_use, int E) {
+int victim(const LayerState& s, const std::vector<uint8_t>& in_use) {
     int best = -1;
-    for (int e = 0; e < E; e++) {
-        if (!s.res[e] || in_use[e]) continue;
-        if (best < 0 || s.freq[e] < s.freq[best]) best = e;
+    for (const int e : s.list) {
+        if (in_use[e]) continue;
+        if (best < 0 || s.freq[e] < s.freq[best] || (s.freq[e] == s.freq[best] && e < best)) best = e;
     }
     return best;
 }
 
 // e enters the cache (evicting a victim); returns false when nothing can go.
-bool enter(LayerState& s, std::vector<uint8_t>& in_use, int E, int e) {
-    const int v = victim(s, in_use, E);
+bool enter(LayerState& s, const std::vector<uint8_t>& in_use, int e) {
+    const int v = victim(s, in_use);
     if (v < 0) return false;
+    const int at = s.pos[v];
+    s.list[at] = e;
+    s.pos[e] = at;
+    s.pos[v] = -1;
     s.res[v] = 0;
     s.res[e] = 1;
     return true;
@@ -79,32 +89,57 @@ extern "C" moe_status_t moe_replay(int N, int L, int E, int k, const float* prob
     const bool admit = pol->admit_mass > 0.f && std::isfinite(pol->admit_mass);
     const double beta = pol->admit_mass, thr = pol->threshold;
 
-    std::vector<int> idx(k);
+    std::vector<LayerState> layers(L);
+    for (int l = 0; l < L; l++) {
+        LayerState& s = layers[l];
+        s.res = resident + (size_t)l * E;
+        s.freq = freq + (size_t)l * E;
+        s.acc = acc + (size_t)l * E;
+        s.pos.assign(E, -1);
+        for (int e = 0; e < E; e++)
+            if (s.res[e]) {
+                s.pos[e] = (int)s.list.size();
+                s.list.push_back(e);
+            }
+    }
+    std::vector<int> idx(k), used;
     std::vector<double> w(k);
-    std::vector<uint8_t> taken(E), in_use(E);
+    std::vector<uint8_t> taken(E, 0), in_use(E, 0);
+    used.reserve(2 * (size_t)k);
     for (int t = 0; t < N; t++) {
         double time = 0.0, mass = 0.0;
         int nf = 0, ns = 0, na = 0;
         for (int l = 0; l < L; l++) {
             const float* p = probs + ((size_t)t * L + l) * E;
-            LayerState s = {resident + (size_t)l * E, freq + (size_t)l * E, acc + (size_t)l * E};
-            // 1. top-k by repeated selection of the largest untaken probability
-            for (int e = 0; e < E; e++) taken[e] = 0;
-            for (int r = 0; r < k; r++) {
-                int b = -1;
-                for (int e = 0; e < E; e++)
-                    if (!taken[e] && (b < 0 || p[e] > p[b])) b = e;
-                taken[b] = 1;
-                idx[r] = b;
+            LayerState& s = layers[l];
+            // 1. top-k in one pass over the experts in id order, keeping the
+            //    best k sorted by probability; an expert enters or moves up
+            //    only past strictly smaller values, so equal values keep the
+            //    lower id first
+            int n = 0;
+            float kth = 0.f;  // the k-th best so far, once k are kept
+            for (int e = 0; e < E; e++) {
+                const float v = p[e];
+                if (n == k && !(v > kth)) continue;
+                int at = n < k ? n++ : k - 1;
+                while (at > 0 && v > p[idx[at - 1]]) {
+                    idx[at] = idx[at - 1];
+                    at--;
+                }
+                idx[at] = e;
+                if (n == k) kth = p[idx[k - 1]];
             }
             double sum = 0.0;
             for (int r = 0; r < k; r++) sum += (double)p[idx[r]];
             for (int r = 0; r < k; r++) w[r] = sum > 0.0 ? (double)p[idx[r]] / sum : 0.0;
-            // 2. frequencies; the routed experts are in use
-            for (int e = 0; e < E; e++) in_use[e] = 0;
+            // 2. frequencies; the routed experts are taken and in use (the
+            //    flags set here are cleared again at the end of the layer)
+            used.clear();
             for (int r = 0; r < k; r++) {
                 s.freq[idx[r]] += 1;
+                taken[idx[r]] = 1;
                 in_use[idx[r]] = 1;
+                used.push_back(idx[r]);
             }
             // 3. the slots in rank order
             int lf = 0;
@@ -115,29 +150,31 @@ extern "C" moe_status_t moe_replay(int N, int L, int E, int k, const float* prob
                 if (pol->policy == MOE_POLICY_FETCH_ALL) fetch = true;
                 else if (pol->policy == MOE_POLICY_FIRST_CHOICE) fetch = r == 0;
                 else fetch = r == 0 || w[r] >= thr;
-                int rep = -1;
+                int rep = -1;  // the stand-in: the most probable resident not taken, lower id on ties
                 if (!fetch) {
-                    for (int c = 0; c < E; c++)
-                        if (s.res[c] && !taken[c] && (rep < 0 || p[c] > p[rep])) rep = c;
+                    for (const int c : s.list)
+                        if (!taken[c] && (rep < 0 || p[c] > p[rep] || (p[c] == p[rep] && c < rep))) rep = c;
                     if (rep < 0) fetch = true;  // no resident candidate left: the miss is kept
                 }
                 if (fetch) {
                     lf++;
-                    enter(s, in_use, E, e);
+                    enter(s, in_use, e);
                     continue;
                 }
                 taken[rep] = 1;
                 in_use[rep] = 1;
+                used.push_back(rep);
                 ns++;
                 mass += w[r];
                 s.acc[e] += w[r];
                 if (admit && s.acc[e] >= beta && !s.res[e]) {
-                    if (enter(s, in_use, E, e)) {
+                    if (enter(s, in_use, e)) {
                         na++;
                         s.acc[e] = 0.0;
                     }
                 }
             }
+            for (const int e : used) taken[e] = in_use[e] = 0;
             nf += lf;
             time += pol->t_layer_us + lf * pol->t_fetch_us;
         }
