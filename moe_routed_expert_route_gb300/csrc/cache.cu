@@ -182,15 +182,17 @@ extern "C" moe_status_t moe_cache_plan(moe_cache_t* c, const float* p, const moe
     //    sorted by probability; an expert enters or moves up only past strictly
     //    smaller values, so equal values keep the lower id first
     int n = 0;
+    float kth = 0.f;  // the k-th best so far, once k are kept
     for (int e = 0; e < E; e++) {
         const float v = p[e];
-        if (n == k && !(v > p[idx[k - 1]])) continue;
+        if (n == k && !(v > kth)) continue;
         int pos = n < k ? n++ : k - 1;
         while (pos > 0 && v > p[idx[pos - 1]]) {
             idx[pos] = idx[pos - 1];
             pos--;
         }
         idx[pos] = e;
+        if (n == k) kth = p[idx[k - 1]];
     }
     for (int r = 0; r < k; r++) taken[idx[r]] = 1;
     double sum = 0.0;
