@@ -182,3 +182,19 @@ def test_preroute_rejects_bad_arguments_before_launch():
     assert call(head(), cur=null) == M.MOE_ERR_INVALID_ARG
     assert call(head(), T=0) == M.MOE_ERR_INVALID_ARG
     assert call(head(), n=ws - 1) == M.MOE_ERR_WORKSPACE
+
+
+def test_noalloc_size_limits_rejected_before_launch():
+    # moe_layer_noalloc keeps its scratch in a fixed array: E <= 1024 and
+    # k*F <= 32768; beyond either it reports MOE_ERR_WORKSPACE before any
+    # device work (fake, aligned pointers: nothing is dereferenced)
+    lib = L._lib
+
+    def call(E, k, D, F):
+        r = L._Router(E, D, k, L.MOE_BF16, 16, None, 1)
+        ex = L._Experts(E, D, F, L.MOE_Q_INT8_SYM_B32, L.MOE_F16, 16, 16, 16, 16, 16, 16)
+        return lib.moe_layer_noalloc(ctypes.byref(r), ctypes.byref(ex), 16, L.MOE_BF16, 16, 16, None, 16, None,
+                                     None)
+    assert call(1025, 2, 64, 64) == M.MOE_ERR_WORKSPACE
+    assert call(8, 8, 64, 8192) == M.MOE_ERR_WORKSPACE       # k*F = 65536
+    assert call(1025, 2, 48, 64) == M.MOE_ERR_INVALID_ARG     # shape errors come first
